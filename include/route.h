@@ -1,0 +1,166 @@
+/*
+ * libroute -- the per-MoE-layer route step on one GB300 (sm_103a), C ABI.
+ *
+ * The route step of one MoE layer, for `rows` token rows:
+ *
+ *   latent[r, n] = bf16( sum_{k<7168} hidden[r, k] * W_latent[k, n] )   n < 3584
+ *   logits[r, e] =       sum_{k<7168} hidden[r, k] * W_router[k, e]    e < 896
+ *   ids[r, :]    = the 16 experts with the largest logits, in rank order
+ *   weights[r,i] = s_i / sum_j s_j,  s_i = 1 / (1 + exp(-logits[r, ids[r, i]]))
+ *
+ * Every sum is accumulated in FP32 over the full K = 7168 and rounded once
+ * (to BF16 for the latent, kept in FP32 for the logits): "Optionally gather
+ * the Kimi3 prefill latent instead of reducing it", Description, Numerics and
+ * Compile bullets.  896 experts = 56 router columns x 16 ranks: "Use two row
+ * blocks for eight-row Kimi paired gathers", body.  The standalone top-16 and
+ * the 1..20-row decode envelope: "Kimi K3.1 recipe: route 9..20 decode rows
+ * through the pushed pair gather and standalone top-16", commit message.
+ *
+ * Conventions for every entry point:
+ *  - All tensors are dense, row-major, contiguous, owned by the caller and
+ *    resident in device memory of the plan's device (except where a function
+ *    says "host").  BF16 tensors are passed as `void*` (IEEE bfloat16 bits).
+ *  - Weights are stored [K, N]: W_latent [7168, 3584], W_router [7168, 896],
+ *    N contiguous.
+ *  - Every device pointer must be 16-byte aligned (TMA and 16-byte vector
+ *    accesses); otherwise ROUTE_ERR_ALIGN is returned and nothing is launched.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *    enqueued asynchronously; no entry point synchronises the device unless it
+ *    says so.  Forward calls never allocate and may be captured in a CUDA
+ *    graph.
+ *  - A plan holds scratch memory (split-K partials and counters), so one plan
+ *    must not run on two streams at the same time.
+ *  - Errors are status codes; no C++ exception crosses this interface.
+ *    route_last_error() returns a message for the calling thread's last
+ *    failure.
+ */
+#ifndef ROUTE_H
+#define ROUTE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ROUTE_K_HIDDEN 7168
+#define ROUTE_N_LATENT 3584
+#define ROUTE_N_EXPERTS 896
+#define ROUTE_TOPK 16
+#define ROUTE_DECODE_MAX_ROWS 20
+#define ROUTE_PREFILL_MAX_ROWS 65536
+
+typedef enum {
+    ROUTE_OK = 0,
+    ROUTE_ERR_ROWS = 1,           /* rows outside the mode's envelope */
+    ROUTE_ERR_MODE = 2,           /* unknown mode */
+    ROUTE_ERR_NULL = 3,           /* a required pointer is NULL */
+    ROUTE_ERR_ALIGN = 4,          /* a pointer is not 16-byte aligned */
+    ROUTE_ERR_CUDA = 5,           /* a CUDA call failed; see route_last_error() */
+    ROUTE_ERR_DEVICE_TIMEOUT = 6, /* a kernel gave up waiting and returned */
+    ROUTE_ERR_PLAN = 7,           /* the plan cannot run this call */
+    ROUTE_ERR_DEVICE = 8          /* the device is not an sm_103 GPU */
+} route_status;
+
+typedef enum {
+    ROUTE_DECODE = 0,  /* 1..20 rows: weight streaming with split-K over all SMs */
+    ROUTE_PREFILL = 1  /* 1..65536 rows: full-K tensor-core tiles */
+} route_mode;
+
+typedef struct route_plan route_plan; /* opaque */
+
+/*
+ * route_prepare: validate the row envelope and build a plan on `device`.
+ * The plan fixes the launch geometry and the split-K partition (which depend
+ * only on the device's SM count, never on the data or on `rows` within the
+ * envelope) and owns its scratch memory, allocated here.
+ * Decode accepts 1 <= rows <= 20 and rejects anything else with
+ * ROUTE_ERR_ROWS before touching the device -- the envelope is checked at
+ * preparation, loudly, with no fallback ("Kimi K3.1 recipe ...", commit
+ * message: "prepares 1-20 rows or raises at preparation"; Tests: the 21-row
+ * envelope rejection).  Prefill accepts 1 <= rows <= 65536.
+ * On success *out receives the plan; on failure *out is set to NULL.
+ */
+route_status route_prepare(int mode, int rows, int device, route_plan **out);
+
+/* route_destroy: free the plan and its scratch memory (synchronises the
+ * plan's device).  NULL is accepted and ignored. */
+route_status route_destroy(route_plan *plan);
+
+/*
+ * latent_router_forward: steps a1 (latent down projection) and a2 (router
+ * logits) for the plan's `rows`.
+ *   hidden   [rows, 7168] BF16     (read)
+ *   W_latent [7168, 3584] BF16     (read)
+ *   W_router [7168, 896]  BF16     (read)
+ *   latent   [rows, 3584] BF16     (written)  one FP32 full-K sum, rounded once
+ *   logits   [rows, 896]  FP32     (written)  FP32 full-K sum
+ * Decode plans also use the plan's scratch for split-K partials, which are
+ * summed in a fixed order, so results are bitwise reproducible and a row's
+ * bits do not depend on `rows`.
+ */
+route_status latent_router_forward(const route_plan *plan, const void *hidden,
+                                   const void *W_latent, const void *W_router, void *latent,
+                                   float *logits, void *stream);
+
+/*
+ * topk16_select: steps a3 (standalone top-16) and a4 (routing weights).
+ *   logits  [rows, 896] FP32 (read)
+ *   ids     [rows, 16] int32 (written)  largest logit first; equal logits
+ *                                       (-0 == +0) go to the lower expert id;
+ *                                       NaN ranks below every number
+ *   weights [rows, 16] FP32  (written)  s_i / sum_j s_j, s = sigmoid(logit),
+ *                                       evaluated in double, rounded to FP32
+ * ("Kimi K3.1 recipe ...", commit message: "the standalone top-16 selects
+ * their experts"; the routing-weight formula is this library's convention.)
+ */
+route_status topk16_select(const route_plan *plan, const float *logits, int32_t *ids,
+                           float *weights, void *stream);
+
+/*
+ * route_step: the whole route step (a1..a4) for the plan's rows, same
+ * arguments and results as latent_router_forward followed by topk16_select.
+ * Decode plans run it as ONE kernel: the CTA that completes the last router
+ * column tile runs the top-16 for every row.
+ */
+route_status route_step(const route_plan *plan, const void *hidden, const void *W_latent,
+                        const void *W_router, void *latent, float *logits, int32_t *ids,
+                        float *weights, void *stream);
+
+/*
+ * route_step_host: route_step with the per-step tensors in HOST memory.
+ * hidden_host [rows, 7168] BF16 is copied to the device, the step runs, and
+ * latent_host, logits_host, ids_host, weights_host receive the results.
+ * Weights stay device pointers (they are resident model parameters).  The
+ * copies use the plan's device staging buffers (allocated by route_prepare)
+ * and are enqueued on `stream`; the call returns after the stream has
+ * finished (it synchronises `stream`).  Host pointers need no alignment;
+ * page-locked host memory makes the copies faster.
+ */
+route_status route_step_host(const route_plan *plan, const void *hidden_host,
+                             const void *W_latent, const void *W_router, void *latent_host,
+                             float *logits_host, int32_t *ids_host, float *weights_host,
+                             void *stream);
+
+/*
+ * route_device_status: synchronise the plan's device, then report (and clear)
+ * the device-side error word that kernels set instead of hanging: ROUTE_OK
+ * or ROUTE_ERR_DEVICE_TIMEOUT (a bounded wait expired; outputs of that launch
+ * are invalid and the plan's split-K counters have been cleared).
+ */
+route_status route_device_status(const route_plan *plan);
+
+/* Plan properties: rows, mode, launch grid (CTAs) and split-K segments. */
+int route_plan_rows(const route_plan *plan);
+int route_plan_mode(const route_plan *plan);
+int route_plan_grid(const route_plan *plan);
+int route_plan_segments(const route_plan *plan);
+
+/* Message for the calling thread's most recent failure ("" if none). */
+const char *route_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ROUTE_H */

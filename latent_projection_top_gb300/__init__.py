@@ -1,0 +1,251 @@
+"""Python binding of the route library (``libroute``, C ABI in ``include/route.h``).
+
+Argument marshalling only: tensors are checked for dtype, shape, layout and
+device, then their pointers and the CUDA stream are passed to the C entry
+points of the same names.  Every step of the route computation runs in the
+library's CUDA kernels; there is no Python or CPU fallback, and importing the
+package fails loudly if the library has not been built (``build()``).
+
+The route step of one MoE layer (see ``include/route.h``):
+
+* ``latent_router_forward`` -- latent down projection (BF16, one FP32 full-K
+  sum rounded once) and FP32 router logits;
+* ``topk16_select`` -- standalone top-16 with sigmoid-renormalised weights;
+* ``route_step`` -- both, as one kernel for decode plans;
+* ``route_step_host`` -- ``route_step`` with host tensors (copies included).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+K_HIDDEN = 7168
+N_LATENT = 3584
+N_EXPERTS = 896
+TOPK = 16
+DECODE_MAX_ROWS = 20
+PREFILL_MAX_ROWS = 65536
+
+DECODE = 0
+PREFILL = 1
+
+ROUTE_OK = 0
+STATUS_NAMES = {
+    0: "ROUTE_OK", 1: "ROUTE_ERR_ROWS", 2: "ROUTE_ERR_MODE", 3: "ROUTE_ERR_NULL",
+    4: "ROUTE_ERR_ALIGN", 5: "ROUTE_ERR_CUDA", 6: "ROUTE_ERR_DEVICE_TIMEOUT",
+    7: "ROUTE_ERR_PLAN", 8: "ROUTE_ERR_DEVICE",
+}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libroute.so")
+
+# Every symbol the header declares (checked by the CPU tests).
+EXPORTS = (
+    "route_prepare", "route_destroy", "latent_router_forward", "topk16_select", "route_step",
+    "route_step_host", "route_device_status", "route_plan_rows", "route_plan_mode",
+    "route_plan_grid", "route_plan_segments", "route_last_error",
+)
+
+
+class RouteError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    from . import builder as _b
+    return _b.build(force=force)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded ``libroute.so``; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RouteError(5, f"{LIB_PATH} is missing: the CUDA library must be built "
+                                "(latent_projection_top_gb300.build())")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32 = ctypes.c_void_p, ctypes.c_int
+        L.route_prepare.argtypes = [i32, i32, i32, ctypes.POINTER(vp)]
+        L.route_destroy.argtypes = [vp]
+        L.latent_router_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp]
+        L.topk16_select.argtypes = [vp, vp, vp, vp, vp]
+        L.route_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.route_step_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.route_device_status.argtypes = [vp]
+        for f in ("route_plan_rows", "route_plan_mode", "route_plan_grid", "route_plan_segments"):
+            getattr(L, f).argtypes = [vp]
+            getattr(L, f).restype = i32
+        L.route_last_error.argtypes = []
+        L.route_last_error.restype = ctypes.c_char_p
+        for f in ("route_prepare", "route_destroy", "latent_router_forward", "topk16_select",
+                  "route_step", "route_step_host", "route_device_status"):
+            getattr(L, f).restype = i32
+        _lib = L
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != ROUTE_OK:
+        msg = lib().route_last_error().decode(errors="replace")
+        raise RouteError(status, msg)
+
+
+class Plan:
+    """A prepared route plan (``route_prepare``): mode, rows, device, launch
+    geometry and the plan's scratch memory.  Use as a context manager or call
+    ``close()``."""
+
+    def __init__(self, mode: int, rows: int, device: int = 0):
+        h = ctypes.c_void_p()
+        _check(lib().route_prepare(int(mode), int(rows), int(device), ctypes.byref(h)))
+        self._h = h
+        self.mode = int(mode)
+        self.rows = int(rows)
+        self.device = int(device)
+
+    @property
+    def handle(self) -> ctypes.c_void_p:
+        if self._h is None or not self._h.value:
+            raise RouteError(7, "plan is closed")
+        return self._h
+
+    @property
+    def grid(self) -> int:
+        return lib().route_plan_grid(self.handle)
+
+    @property
+    def segments(self) -> int:
+        return lib().route_plan_segments(self.handle)
+
+    def close(self) -> None:
+        if self._h is not None and self._h.value:
+            lib().route_destroy(self._h)
+        self._h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def route_prepare(mode: int, rows: int, device: int = 0) -> Plan:
+    return Plan(mode, rows, device)
+
+
+# ---- marshalling helpers ---------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dev_tensor(t, name, shape, dtypes, device):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda" or t.device.index != device:
+        raise ValueError(f"{name} must be on cuda:{device}")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}; expected one of {dtypes}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}; expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _host_tensor(t, name, shape, dtypes):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+        raise TypeError(f"{name} must be a CPU torch.Tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}; expected one of {dtypes}")
+    if tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous with shape {tuple(shape)}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _bf16_types():
+    torch = _torch()
+    return (torch.bfloat16, torch.int16, torch.uint16) if hasattr(torch, "uint16") else \
+        (torch.bfloat16, torch.int16)
+
+
+def _stream(stream, device):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _proj_ptrs(plan, hidden, W_latent, W_router, latent, logits):
+    torch = _torch()
+    R, d = plan.rows, plan.device
+    bf = _bf16_types()
+    return (_dev_tensor(hidden, "hidden", (R, K_HIDDEN), bf, d),
+            _dev_tensor(W_latent, "W_latent", (K_HIDDEN, N_LATENT), bf, d),
+            _dev_tensor(W_router, "W_router", (K_HIDDEN, N_EXPERTS), bf, d),
+            _dev_tensor(latent, "latent", (R, N_LATENT), bf, d),
+            _dev_tensor(logits, "logits", (R, N_EXPERTS), (torch.float32,), d))
+
+
+def _topk_ptrs(plan, ids, weights):
+    torch = _torch()
+    R, d = plan.rows, plan.device
+    return (_dev_tensor(ids, "ids", (R, TOPK), (torch.int32,), d),
+            _dev_tensor(weights, "weights", (R, TOPK), (torch.float32,), d))
+
+
+# ---- the C entry points ------------------------------------------------------
+
+def latent_router_forward(plan: Plan, hidden, W_latent, W_router, latent, logits,
+                          stream=None) -> None:
+    p = _proj_ptrs(plan, hidden, W_latent, W_router, latent, logits)
+    _check(lib().latent_router_forward(plan.handle, *p, _stream(stream, plan.device)))
+
+
+def topk16_select(plan: Plan, logits, ids, weights, stream=None) -> None:
+    torch = _torch()
+    lg = _dev_tensor(logits, "logits", (plan.rows, N_EXPERTS), (torch.float32,), plan.device)
+    i, w = _topk_ptrs(plan, ids, weights)
+    _check(lib().topk16_select(plan.handle, lg, i, w, _stream(stream, plan.device)))
+
+
+def route_step(plan: Plan, hidden, W_latent, W_router, latent, logits, ids, weights,
+               stream=None) -> None:
+    p = _proj_ptrs(plan, hidden, W_latent, W_router, latent, logits)
+    i, w = _topk_ptrs(plan, ids, weights)
+    _check(lib().route_step(plan.handle, *p, i, w, _stream(stream, plan.device)))
+
+
+def route_step_host(plan: Plan, hidden_host, W_latent, W_router, latent_host, logits_host,
+                    ids_host, weights_host, stream=None) -> None:
+    torch = _torch()
+    R, d = plan.rows, plan.device
+    bf = _bf16_types()
+    args = (_host_tensor(hidden_host, "hidden_host", (R, K_HIDDEN), bf),
+            _dev_tensor(W_latent, "W_latent", (K_HIDDEN, N_LATENT), bf, d),
+            _dev_tensor(W_router, "W_router", (K_HIDDEN, N_EXPERTS), bf, d),
+            _host_tensor(latent_host, "latent_host", (R, N_LATENT), bf),
+            _host_tensor(logits_host, "logits_host", (R, N_EXPERTS), (torch.float32,)),
+            _host_tensor(ids_host, "ids_host", (R, TOPK), (torch.int32,)),
+            _host_tensor(weights_host, "weights_host", (R, TOPK), (torch.float32,)))
+    _check(lib().route_step_host(plan.handle, *args, _stream(stream, d)))
+
+
+def route_device_status(plan: Plan) -> None:
+    """Synchronise and raise RouteError if a kernel of this plan gave up waiting."""
+    _check(lib().route_device_status(plan.handle))

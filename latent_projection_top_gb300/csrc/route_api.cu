@@ -1,0 +1,426 @@
+// C ABI of the route library: plan preparation (envelope checks, launch
+// geometry, split-K partition, scratch), argument validation and launches.
+// Every check happens on the host before anything is enqueued; failures are
+// status codes plus a per-thread message.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "common.cuh"
+#include "route.h"
+
+using namespace route;
+
+struct route_plan {
+    int mode;
+    int rows;
+    int device;
+    int bn;
+    int grid;
+    int segments;
+    ProjArgs base;            // filled at prepare; per-call pointers added at launch
+    float *ws;                // decode split-K partials
+    unsigned *words;          // counters [kColTiles + 1] then status, zeroed at prepare
+    uint8_t *staging;         // device staging for route_step_host
+    size_t staging_bytes;
+};
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+route_status fail(route_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+route_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(ROUTE_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+std::mutex g_encode_mu;
+EncodeTiledFn g_encode = nullptr;
+
+route_status get_encode(EncodeTiledFn *out) {
+    std::lock_guard<std::mutex> lk(g_encode_mu);
+    if (!g_encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+            return fail(ROUTE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    *out = g_encode;
+    return ROUTE_OK;
+}
+
+// 2-D BF16 tensor map, 128-byte swizzle, zero fill out of bounds.
+route_status encode_2d(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer,
+                       uint32_t box_inner, uint32_t box_outer, const char *what) {
+    EncodeTiledFn enc;
+    route_status st = get_encode(&enc);
+    if (st != ROUTE_OK) return st;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ROUTE_ERR_CUDA, "tensor map for %s rejected (CUresult %d)", what, (int)r);
+    return ROUTE_OK;
+}
+
+struct DeviceGuard {
+    int prev = -1;
+    bool changed = false;
+    cudaError_t err = cudaSuccess;
+    explicit DeviceGuard(int dev) {
+        err = cudaGetDevice(&prev);
+        if (err == cudaSuccess && prev != dev) {
+            err = cudaSetDevice(dev);
+            changed = (err == cudaSuccess);
+        }
+    }
+    ~DeviceGuard() {
+        if (changed) cudaSetDevice(prev);
+    }
+};
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+void free_plan(route_plan *p) {
+    if (!p) return;
+    if (p->ws) cudaFree(p->ws);
+    if (p->words) cudaFree(p->words);
+    if (p->staging) cudaFree(p->staging);
+    delete p;
+}
+
+// Staging layout for route_step_host: hidden, latent, logits, ids, weights.
+struct Staging {
+    void *hidden, *latent;
+    float *logits, *weights;
+    int32_t *ids;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+Staging staging_of(const route_plan *p) {
+    size_t r = (size_t)p->rows;
+    uint8_t *b = p->staging;
+    Staging s;
+    s.hidden = b;
+    b += align256(r * kHidden * 2);
+    s.latent = b;
+    b += align256(r * kLatent * 2);
+    s.logits = reinterpret_cast<float *>(b);
+    b += align256(r * kExperts * 4);
+    s.ids = reinterpret_cast<int32_t *>(b);
+    b += align256(r * kTopK * 4);
+    s.weights = reinterpret_cast<float *>(b);
+    return s;
+}
+
+size_t staging_size(int rows) {
+    size_t r = (size_t)rows;
+    return align256(r * kHidden * 2) + align256(r * kLatent * 2) + align256(r * kExperts * 4) +
+           align256(r * kTopK * 4) + align256(r * kTopK * 4);
+}
+
+route_status check_plan(const route_plan *p) {
+    if (!p) return fail(ROUTE_ERR_NULL, "plan is NULL");
+    return ROUTE_OK;
+}
+
+route_status launch_proj(const route_plan *p, const void *hidden, const void *W_latent,
+                         const void *W_router, void *latent, float *logits, int32_t *ids,
+                         float *weights, int fuse, cudaStream_t stream) {
+    CUtensorMap mh, ml, mr;
+    route_status st;
+    if ((st = encode_2d(&mh, hidden, kHidden, (uint64_t)p->rows, kKBlock, (uint32_t)p->bn,
+                        "hidden")) != ROUTE_OK)
+        return st;
+    if ((st = encode_2d(&ml, W_latent, kLatent, kHidden, 64, kKBlock, "W_latent")) != ROUTE_OK)
+        return st;
+    if ((st = encode_2d(&mr, W_router, kExperts, kHidden, 64, kKBlock, "W_router")) != ROUTE_OK)
+        return st;
+    ProjArgs a = p->base;
+    a.latent = static_cast<uint16_t *>(latent);
+    a.logits = logits;
+    a.ids = ids;
+    a.weights = weights;
+    a.fuse_topk = fuse;
+    cudaError_t e = proj_launch(p->bn, mh, ml, mr, a, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "projection kernel launch");
+    return ROUTE_OK;
+}
+
+route_status check_forward_args(const route_plan *p, const void *hidden, const void *W_latent,
+                                const void *W_router, const void *latent, const float *logits) {
+    route_status st = check_plan(p);
+    if (st != ROUTE_OK) return st;
+    if (!hidden || !W_latent || !W_router || !latent || !logits)
+        return fail(ROUTE_ERR_NULL, "hidden, W_latent, W_router, latent and logits must be non-NULL");
+    if (!aligned16(hidden) || !aligned16(W_latent) || !aligned16(W_router) || !aligned16(latent) ||
+        !aligned16(logits))
+        return fail(ROUTE_ERR_ALIGN, "every device pointer must be 16-byte aligned");
+    return ROUTE_OK;
+}
+
+route_status check_topk_args(const route_plan *p, const float *logits, const int32_t *ids,
+                             const float *weights) {
+    route_status st = check_plan(p);
+    if (st != ROUTE_OK) return st;
+    if (!logits || !ids || !weights)
+        return fail(ROUTE_ERR_NULL, "logits, ids and weights must be non-NULL");
+    if (!aligned16(logits) || !aligned16(ids) || !aligned16(weights))
+        return fail(ROUTE_ERR_ALIGN, "every device pointer must be 16-byte aligned");
+    return ROUTE_OK;
+}
+
+route_status run_step(const route_plan *p, const void *hidden, const void *W_latent,
+                      const void *W_router, void *latent, float *logits, int32_t *ids,
+                      float *weights, cudaStream_t stream) {
+    if (p->mode == ROUTE_DECODE)
+        return launch_proj(p, hidden, W_latent, W_router, latent, logits, ids, weights, 1, stream);
+    route_status st =
+        launch_proj(p, hidden, W_latent, W_router, latent, logits, nullptr, nullptr, 0, stream);
+    if (st != ROUTE_OK) return st;
+    cudaError_t e = topk_launch(logits, p->rows, ids, weights, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "top-16 kernel launch");
+    return ROUTE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *route_last_error(void) { return g_err; }
+
+route_status route_prepare(int mode, int rows, int device, route_plan **out) {
+    g_err[0] = '\0';
+    if (!out) return fail(ROUTE_ERR_NULL, "out is NULL");
+    *out = nullptr;
+    if (mode != ROUTE_DECODE && mode != ROUTE_PREFILL)
+        return fail(ROUTE_ERR_MODE, "mode %d is neither ROUTE_DECODE (0) nor ROUTE_PREFILL (1)", mode);
+    if (mode == ROUTE_DECODE && (rows < 1 || rows > ROUTE_DECODE_MAX_ROWS))
+        return fail(ROUTE_ERR_ROWS, "decode prepares 1-%d rows; got %d", ROUTE_DECODE_MAX_ROWS, rows);
+    if (mode == ROUTE_PREFILL && (rows < 1 || rows > ROUTE_PREFILL_MAX_ROWS))
+        return fail(ROUTE_ERR_ROWS, "prefill prepares 1-%d rows; got %d", ROUTE_PREFILL_MAX_ROWS, rows);
+
+    int ndev = 0;
+    cudaError_t e = cudaGetDeviceCount(&ndev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceCount");
+    if (device < 0 || device >= ndev)
+        return fail(ROUTE_ERR_DEVICE, "device %d does not exist (%d devices)", device, ndev);
+    cudaDeviceProp prop;
+    if ((e = cudaGetDeviceProperties(&prop, device)) != cudaSuccess)
+        return cuda_fail(e, "cudaGetDeviceProperties");
+    if (prop.major != 10 || prop.minor != 3)
+        return fail(ROUTE_ERR_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a only",
+                    device, prop.major, prop.minor);
+    EncodeTiledFn enc;
+    route_status st = get_encode(&enc);
+    if (st != ROUTE_OK) return st;
+
+    DeviceGuard guard(device);
+    if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+
+    route_plan *p = new (std::nothrow) route_plan();
+    if (!p) return fail(ROUTE_ERR_PLAN, "out of host memory");
+    p->mode = mode;
+    p->rows = rows;
+    p->device = device;
+    p->bn = proj_bn_for(mode, rows);
+    const int smem = proj_smem_bytes(p->bn);
+    if (smem < 0 || (size_t)smem > prop.sharedMemPerBlockOptin) {
+        free_plan(p);
+        return fail(ROUTE_ERR_DEVICE, "kernel needs %d B of shared memory per block; device allows %zu",
+                    smem, (size_t)prop.sharedMemPerBlockOptin);
+    }
+    if ((e = proj_configure(p->bn)) != cudaSuccess) {
+        free_plan(p);
+        return cuda_fail(e, "cudaFuncSetAttribute");
+    }
+
+    ProjArgs &a = p->base;
+    memset(&a, 0, sizeof a);
+    a.rows = rows;
+    a.mode = mode;
+    a.timeout_ns = 2000000000ull;
+    const int sms = prop.multiProcessorCount;
+    if (mode == ROUTE_DECODE) {
+        a.units = kColTiles * kKBlocks;
+        a.row_tiles = 1;
+        a.grid = sms < a.units ? sms : a.units;
+        // Split-K partition: CTA g owns units [g*U/G, (g+1)*U/G); unit u is
+        // (column tile u / 112, k-block u % 112).  Tables per column tile.
+        const long long U = a.units, G = a.grid;
+        int slots = 0;
+        for (int c = 0; c < kColTiles; ++c) {
+            const long long first_u = (long long)c * kKBlocks, last_u = first_u + kKBlocks - 1;
+            int g_first = -1, g_last = -1;
+            for (int g = 0; g < a.grid; ++g) {
+                const long long u0 = g * U / G, u1 = (g + 1) * U / G;
+                if (u0 <= first_u && first_u < u1) g_first = g;
+                if (u0 <= last_u && last_u < u1) g_last = g;
+            }
+            a.cta_first[c] = g_first;
+            a.seg_count[c] = g_last - g_first + 1;
+            a.seg_base[c] = slots;
+            slots += a.seg_count[c];
+        }
+        p->segments = slots;
+        const size_t ws_bytes = (size_t)slots * kDecodeMaxRows * kTileCols * sizeof(float);
+        if ((e = cudaMalloc(&p->ws, ws_bytes)) != cudaSuccess) {
+            free_plan(p);
+            return cuda_fail(e, "cudaMalloc(split-K scratch)");
+        }
+    } else {
+        a.units = 0;
+        a.row_tiles = (rows + p->bn - 1) / p->bn;
+        const int tiles = kColTiles * a.row_tiles;
+        a.grid = sms < tiles ? sms : tiles;
+        p->segments = tiles;
+    }
+    p->grid = a.grid;
+    const size_t words = 64;
+    if ((e = cudaMalloc(&p->words, words * sizeof(unsigned))) != cudaSuccess ||
+        (e = cudaMemset(p->words, 0, words * sizeof(unsigned))) != cudaSuccess) {
+        free_plan(p);
+        return cuda_fail(e, "cudaMalloc(counters)");
+    }
+    a.ws = p->ws;
+    a.counters = p->words;
+    a.status = p->words + (kColTiles + 1);
+    p->staging_bytes = staging_size(rows);
+    if ((e = cudaMalloc(&p->staging, p->staging_bytes)) != cudaSuccess) {
+        free_plan(p);
+        return cuda_fail(e, "cudaMalloc(staging)");
+    }
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess) {
+        free_plan(p);
+        return cuda_fail(e, "cudaDeviceSynchronize");
+    }
+    *out = p;
+    return ROUTE_OK;
+}
+
+route_status route_destroy(route_plan *plan) {
+    if (!plan) return ROUTE_OK;
+    DeviceGuard guard(plan->device);
+    cudaDeviceSynchronize();
+    free_plan(plan);
+    return ROUTE_OK;
+}
+
+route_status latent_router_forward(const route_plan *plan, const void *hidden,
+                                   const void *W_latent, const void *W_router, void *latent,
+                                   float *logits, void *stream) {
+    route_status st = check_forward_args(plan, hidden, W_latent, W_router, latent, logits);
+    if (st != ROUTE_OK) return st;
+    DeviceGuard guard(plan->device);
+    if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+    return launch_proj(plan, hidden, W_latent, W_router, latent, logits, nullptr, nullptr, 0,
+                       static_cast<cudaStream_t>(stream));
+}
+
+route_status topk16_select(const route_plan *plan, const float *logits, int32_t *ids,
+                           float *weights, void *stream) {
+    route_status st = check_topk_args(plan, logits, ids, weights);
+    if (st != ROUTE_OK) return st;
+    DeviceGuard guard(plan->device);
+    if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+    cudaError_t e = topk_launch(logits, plan->rows, ids, weights, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "top-16 kernel launch");
+    return ROUTE_OK;
+}
+
+route_status route_step(const route_plan *plan, const void *hidden, const void *W_latent,
+                        const void *W_router, void *latent, float *logits, int32_t *ids,
+                        float *weights, void *stream) {
+    route_status st = check_forward_args(plan, hidden, W_latent, W_router, latent, logits);
+    if (st != ROUTE_OK) return st;
+    if ((st = check_topk_args(plan, logits, ids, weights)) != ROUTE_OK) return st;
+    DeviceGuard guard(plan->device);
+    if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+    return run_step(plan, hidden, W_latent, W_router, latent, logits, ids, weights,
+                    static_cast<cudaStream_t>(stream));
+}
+
+route_status route_step_host(const route_plan *plan, const void *hidden_host,
+                             const void *W_latent, const void *W_router, void *latent_host,
+                             float *logits_host, int32_t *ids_host, float *weights_host,
+                             void *stream) {
+    route_status st = check_plan(plan);
+    if (st != ROUTE_OK) return st;
+    if (!hidden_host || !W_latent || !W_router || !latent_host || !logits_host || !ids_host ||
+        !weights_host)
+        return fail(ROUTE_ERR_NULL, "every pointer must be non-NULL");
+    if (!aligned16(W_latent) || !aligned16(W_router))
+        return fail(ROUTE_ERR_ALIGN, "weight pointers must be 16-byte aligned");
+    DeviceGuard guard(plan->device);
+    if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Staging d = staging_of(plan);
+    const size_t r = (size_t)plan->rows;
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(d.hidden, hidden_host, r * kHidden * 2, cudaMemcpyHostToDevice, s)) !=
+        cudaSuccess)
+        return cuda_fail(e, "copy hidden to device");
+    if ((st = run_step(plan, d.hidden, W_latent, W_router, d.latent, d.logits, d.ids, d.weights,
+                       s)) != ROUTE_OK)
+        return st;
+    if ((e = cudaMemcpyAsync(latent_host, d.latent, r * kLatent * 2, cudaMemcpyDeviceToHost, s)) !=
+            cudaSuccess ||
+        (e = cudaMemcpyAsync(logits_host, d.logits, r * kExperts * 4, cudaMemcpyDeviceToHost, s)) !=
+            cudaSuccess ||
+        (e = cudaMemcpyAsync(ids_host, d.ids, r * kTopK * 4, cudaMemcpyDeviceToHost, s)) !=
+            cudaSuccess ||
+        (e = cudaMemcpyAsync(weights_host, d.weights, r * kTopK * 4, cudaMemcpyDeviceToHost, s)) !=
+            cudaSuccess)
+        return cuda_fail(e, "copy results to host");
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    return ROUTE_OK;
+}
+
+route_status route_device_status(const route_plan *plan) {
+    route_status st = check_plan(plan);
+    if (st != ROUTE_OK) return st;
+    DeviceGuard guard(plan->device);
+    if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    unsigned status = 0;
+    if ((e = cudaMemcpy(&status, plan->base.status, sizeof status, cudaMemcpyDeviceToHost)) !=
+        cudaSuccess)
+        return cuda_fail(e, "read device status");
+    if (status == 0) return ROUTE_OK;
+    cudaMemset(plan->words, 0, 64 * sizeof(unsigned));  // counters and status
+    cudaDeviceSynchronize();
+    return fail(ROUTE_ERR_DEVICE_TIMEOUT,
+                "a kernel gave up waiting (status 0x%x); that launch's outputs are invalid", status);
+}
+
+int route_plan_rows(const route_plan *plan) { return plan ? plan->rows : -1; }
+int route_plan_mode(const route_plan *plan) { return plan ? plan->mode : -1; }
+int route_plan_grid(const route_plan *plan) { return plan ? plan->grid : -1; }
+int route_plan_segments(const route_plan *plan) { return plan ? plan->segments : -1; }
+
+}  // extern "C"

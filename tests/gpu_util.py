@@ -1,0 +1,74 @@
+"""Helpers shared by the GPU tests: device copies of seeded inputs, calls
+through the C ABI, and a cache of oracle results (computed once per input)."""
+
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+import torch
+
+import latent_projection_top_gb300 as route
+import oracle
+import synth
+
+DEV = "cuda:0"
+
+
+def require_gpu():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    route.build()
+    return route.lib()
+
+
+def to_dev_bf16(bits: np.ndarray) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.to(DEV).view(torch.bfloat16)
+
+
+def bits_of(t: torch.Tensor) -> np.ndarray:
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def outputs(rows: int, poison: bool = True):
+    lat = torch.empty((rows, route.N_LATENT), dtype=torch.bfloat16, device=DEV)
+    lg = torch.empty((rows, route.N_EXPERTS), dtype=torch.float32, device=DEV)
+    ids = torch.empty((rows, route.TOPK), dtype=torch.int32, device=DEV)
+    w = torch.empty((rows, route.TOPK), dtype=torch.float32, device=DEV)
+    if poison:  # NaN / -1 so that an unwritten element cannot pass
+        lat.view(torch.int16).fill_(0x7FC0)
+        lg.fill_(float("nan"))
+        ids.fill_(-1)
+        w.fill_(float("nan"))
+    return lat, lg, ids, w
+
+
+def run_step(plan, h, wl, wr, fused=True):
+    lat, lg, ids, w = outputs(plan.rows)
+    if fused:
+        route.route_step(plan, h, wl, wr, lat, lg, ids, w)
+    else:
+        route.latent_router_forward(plan, h, wl, wr, lat, lg)
+        route.topk16_select(plan, lg, ids, w)
+    route.route_device_status(plan)
+    torch.cuda.synchronize()
+    return bits_of(lat), lg.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy()
+
+
+@functools.lru_cache(maxsize=8)
+def bank(workload: str, b: int):
+    wk = synth.WORKLOADS[workload]
+    hid = wk.hidden(b, max(wk.rows))
+    wl, wr = wk.bank(b, hid)
+    return hid, wl, wr
+
+
+@functools.lru_cache(maxsize=16)
+def oracle_rows(workload: str, b: int, rows: tuple):
+    """Oracle latent/logits (and float64 sums, sum|hw|) for the given row indices."""
+    hid, wl, wr = bank(workload, b)
+    h = np.ascontiguousarray(hid[list(rows)])
+    lat, lg, y_lat, y_log = oracle.latent_router(h, wl, wr)
+    from gates import abs_dot
+    return {"latent": lat, "logits": lg, "y_lat": y_lat, "y_log": y_log,
+            "abs_lat": abs_dot(h, wl), "abs_log": abs_dot(h, wr)}

@@ -1,0 +1,98 @@
+"""The C-ABI library on a machine without a GPU: it builds for sm_103a, loads,
+exports every entry point the header declares, and rejects bad arguments with
+status codes before it touches a device (no compute call is made here)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import latent_projection_top_gb300 as route
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "route.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    route.build()
+    return route.lib()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(route_\w+|latent_\w+|topk16_\w+)\s*\(",
+                                 text, flags=re.M)))
+
+
+def test_header_declares_the_binding_exports():
+    fns = header_functions()
+    assert "route_prepare" in fns and "latent_router_forward" in fns and "topk16_select" in fns
+    assert sorted(route.EXPORTS) == fns
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+
+
+def _prepare(lib, mode, rows):
+    h = ctypes.c_void_p(123)
+    st = lib.route_prepare(mode, rows, 0, ctypes.byref(h))
+    return st, h
+
+
+@pytest.mark.parametrize("rows", [0, -1, 21, 1000])
+def test_decode_envelope_rejected_at_preparation(lib, rows, figures):
+    st, h = _prepare(lib, route.DECODE, rows)
+    assert st == 1 and h.value is None  # ROUTE_ERR_ROWS, *out cleared
+    assert b"1-20" in lib.route_last_error()
+
+
+def test_the_21_row_rejection_matches_the_pages(lib, figures):
+    assert figures["decode_rows_rejected"] == route.DECODE_MAX_ROWS + 1
+    st, _ = _prepare(lib, route.DECODE, figures["decode_rows_rejected"])
+    assert st == 1
+
+
+@pytest.mark.parametrize("rows", [0, route.PREFILL_MAX_ROWS + 1])
+def test_prefill_envelope(lib, rows):
+    st, _ = _prepare(lib, route.PREFILL, rows)
+    assert st == 1
+
+
+def test_bad_mode_and_null_out(lib):
+    st, _ = _prepare(lib, 7, 8)
+    assert st == 2
+    assert lib.route_prepare(route.DECODE, 8, 0, None) == 3
+
+
+def test_valid_request_without_gpu_fails_loudly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st, h = _prepare(lib, route.DECODE, 8)
+    assert st in (5, 8) and h.value is None  # ROUTE_ERR_CUDA / ROUTE_ERR_DEVICE
+    assert lib.route_last_error()
+
+
+def test_calls_with_null_plan(lib):
+    null = ctypes.c_void_p(0)
+    x = ctypes.c_void_p(0x1000)
+    assert lib.latent_router_forward(null, x, x, x, x, x, None) == 3
+    assert lib.topk16_select(null, x, x, x, None) == 3
+    assert lib.route_step(null, x, x, x, x, x, x, x, None) == 3
+    assert lib.route_step_host(null, x, x, x, x, x, x, x, None) == 3
+    assert lib.route_device_status(null) == 3
+    assert lib.route_destroy(null) == 0
+    for f in ("route_plan_rows", "route_plan_mode", "route_plan_grid", "route_plan_segments"):
+        assert getattr(lib, f)(null) == -1
+
+
+def test_binding_refuses_to_run_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(route, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(route, "_lib", None)
+    with pytest.raises(route.RouteError):
+        route.lib()

@@ -1,0 +1,259 @@
+"""Parity of the CUDA route step with the oracle, through the C ABI.
+
+Sizes are chosen so the oracle finishes in seconds while the kernels still
+span several tiles and a ragged tail; at the full prefill sizes outputs are
+checked on sampled rows that the oracle computes one by one."""
+
+import numpy as np
+import pytest
+import torch
+
+import latent_projection_top_gb300 as route
+import oracle
+import synth
+from gates import (check_ids_end_to_end, check_latent, check_logits, check_topk_exact)
+from gpu_util import (DEV, bank, bits_of, oracle_rows, outputs, require_gpu, run_step,
+                      to_dev_bf16)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+# ---------------------------------------------------------------- top-16 (G1)
+
+def _topk_gpu(logits: np.ndarray, mode=route.DECODE):
+    R = logits.shape[0]
+    with route.Plan(mode, R) as plan:
+        lg = torch.from_numpy(np.ascontiguousarray(logits, np.float32)).to(DEV)
+        _, _, ids, w = outputs(R)
+        route.topk16_select(plan, lg, ids, w)
+        torch.cuda.synchronize()
+        return ids.cpu().numpy(), w.cpu().numpy()
+
+
+def special_rows() -> np.ndarray:
+    E = 896
+    rng = np.random.default_rng(0)
+    rows = [
+        -np.arange(E, dtype=np.float32),
+        np.arange(E, dtype=np.float32),
+        np.full(E, 0.75, np.float32),
+        (np.round(rng.standard_normal(E) * 2) / 2).astype(np.float32),   # many ties
+        np.where(rng.random(E) < 0.5, -0.0, 0.0).astype(np.float32),   # +-0 only
+    ]
+    r = -np.arange(E, dtype=np.float32) - 10
+    r[:15] = 5.0 + np.arange(15, 0, -1)
+    r[[700, 40, 41]] = 1.5                                             # tie at ranks 16/17
+    rows.append(r)
+    r = rng.standard_normal(E).astype(np.float32)
+    r[[3, 600]] = np.inf
+    r[[5, 6]] = -np.inf
+    r[[7, 800, 801]] = np.nan
+    rows.append(r)
+    r = np.full(E, np.nan, np.float32)
+    r[[3, 7]] = [-np.inf, 2.0]
+    rows.append(r)                                                      # mostly NaN
+    r = np.full(E, -np.inf, np.float32)
+    rows.append(r)                                                      # all -Inf
+    r = rng.standard_normal(E).astype(np.float32) * 1e-30              # tiny and subnormal
+    r[::7] = np.float32(1e-45)
+    rows.append(r)
+    r = rng.standard_normal(E).astype(np.float32) * 40                 # sigmoid saturation
+    rows.append(r)
+    r = np.full(E, -3.0, np.float32)
+    r[np.arange(0, E, 31)] = 2.0                                       # equal values per lane stride
+    rows.append(r)
+    return np.stack(rows)
+
+
+def test_topk_bit_exact_special_rows():
+    logits = special_rows()
+    ids, w = _topk_gpu(logits)
+    ids_ref, w_ref = oracle.topk(logits)
+    check_topk_exact(ids, w, ids_ref, w_ref)
+
+
+@pytest.mark.parametrize("R,mode", [(20, route.DECODE), (3072, route.PREFILL)])
+def test_topk_bit_exact_random(R, mode):
+    rng = np.random.default_rng(R)
+    logits = (rng.standard_normal((R, 896)) * 2).astype(np.float32)
+    # a quarter of the rows get exact duplicates across the 16/17 boundary
+    srt = np.sort(logits, axis=1)[:, ::-1]
+    for r in range(0, R, 4):
+        j = int(np.argwhere(logits[r] == srt[r, 16])[0, 0])
+        logits[r, j] = srt[r, 15]
+    ids, w = _topk_gpu(logits, mode)
+    ids_ref, w_ref = oracle.topk(logits)
+    check_topk_exact(ids, w, ids_ref, w_ref)
+
+
+# ------------------------------------------------------------ decode (G1-G5)
+
+DECODE_CASES = [("decode_r1", 1), ("decode_r8", 8), ("decode_sweep", 9), ("decode_sweep", 12),
+                ("decode_sweep", 16), ("decode_sweep", 20)]
+
+
+@pytest.mark.parametrize("workload,rows", DECODE_CASES)
+def test_decode_route_step_parity(workload, rows):
+    hid, wl, wr = bank(workload, 0)
+    ref = oracle_rows(workload, 0, tuple(range(max(synth.WORKLOADS[workload].rows))))
+    h = to_dev_bf16(hid[:rows])
+    dwl, dwr = to_dev_bf16(wl), to_dev_bf16(wr)
+    with route.Plan(route.DECODE, rows) as plan:
+        lat, lg, ids, w = run_step(plan, h, dwl, dwr, fused=True)
+        lat2, lg2, ids2, w2 = run_step(plan, h, dwl, dwr, fused=False)
+    sl = slice(0, rows)
+    check_latent(lat, ref["latent"][sl], ref["y_lat"][sl], ref["abs_lat"][sl])
+    check_logits(lg, ref["y_log"][sl], ref["abs_log"][sl])
+    # the fused top-16 equals the oracle's top-16 on the same (GPU) logits
+    ids_o, w_o = oracle.topk(lg)
+    check_topk_exact(ids, w, ids_o, w_o)
+    # end to end against the oracle's own logits
+    ids_ref, _ = oracle.topk(ref["logits"][sl])
+    check_ids_end_to_end(ids, ids_ref, ref["logits"][sl])
+    # the unfused path computes the same bits
+    assert np.array_equal(lat, lat2) and np.array_equal(lg.view(np.uint32), lg2.view(np.uint32))
+    assert np.array_equal(ids, ids2) and np.array_equal(w.view(np.uint32), w2.view(np.uint32))
+
+
+def test_decode_batch_invariance_and_determinism():
+    hid, wl, wr = bank("decode_sweep", 1)
+    dwl, dwr = to_dev_bf16(wl), to_dev_bf16(wr)
+    results = {}
+    for rows in (20, 1, 8, 16, 17):
+        with route.Plan(route.DECODE, rows) as plan:
+            results[rows] = run_step(plan, to_dev_bf16(hid[:rows]), dwl, dwr)
+            again = run_step(plan, to_dev_bf16(hid[:rows]), dwl, dwr)
+            for a, b in zip(results[rows], again):
+                assert np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8))
+    full = results[20]
+    for rows in (1, 8, 16, 17):
+        for a, b in zip(results[rows], full):
+            assert np.array_equal(np.asarray(a).view(np.uint8),
+                                  np.asarray(b)[:rows].view(np.uint8)), f"rows={rows}"
+
+
+def test_decode_bank_cycling_under_graph_replay():
+    """Eight banks cycled inside one captured CUDA graph give the eager bits."""
+    rows = 8
+    banks = [bank("decode_r8", b) for b in range(3)]
+    dev = [(to_dev_bf16(h[:rows]), to_dev_bf16(wl), to_dev_bf16(wr)) for h, wl, wr in banks]
+    with route.Plan(route.DECODE, rows) as plan:
+        eager = [run_step(plan, *d) for d in dev]
+        outs = [outputs(rows) for _ in dev]
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for d, o in zip(dev, outs):
+                    route.route_step(plan, *d, *o, stream=s)
+        for _ in range(20):
+            for o in outs:
+                o[0].view(torch.int16).fill_(0x7FC0)
+                o[1].fill_(float("nan"))
+            g.replay()
+        torch.cuda.synchronize()
+        route.route_device_status(plan)
+        for o, e in zip(outs, eager):
+            assert np.array_equal(bits_of(o[0]), e[0])
+            assert np.array_equal(o[1].cpu().numpy().view(np.uint32), e[1].view(np.uint32))
+            assert np.array_equal(o[2].cpu().numpy(), e[2])
+
+
+# ------------------------------------------------------------------- prefill
+
+@pytest.mark.parametrize("rows,sample", [(1, None), (40, None), (256, (0, 100, 255)),
+                                         (300, (0, 255, 256, 299))])
+def test_prefill_ragged_parity(rows, sample):
+    hid, wl, wr = bank("prefill_r1024", 0)
+    idx = tuple(range(rows)) if sample is None else sample
+    ref = oracle_rows("prefill_r1024", 0, idx)
+    with route.Plan(route.PREFILL, rows) as plan:
+        lat, lg, ids, w = run_step(plan, to_dev_bf16(hid[:rows]), to_dev_bf16(wl), to_dev_bf16(wr))
+    sel = list(idx)
+    check_latent(lat[sel], ref["latent"], ref["y_lat"], ref["abs_lat"])
+    check_logits(lg[sel], ref["y_log"], ref["abs_log"])
+    ids_o, w_o = oracle.topk(lg)
+    check_topk_exact(ids, w, ids_o, w_o)
+    ids_ref, _ = oracle.topk(ref["logits"])
+    check_ids_end_to_end(ids[sel], ids_ref, ref["logits"])
+
+
+def test_prefill_1024_cancel_group_sampled():
+    """Rows d < 448 see cancelling K-slice partials on latent column d."""
+    hid, wl, wr = bank("prefill_r1024", 0)
+    idx = (0, 1, 2, 63, 127, 128, 255, 300, 447, 448, 511, 640, 767, 896, 1000, 1023)
+    ref = oracle_rows("prefill_r1024", 0, idx)
+    with route.Plan(route.PREFILL, 1024) as plan:
+        lat, lg, ids, w = run_step(plan, to_dev_bf16(hid), to_dev_bf16(wl), to_dev_bf16(wr))
+    sel = list(idx)
+    check_latent(lat[sel], ref["latent"], ref["y_lat"], ref["abs_lat"])
+    check_logits(lg[sel], ref["y_log"], ref["abs_log"])
+    ids_o, w_o = oracle.topk(lg)
+    check_topk_exact(ids, w, ids_o, w_o)
+    ids_ref, _ = oracle.topk(ref["logits"])
+    check_ids_end_to_end(ids[sel], ids_ref, ref["logits"])
+
+
+def test_prefill_3072_sampled_and_deterministic():
+    hid, wl, wr = bank("prefill_r3072", 0)
+    idx = (0, 1, 255, 256, 1000, 1535, 2047, 2048, 2900, 3071)
+    ref = oracle_rows("prefill_r3072", 0, idx)
+    dh, dwl, dwr = to_dev_bf16(hid), to_dev_bf16(wl), to_dev_bf16(wr)
+    with route.Plan(route.PREFILL, 3072) as plan:
+        a = run_step(plan, dh, dwl, dwr)
+        b = run_step(plan, dh, dwl, dwr)
+    for x, y in zip(a, b):
+        assert np.array_equal(np.asarray(x).view(np.uint8), np.asarray(y).view(np.uint8))
+    lat, lg, ids, w = a
+    sel = list(idx)
+    check_latent(lat[sel], ref["latent"], ref["y_lat"], ref["abs_lat"])
+    check_logits(lg[sel], ref["y_log"], ref["abs_log"])
+    ids_o, w_o = oracle.topk(lg)
+    check_topk_exact(ids, w, ids_o, w_o)
+
+
+# ------------------------------------------------------- host entry / errors
+
+def test_route_step_host_matches_device():
+    hid, wl, wr = bank("decode_r8", 0)
+    rows = 8
+    dwl, dwr = to_dev_bf16(wl), to_dev_bf16(wr)
+    with route.Plan(route.DECODE, rows) as plan:
+        dev = run_step(plan, to_dev_bf16(hid[:rows]), dwl, dwr)
+        h_host = torch.from_numpy(hid[:rows].view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+        lat = torch.empty((rows, route.N_LATENT), dtype=torch.bfloat16).pin_memory()
+        lg = torch.empty((rows, route.N_EXPERTS), dtype=torch.float32).pin_memory()
+        ids = torch.empty((rows, route.TOPK), dtype=torch.int32).pin_memory()
+        w = torch.empty((rows, route.TOPK), dtype=torch.float32).pin_memory()
+        route.route_step_host(plan, h_host, dwl, dwr, lat, lg, ids, w)
+    assert np.array_equal(lat.view(torch.int16).numpy().view(np.uint16), dev[0])
+    assert np.array_equal(lg.numpy().view(np.uint32), dev[1].view(np.uint32))
+    assert np.array_equal(ids.numpy(), dev[2])
+    assert np.array_equal(w.numpy().view(np.uint32), dev[3].view(np.uint32))
+
+
+def test_gpu_argument_errors():
+    lib = route.lib()
+    import ctypes
+    with route.Plan(route.DECODE, 4) as plan:
+        buf = torch.zeros(1 << 22, dtype=torch.uint8, device=DEV)
+        base = buf.data_ptr()
+        ok = ctypes.c_void_p(base)
+        odd = ctypes.c_void_p(base + 2)
+        assert lib.latent_router_forward(plan.handle, odd, ok, ok, ok, ok, None) == 4
+        assert lib.topk16_select(plan.handle, ok, odd, ok, None) == 4
+        assert lib.latent_router_forward(plan.handle, None, ok, ok, ok, ok, None) == 3
+    with pytest.raises(route.RouteError):
+        route.Plan(route.DECODE, 4, device=torch.cuda.device_count())
+    # shape and dtype are checked by the binding before the C call
+    with route.Plan(route.DECODE, 2) as plan:
+        lat, lg, ids, w = outputs(2)
+        bad = torch.zeros((3, route.K_HIDDEN), dtype=torch.bfloat16, device=DEV)
+        with pytest.raises(ValueError):
+            route.latent_router_forward(plan, bad, bad, bad, lat, lg)
