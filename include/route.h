@@ -150,6 +150,18 @@ route_status route_step_host(const route_plan *plan, const void *hidden_host,
  */
 route_status route_device_status(const route_plan *plan);
 
+/*
+ * route_test_stall: TEST HOOK for the bounded-wait path, not for production.
+ * With enable != 0, each CTA of the plan's projection kernel skips its last
+ * weight copy, so its MMA warp waits for data that never arrives; after
+ * timeout_ns the wait gives up, the kernel sets the device status word, drains
+ * its in-flight work, frees its tensor memory and returns, and
+ * route_device_status() then reports ROUTE_ERR_DEVICE_TIMEOUT.  enable == 0
+ * restores normal operation with the default bound (2 s).  Not thread-safe
+ * with concurrent use of the plan.
+ */
+route_status route_test_stall(route_plan *plan, int enable, uint64_t timeout_ns);
+
 /* Plan properties: rows, mode, launch grid (CTAs) and split-K segments. */
 int route_plan_rows(const route_plan *plan);
 int route_plan_mode(const route_plan *plan);

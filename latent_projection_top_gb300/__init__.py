@@ -44,7 +44,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libroute.so")
 EXPORTS = (
     "route_prepare", "route_destroy", "latent_router_forward", "topk16_select", "route_step",
     "route_step_host", "route_device_status", "route_plan_rows", "route_plan_mode",
-    "route_plan_grid", "route_plan_segments", "route_last_error",
+    "route_plan_grid", "route_plan_segments", "route_last_error", "route_test_stall",
 )
 
 
@@ -78,6 +78,8 @@ def lib() -> ctypes.CDLL:
         L.route_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.route_step_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.route_device_status.argtypes = [vp]
+        L.route_test_stall.argtypes = [vp, i32, ctypes.c_uint64]
+        L.route_test_stall.restype = i32
         for f in ("route_plan_rows", "route_plan_mode", "route_plan_grid", "route_plan_segments"):
             getattr(L, f).argtypes = [vp]
             getattr(L, f).restype = i32
@@ -244,6 +246,12 @@ def route_step_host(plan: Plan, hidden_host, W_latent, W_router, latent_host, lo
             _host_tensor(ids_host, "ids_host", (R, TOPK), (torch.int32,)),
             _host_tensor(weights_host, "weights_host", (R, TOPK), (torch.float32,)))
     _check(lib().route_step_host(plan.handle, *args, _stream(stream, d)))
+
+
+def route_test_stall(plan: Plan, enable: bool, timeout_ns: int = 1_000_000) -> None:
+    """Test hook: make the plan's projection kernel wait for a copy that never
+    comes, so that its bounded wait expires (see include/route.h)."""
+    _check(lib().route_test_stall(plan.handle, int(bool(enable)), int(timeout_ns)))
 
 
 def route_device_status(plan: Plan) -> None:

@@ -41,6 +41,7 @@ struct ProjArgs {
     int grid;            // CTAs launched
     int units;           // decode: kColTiles * kKBlocks (k-block units split over CTAs)
     int fuse_topk;       // decode: the CTA finishing the last router tile runs the top-16
+    int test_stall;      // test hook: skip each CTA's last copy so a wait must time out
     unsigned long long timeout_ns;  // bound on every wait inside the kernel
     // decode split-K partition, fixed at plan time (depends on grid only):
     int seg_base[kColTiles];   // first partial slot of column tile c

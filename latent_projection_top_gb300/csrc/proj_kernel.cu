@@ -48,6 +48,7 @@ namespace {
 
 constexpr uint32_t kABoxBytes = 64 * 64 * 2;       // 64 columns x 64 k, BF16
 constexpr uint32_t kAStageBytes = 2 * kABoxBytes;  // 128 columns x 64 k
+constexpr int kReduceBatch = 8;                    // split-K partials loaded per batch
 
 template <int BN>
 struct ProjCfg {
@@ -166,6 +167,7 @@ __global__ void __launch_bounds__(kProjThreads, 1)
     __shared__ uint32_t s_tmem_base;
     __shared__ volatile int s_abort;
     __shared__ int s_last;
+    __shared__ uint2 s_cand[4][kCandMax];  // fused top-16 candidates, one buffer per epilogue warp
 
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -227,6 +229,8 @@ __global__ void __launch_bounds__(kProjThreads, 1)
                         ok = false;
                         break;
                     }
+                    if (args.test_stall && i == nseg - 1 && kb == sg.kb1 - 1)
+                        continue;  // test hook: this stage is never filled
                     const uint32_t a = sbase + s * C::kStageBytes;
                     ptx::mbar_arrive_expect_tx(full_bar(s), C::kStageBytes);
                     ptx::tma_load_2d(a, wmap, full_bar(s), x0, kb * kKBlock, pol_w);
@@ -329,18 +333,59 @@ __global__ void __launch_bounds__(kProjThreads, 1)
                 ptx::named_bar_sync(1, 128);
                 if (s_last) {
                     // Last arrival: sum the tile's partials in segment order.
+                    // Items are (row, 4 columns); all of an item's partials are
+                    // loaded before any is added, two items at a time.
                     __threadfence();
                     const int ns = args.seg_count[sg.c];
-                    const float *p0 =
-                        args.ws + (size_t)args.seg_base[sg.c] * kDecodeMaxRows * kTileCols + col;
-                    for (int r = 0; r < rows; ++r) {
-                        float acc = __ldcg(p0 + r * kTileCols);
-                        for (int s = 1; s < ns; ++s)
-                            acc += __ldcg(p0 + ((size_t)s * kDecodeMaxRows + r) * kTileCols);
-                        if (lat)
-                            args.latent[(size_t)r * kLatent + ncol] = bf16_bits(acc);
-                        else
-                            args.logits[(size_t)r * kExperts + ncol] = acc;
+                    const float *p0 = args.ws + (size_t)args.seg_base[sg.c] * kDecodeMaxRows * kTileCols;
+                    const int items = rows * (kTileCols / 4);
+                    const int nbase = (lat ? sg.c : sg.c - kLatentTiles) * kTileCols;
+                    for (int it0 = et; it0 < items; it0 += 256) {
+                        float4 acc[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int s0 = 0; s0 < ns; s0 += kReduceBatch) {
+                            float4 part[2][kReduceBatch];
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const int it = it0 + 128 * u;
+                                const float *p = p0 + (it >> 5) * kTileCols + (it & 31) * 4;
+#pragma unroll
+                                for (int j = 0; j < kReduceBatch; ++j)
+                                    if (it < items && s0 + j < ns)
+                                        part[u][j] = __ldcg(reinterpret_cast<const float4 *>(
+                                            p + (size_t)(s0 + j) * kDecodeMaxRows * kTileCols));
+                            }
+#pragma unroll
+                            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                                for (int j = 0; j < kReduceBatch; ++j)
+                                    if (s0 + j < ns) {
+                                        if (s0 + j == 0) {
+                                            acc[u] = part[u][j];
+                                        } else {
+                                            acc[u].x += part[u][j].x;
+                                            acc[u].y += part[u][j].y;
+                                            acc[u].z += part[u][j].z;
+                                            acc[u].w += part[u][j].w;
+                                        }
+                                    }
+                        }
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int it = it0 + 128 * u;
+                            if (it >= items) continue;
+                            const int r = it >> 5;
+                            const int n = nbase + (it & 31) * 4;
+                            if (lat) {
+                                uint2 packed;
+                                packed.x = (uint32_t)bf16_bits(acc[u].x) | ((uint32_t)bf16_bits(acc[u].y) << 16);
+                                packed.y = (uint32_t)bf16_bits(acc[u].z) | ((uint32_t)bf16_bits(acc[u].w) << 16);
+                                *reinterpret_cast<uint2 *>(args.latent + (size_t)r * kLatent + n) = packed;
+                            } else {
+                                *reinterpret_cast<float4 *>(args.logits + (size_t)r * kExperts + n) = acc[u];
+                            }
+                        }
                     }
                     if (et == 0) args.counters[sg.c] = 0u;  // ready for the next launch
                     if (args.fuse_topk && !lat) {
@@ -357,7 +402,8 @@ __global__ void __launch_bounds__(kProjThreads, 1)
                             for (int r = et >> 5; r < rows; r += 4)
                                 topk16_warp(args.logits + (size_t)r * kExperts,
                                             args.ids + (size_t)r * kTopK,
-                                            args.weights + (size_t)r * kTopK, lane);
+                                            args.weights + (size_t)r * kTopK, lane,
+                                            s_cand[et >> 5]);
                             if (et == 0) args.counters[kColTiles] = 0u;
                         }
                     }

@@ -32,6 +32,8 @@ struct route_plan {
 
 namespace {
 
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // bound on every in-kernel wait
+
 thread_local char g_err[512] = "";
 
 route_status fail(route_status st, const char *fmt, ...) {
@@ -263,7 +265,7 @@ route_status route_prepare(int mode, int rows, int device, route_plan **out) {
     memset(&a, 0, sizeof a);
     a.rows = rows;
     a.mode = mode;
-    a.timeout_ns = 2000000000ull;
+    a.timeout_ns = kDefaultTimeoutNs;
     const int sms = prop.multiProcessorCount;
     if (mode == ROUTE_DECODE) {
         a.units = kColTiles * kKBlocks;
@@ -416,6 +418,14 @@ route_status route_device_status(const route_plan *plan) {
     cudaDeviceSynchronize();
     return fail(ROUTE_ERR_DEVICE_TIMEOUT,
                 "a kernel gave up waiting (status 0x%x); that launch's outputs are invalid", status);
+}
+
+route_status route_test_stall(route_plan *plan, int enable, uint64_t timeout_ns) {
+    route_status st = check_plan(plan);
+    if (st != ROUTE_OK) return st;
+    plan->base.test_stall = enable ? 1 : 0;
+    plan->base.timeout_ns = enable ? (timeout_ns ? timeout_ns : 1000000ull) : kDefaultTimeoutNs;
+    return ROUTE_OK;
 }
 
 int route_plan_rows(const route_plan *plan) { return plan ? plan->rows : -1; }

@@ -8,6 +8,14 @@
 // unsigned key whose integer order is that ranking, so a pick is
 // (largest key, then smallest id) and needs two warp reductions.
 //
+// Lane l holds the 28 logits with ids 32*j + l.  A threshold T = the 16th
+// largest of the 32 lane maxima is a lower bound on the 16th largest key
+// (at least 16 lanes hold a key >= T), so only keys >= T can be picked.
+// Those candidates (usually a few dozen) are compacted into shared memory and
+// the 16 picks are made among them; rows with more than 64 candidates (heavy
+// ties) take the same 16 picks over all 896 keys.  Both give the unique
+// ranking above.
+//
 // Weights: w_i = s_i / sum_j s_j, s_i = 1 / (1 + exp(-logit_i)), evaluated in
 // double and rounded once to FP32 (the library's stated convention).
 #pragma once
@@ -17,6 +25,7 @@
 namespace route {
 
 constexpr int kPerLane = 896 / 32;  // 28 logits per lane; lane l holds ids 32*j + l
+constexpr int kCandMax = 64;        // candidate buffer per warp (two per lane)
 
 // Order-preserving key: NaN -> 1 (below -Inf), -0 -> +0, removed entries -> 0.
 __device__ __forceinline__ uint32_t rank_key(float v) {
@@ -33,45 +42,102 @@ __device__ __forceinline__ float key_to_float(uint32_t key) {
     return __uint_as_float(b);
 }
 
+// The 16th largest of the 32 lanes' values (bitonic sort, ascending).
+__device__ __forceinline__ uint32_t warp_16th_largest(uint32_t v, int lane) {
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, v, j);
+            const bool ascending = (lane & k) == 0 || k == 32;
+            const bool lower = (lane & j) == 0;
+            v = (lower == ascending) ? min(v, other) : max(v, other);
+        }
+    }
+    return __shfl_sync(0xFFFFFFFFu, v, 16);
+}
+
 // The calling warp selects row `row` (896 logits, read through L2 so that
 // values written by other CTAs of the same kernel are seen) and writes 16 ids
-// and weights.  All 32 lanes must call it.
+// and weights.  All 32 lanes must call it; `cand` is this warp's shared
+// buffer of kCandMax entries.
 __device__ __forceinline__ void topk16_warp(const float *row, int32_t *ids_out, float *w_out,
-                                            int lane) {
+                                            int lane, uint2 *cand) {
     uint32_t key[kPerLane];
 #pragma unroll
     for (int j = 0; j < kPerLane; ++j) key[j] = rank_key(__ldcg(row + 32 * j + lane));
 
-    uint32_t best = 0u;
-    int best_j = 0;
+    uint32_t lane_max = 0u;
 #pragma unroll
-    for (int j = 0; j < kPerLane; ++j)
-        if (key[j] > best) {
-            best = key[j];
-            best_j = j;
-        }
+    for (int j = 0; j < kPerLane; ++j) lane_max = max(lane_max, key[j]);
+    const uint32_t T = warp_16th_largest(lane_max, lane);
+
+    uint32_t cnt = 0u;
+#pragma unroll
+    for (int j = 0; j < kPerLane; ++j) cnt += (key[j] >= T) ? 1u : 0u;
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
 
     uint32_t mine_key = 0u;  // lane i keeps the i-th pick (i < 16)
     uint32_t mine_id = 0u;
-#pragma unroll 1
-    for (int i = 0; i < 16; ++i) {
-        uint32_t top = __reduce_max_sync(0xFFFFFFFFu, best);
-        uint32_t cand = (best == top) ? (uint32_t)(32 * best_j + lane) : 0xFFFFFFFFu;
-        uint32_t pick = __reduce_min_sync(0xFFFFFFFFu, cand);
-        if (lane == i) {
-            mine_key = top;
-            mine_id = pick;
-        }
-        if ((int)(pick & 31u) == lane) {  // the owner removes the pick and rescans
-            int js = (int)(pick >> 5);
-            best = 0u;
-            best_j = 0;
+    if (total <= (uint32_t)kCandMax) {
+        uint32_t pos = incl - cnt;
 #pragma unroll
-            for (int j = 0; j < kPerLane; ++j) {
-                if (j == js) key[j] = 0u;
-                if (key[j] > best) {
-                    best = key[j];
-                    best_j = j;
+        for (int j = 0; j < kPerLane; ++j)
+            if (key[j] >= T) cand[pos++] = make_uint2(key[j], (uint32_t)(32 * j + lane));
+        __syncwarp();
+        uint2 c0 = make_uint2(0u, 0xFFFFFFFFu), c1 = make_uint2(0u, 0xFFFFFFFFu);
+        if ((uint32_t)lane < total) c0 = cand[lane];
+        if ((uint32_t)lane + 32u < total) c1 = cand[lane + 32];
+        __syncwarp();
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i) {
+            const bool second = c1.x > c0.x || (c1.x == c0.x && c1.y < c0.y);
+            const uint32_t bk = second ? c1.x : c0.x;
+            const uint32_t bi = second ? c1.y : c0.y;
+            const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, bk);
+            const uint32_t pick = __reduce_min_sync(0xFFFFFFFFu, bk == top ? bi : 0xFFFFFFFFu);
+            if (lane == i) {
+                mine_key = top;
+                mine_id = pick;
+            }
+            if (c0.y == pick) c0.x = 0u;
+            if (c1.y == pick) c1.x = 0u;
+        }
+    } else {
+        uint32_t best = 0u;
+        int best_j = 0;
+#pragma unroll
+        for (int j = 0; j < kPerLane; ++j)
+            if (key[j] > best) {
+                best = key[j];
+                best_j = j;
+            }
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, best);
+            const uint32_t c = (best == top) ? (uint32_t)(32 * best_j + lane) : 0xFFFFFFFFu;
+            const uint32_t pick = __reduce_min_sync(0xFFFFFFFFu, c);
+            if (lane == i) {
+                mine_key = top;
+                mine_id = pick;
+            }
+            if ((int)(pick & 31u) == lane) {  // the owner removes the pick and rescans
+                const int js = (int)(pick >> 5);
+                best = 0u;
+                best_j = 0;
+#pragma unroll
+                for (int j = 0; j < kPerLane; ++j) {
+                    if (j == js) key[j] = 0u;
+                    if (key[j] > best) {
+                        best = key[j];
+                        best_j = j;
+                    }
                 }
             }
         }
@@ -79,13 +145,13 @@ __device__ __forceinline__ void topk16_warp(const float *row, int32_t *ids_out, 
 
     double s = 0.0;
     if (lane < 16) s = 1.0 / (1.0 + exp(-(double)key_to_float(mine_key)));
-    double total = s;
+    double total_s = s;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) total += __shfl_xor_sync(0xFFFFFFFFu, total, off);
-    total = __shfl_sync(0xFFFFFFFFu, total, 0);  // one association order for every lane
+    for (int off = 16; off > 0; off >>= 1) total_s += __shfl_xor_sync(0xFFFFFFFFu, total_s, off);
+    total_s = __shfl_sync(0xFFFFFFFFu, total_s, 0);  // one association order for every lane
     if (lane < 16) {
         ids_out[lane] = (int32_t)mine_id;
-        w_out[lane] = (float)(s / total);
+        w_out[lane] = (float)(s / total_s);
     }
 }
 

@@ -12,10 +12,12 @@ constexpr int kRowsPerBlock = 8;
 __global__ void __launch_bounds__(32 * kRowsPerBlock)
     topk16_kernel(const float *__restrict__ logits, int rows, int32_t *__restrict__ ids,
                   float *__restrict__ weights) {
-    const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
+    __shared__ uint2 cand[kRowsPerBlock][kCandMax];
+    const int warp = threadIdx.x >> 5;
+    const int row = blockIdx.x * kRowsPerBlock + warp;
     if (row >= rows) return;  // whole warps leave together
     topk16_warp(logits + (size_t)row * kExperts, ids + (size_t)row * kTopK,
-                weights + (size_t)row * kTopK, threadIdx.x & 31);
+                weights + (size_t)row * kTopK, threadIdx.x & 31, cand[warp]);
 }
 
 }  // namespace

@@ -11,12 +11,18 @@ G3  logits: |out - y64| <= 2^-20 * sum_k |h w| per element.
 G4  end-to-end ids (GPU logits -> GPU top-16) against the oracle's ids: equal
     sets, or one id out and one in whose oracle logits lie within 2 FP32 ULP
     of each other (same page: "a 1-for-1 swap within 2 fp32 ULP"); within
-    equal sets, a reordering only between entries within 2 ULP.
+    equal sets, two ids may trade places only if their float64 logits are
+    closer than the sum of their G3 allowances.
+
+Set ROUTE_PARITY_STATS=<file> to append each check's statistics (relative
+RMS, ULP distances, swap counts) to a JSON-lines file.
 """
 
 from __future__ import annotations
 
+import json
 import math
+import os
 
 import numpy as np
 
@@ -24,6 +30,13 @@ import oracle
 
 SLACK = 2.0 ** -20
 REL_RMS_BAR = 2e-3
+
+
+def record(case: str, **stats) -> None:
+    path = os.environ.get("ROUTE_PARITY_STATS")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"case": case, **stats}) + "\n")
 
 
 def bf16_vals(bits) -> np.ndarray:
@@ -48,7 +61,7 @@ def abs_dot(h_bits, W_bits) -> np.ndarray:
                         np.asarray(W_bits, np.uint16) & 0x7FFF)
 
 
-def check_latent(out_bits, ref_bits, y64, absdot) -> dict:
+def check_latent(out_bits, ref_bits, y64, absdot, rms_bar: bool = True) -> dict:
     out = bf16_vals(out_bits)
     ref = bf16_vals(ref_bits)
     assert np.isfinite(out).all(), "non-finite latent"
@@ -59,7 +72,8 @@ def check_latent(out_bits, ref_bits, y64, absdot) -> dict:
     assert not bad.any(), (
         f"{int(bad.sum())} latent elements outside the gate; first at "
         f"{np.argwhere(bad)[0].tolist()}")
-    assert rel <= REL_RMS_BAR, f"latent relative RMS {rel:.3e} > {REL_RMS_BAR}"
+    if rms_bar:
+        assert rel <= REL_RMS_BAR, f"latent relative RMS {rel:.3e} > {REL_RMS_BAR}"
     exact = np.asarray(out_bits).view(np.uint16) == np.asarray(ref_bits).view(np.uint16)
     return {"rel_rms": rel, "slack_only": int((~strict).sum()),
             "cr_miss_rate": float(1.0 - exact.mean())}
@@ -84,7 +98,11 @@ def check_topk_exact(ids, w, ids_ref, w_ref, ulp_bound: int = 5) -> dict:
     return {"max_weight_ulp": float(ulps.max())}
 
 
-def check_ids_end_to_end(ids, ids_ref, logits_ref) -> dict:
+def check_ids_end_to_end(ids, ids_ref, logits_ref, y_log=None, abs_log=None) -> dict:
+    """G4.  A set difference must be one id out, one in, within 2 FP32 ULP of
+    each other.  Within equal sets, two ids may trade places only if their
+    float64 logits are closer than the sum of the two logits' G3 error
+    allowances (when y_log / abs_log are given), else within 2 ULP."""
     swaps = 0
     for r in range(ids.shape[0]):
         got, want = list(ids[r]), list(ids_ref[r])
@@ -96,11 +114,17 @@ def check_ids_end_to_end(ids, ids_ref, logits_ref) -> dict:
             assert len(out_) == 1 and len(in_) == 1, f"row {r}: {len(out_)} ids differ"
             o, g = out_.pop(), in_.pop()
             win = 2 * ulp_f32(max(abs(lg[o]), abs(lg[g])))
-            assert abs(lg[g] - lg[o]) <= win, f"row {r}: swap {o}->{g} outside 2 ULP"
+            assert abs(lg[g] - lg[o]) <= win, (
+                f"row {r}: swap {o}->{g} outside 2 ULP ({lg[o]!r} vs {lg[g]!r})")
             swaps += 1
             continue
         for a, b in zip(got, want):
             if a != b:
-                win = 2 * ulp_f32(max(abs(lg[a]), abs(lg[b])))
-                assert abs(lg[a] - lg[b]) <= win, f"row {r}: order differs outside 2 ULP"
+                if y_log is not None:
+                    win = SLACK * (abs_log[r][a] + abs_log[r][b])
+                    d = abs(y_log[r][a] - y_log[r][b])
+                else:
+                    win = 2 * ulp_f32(max(abs(lg[a]), abs(lg[b])))
+                    d = abs(lg[a] - lg[b])
+                assert d <= win, f"row {r}: ids {a},{b} trade places {d!r} apart (window {win!r})"
     return {"swap_rows": swaps, "rows": int(ids.shape[0])}

@@ -11,7 +11,7 @@ import torch
 import latent_projection_top_gb300 as route
 import oracle
 import synth
-from gates import (check_ids_end_to_end, check_latent, check_logits, check_topk_exact)
+from gates import (check_ids_end_to_end, check_latent, check_logits, check_topk_exact, record)
 from gpu_util import (DEV, bank, bits_of, oracle_rows, outputs, require_gpu, run_step,
                       to_dev_bf16)
 
@@ -107,14 +107,15 @@ def test_decode_route_step_parity(workload, rows):
         lat, lg, ids, w = run_step(plan, h, dwl, dwr, fused=True)
         lat2, lg2, ids2, w2 = run_step(plan, h, dwl, dwr, fused=False)
     sl = slice(0, rows)
-    check_latent(lat, ref["latent"][sl], ref["y_lat"][sl], ref["abs_lat"][sl])
-    check_logits(lg, ref["y_log"][sl], ref["abs_log"][sl])
+    s1 = check_latent(lat, ref["latent"][sl], ref["y_lat"][sl], ref["abs_lat"][sl])
+    s2 = check_logits(lg, ref["y_log"][sl], ref["abs_log"][sl])
     # the fused top-16 equals the oracle's top-16 on the same (GPU) logits
     ids_o, w_o = oracle.topk(lg)
-    check_topk_exact(ids, w, ids_o, w_o)
+    s3 = check_topk_exact(ids, w, ids_o, w_o)
     # end to end against the oracle's own logits
     ids_ref, _ = oracle.topk(ref["logits"][sl])
-    check_ids_end_to_end(ids, ids_ref, ref["logits"][sl])
+    s4 = check_ids_end_to_end(ids, ids_ref, ref["logits"][sl], ref["y_log"][sl], ref["abs_log"][sl])
+    record(f"decode_{workload}_r{rows}", **s1, **s2, **s3, **s4)
     # the unfused path computes the same bits
     assert np.array_equal(lat, lat2) and np.array_equal(lg.view(np.uint32), lg2.view(np.uint32))
     assert np.array_equal(ids, ids2) and np.array_equal(w.view(np.uint32), w2.view(np.uint32))
@@ -176,12 +177,13 @@ def test_prefill_ragged_parity(rows, sample):
     with route.Plan(route.PREFILL, rows) as plan:
         lat, lg, ids, w = run_step(plan, to_dev_bf16(hid[:rows]), to_dev_bf16(wl), to_dev_bf16(wr))
     sel = list(idx)
-    check_latent(lat[sel], ref["latent"], ref["y_lat"], ref["abs_lat"])
-    check_logits(lg[sel], ref["y_log"], ref["abs_log"])
+    s1 = check_latent(lat[sel], ref["latent"], ref["y_lat"], ref["abs_lat"])
+    s2 = check_logits(lg[sel], ref["y_log"], ref["abs_log"])
     ids_o, w_o = oracle.topk(lg)
-    check_topk_exact(ids, w, ids_o, w_o)
+    s3 = check_topk_exact(ids, w, ids_o, w_o)
     ids_ref, _ = oracle.topk(ref["logits"])
-    check_ids_end_to_end(ids[sel], ids_ref, ref["logits"])
+    s4 = check_ids_end_to_end(ids[sel], ids_ref, ref["logits"], ref["y_log"], ref["abs_log"])
+    record(f"prefill_ragged_r{rows}", **s1, **s2, **s3, **s4)
 
 
 def test_prefill_1024_cancel_group_sampled():
@@ -192,12 +194,20 @@ def test_prefill_1024_cancel_group_sampled():
     with route.Plan(route.PREFILL, 1024) as plan:
         lat, lg, ids, w = run_step(plan, to_dev_bf16(hid), to_dev_bf16(wl), to_dev_bf16(wr))
     sel = list(idx)
-    check_latent(lat[sel], ref["latent"], ref["y_lat"], ref["abs_lat"])
-    check_logits(lg[sel], ref["y_log"], ref["abs_log"])
+    s1 = check_latent(lat[sel], ref["latent"], ref["y_lat"], ref["abs_lat"])
+    s2 = check_logits(lg[sel], ref["y_log"], ref["abs_log"])
     ids_o, w_o = oracle.topk(lg)
-    check_topk_exact(ids, w, ids_o, w_o)
+    s3 = check_topk_exact(ids, w, ids_o, w_o)
     ids_ref, _ = oracle.topk(ref["logits"])
-    check_ids_end_to_end(ids[sel], ids_ref, ref["logits"])
+    s4 = check_ids_end_to_end(ids[sel], ids_ref, ref["logits"], ref["y_log"], ref["abs_log"])
+    record("prefill_r1024_cancel_sampled", **s1, **s2, **s3, **s4)
+    # the cancel-group columns of the sampled rows d < 448, on their own
+    cols = [(i, d) for i, d in enumerate(idx) if d < 448]
+    out = np.array([lat[d, d] for _, d in cols], np.uint16)
+    refc = np.array([ref["latent"][i, d] for i, d in cols], np.uint16)
+    yc = np.array([ref["y_lat"][i, d] for i, d in cols])
+    ac = np.array([ref["abs_lat"][i, d] for i, d in cols])
+    record("prefill_r1024_cancel_columns", **check_latent(out, refc, yc, ac, rms_bar=False))
 
 
 def test_prefill_3072_sampled_and_deterministic():
