@@ -18,7 +18,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libroute.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-SOURCES = ["proj_kernel.cu", "topk_kernel.cu", "route_api.cu"]
+SOURCES = ["decode_kernel.cu", "prefill_kernel.cu", "topk_kernel.cu", "route_api.cu"]
 HEADERS = ["common.cuh", "sm103_ptx.cuh", "topk16.cuh"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")

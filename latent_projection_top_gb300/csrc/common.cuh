@@ -18,14 +18,14 @@ constexpr int kExperts = 896;
 constexpr int kTopK = 16;
 constexpr int kDecodeMaxRows = 20;
 
-// Tiling of the projection: one tile = 128 weight columns (the MMA M side)
-// x BN token rows (the MMA N side); K is consumed 64 at a time.
+// Prefill tiling: one tile = 128 weight columns (the MMA M side) x 256 token
+// rows (the MMA N side); K is consumed 64 at a time.
 constexpr int kTileCols = 128;
 constexpr int kKBlock = 64;
 constexpr int kKBlocks = kHidden / kKBlock;                 // 112
 constexpr int kLatentTiles = kLatent / kTileCols;           // 28
 constexpr int kRouterTiles = kExperts / kTileCols;          // 7
-constexpr int kColTiles = kLatentTiles + kRouterTiles;      // 35
+constexpr int kColTiles = kLatentTiles + kRouterTiles;      // 35 (prefill tiles)
 constexpr int kProjThreads = 192;                           // 6 warps
 
 enum Mode : int { kDecode = 0, kPrefill = 1 };
@@ -33,35 +33,59 @@ enum Mode : int { kDecode = 0, kPrefill = 1 };
 // Device status bits (the kernels set them instead of hanging).
 constexpr unsigned kStatusTimeout = 1u;
 
-// Everything the projection kernel needs besides its three tensor maps.
+// Everything the prefill projection kernel needs besides its tensor maps.
 struct ProjArgs {
     int rows;            // token rows in this call
-    int mode;            // kDecode or kPrefill
-    int row_tiles;       // prefill: ceil(rows / BN); decode: 1
-    int grid;            // CTAs launched
-    int units;           // decode: kColTiles * kKBlocks (k-block units split over CTAs)
-    int fuse_topk;       // decode: the CTA finishing the last router tile runs the top-16
+    int row_tiles;       // ceil(rows / BN)
+    int grid;            // persistent CTAs launched
     int test_stall;      // test hook: skip each CTA's last copy so a wait must time out
     unsigned long long timeout_ns;  // bound on every wait inside the kernel
-    // decode split-K partition, fixed at plan time (depends on grid only):
-    int seg_base[kColTiles];   // first partial slot of column tile c
-    int seg_count[kColTiles];  // number of CTAs (partials) covering tile c
-    int cta_first[kColTiles];  // first CTA covering tile c
-    float *ws;                 // partials [slot][kDecodeMaxRows][kTileCols] FP32
-    unsigned *counters;        // [kColTiles] arrivals per tile, [kColTiles] router tiles done
     unsigned *status;          // device status word
     uint16_t *latent;          // [rows, 3584] BF16 bits
     float *logits;             // [rows, 896]
-    int32_t *ids;              // [rows, 16]   (fused top-16 only)
-    float *weights;            // [rows, 16]   (fused top-16 only)
 };
 
-// Internal launchers (defined next to their kernels).
-int proj_bn_for(int mode, int rows);
-int proj_smem_bytes(int bn);
-cudaError_t proj_configure(int bn);  // opt in to the kernel's shared memory size
-cudaError_t proj_launch(int bn, const CUtensorMap &map_h, const CUtensorMap &map_wl,
-                        const CUtensorMap &map_wr, const ProjArgs &args, cudaStream_t stream);
+// Decode split-K: 18 column tiles of 256 columns (14 latent, 4 router -- the
+// last router tile is 128 wide) x 112 k-blocks.
+constexpr int kDTileCols = 256;
+constexpr int kDLatTiles = kLatent / kDTileCols;                           // 14
+constexpr int kDRouterTiles = (kExperts + kDTileCols - 1) / kDTileCols;    // 4
+constexpr int kDTiles = kDLatTiles + kDRouterTiles;                        // 18
+constexpr int kMaxGrid = 256;
+
+struct DecodeArgs {
+    int rows;            // 1..20
+    int grid;            // CTAs of the stream kernel (<= kMaxGrid)
+    int test_stall;      // test hook: skip each CTA's last copy so a wait must time out
+    unsigned long long timeout_ns;
+    int cta_unit[kMaxGrid + 1];  // CTA g owns units [cta_unit[g], cta_unit[g+1]); unit u =
+                                 // (tile u / 112, k-block u % 112)
+    int seg_base[kDTiles];       // first partial slot of tile t
+    int seg_count[kDTiles];      // CTAs (partials) covering tile t
+    int cta_first[kDTiles];      // first CTA covering tile t
+    float2 *ws;                  // partials [slot][kDecodeMaxRows][256] as (hi, lo)
+    unsigned *status;
+    uint16_t *latent;
+    float *logits;
+    int32_t *ids;
+    float *weights;
+};
+
+// Internal launchers (defined next to their kernels).  Every launch uses
+// programmatic dependent launch (see the kernels for what each waits on).
+int prefill_smem_bytes();
+cudaError_t prefill_configure();
+cudaError_t prefill_launch(const CUtensorMap &map_h, const CUtensorMap &map_wl,
+                           const CUtensorMap &map_wr, const ProjArgs &args, cudaStream_t stream);
+constexpr int kPrefillBN = 256;
+
+int decode_bn_for(int rows);
+int decode_smem_bytes(int bn);
+cudaError_t decode_configure(int bn);
+cudaError_t decode_launch(int bn, const CUtensorMap &map_h, const CUtensorMap &map_wl,
+                          const CUtensorMap &map_wr, const DecodeArgs &args, int do_topk,
+                          cudaStream_t stream);
+
 cudaError_t topk_launch(const float *logits, int rows, int32_t *ids, float *weights,
                         cudaStream_t stream);
 

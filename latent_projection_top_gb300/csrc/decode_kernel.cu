@@ -1,0 +1,434 @@
+// Decode route step (1..20 token rows): steps a1..a4 as two kernels.
+//
+//   latent[r, n] = bf16( sum_k hidden[r, k] * W_latent[k, n] )   n < 3584
+//   logits[r, e] =       sum_k hidden[r, k] * W_router[k, e]    e < 896
+//   ids / weights = top-16 of logits[r, :]
+//
+// At decode widths the step is a stream of the 64.2 MB of weights; the
+// arithmetic is small.  It is built for that stream:
+//
+// decode_stream_kernel -- one CTA per SM.  The weights are cut into 18 column
+//   tiles of 256 columns (14 latent, 4 router; the last router tile holds
+//   128) and 112 k-blocks of 64; a CTA owns a contiguous, byte-balanced run
+//   of (tile, k-block) units.  Per unit a TMA producer brings four 64x64
+//   weight boxes (two for the narrow tile) and the hidden box into a shared
+//   memory ring; one thread issues tcgen05 MMAs (128 weight columns on M,
+//   token rows on N) into a fresh TMEM accumulator per k-block; four
+//   epilogue warps add each k-block's FP32 result into a two-float
+//   (TwoSum) running sum, so the only rounding errors left are those inside
+//   one 64-long block.  At the end of a run the CTA stores its two-float
+//   partial for its (tile, rows, 256 columns) slot.  The partition depends
+//   only on the grid, never on the data or the row count.
+//
+// decode_finish_kernel -- rows x 15 small CTAs.  Each sums the partials of
+//   one (row, latent tile) or one row of router logits in segment order
+//   (two-float), rounds once, writes, and the router CTAs run the top-16.
+//
+// Both kernels use programmatic dependent launch: the stream kernel starts
+// while the previous kernel finishes and prefetches weight boxes (model
+// parameters no predecessor writes) before `griddepcontrol.wait`; it reads
+// the hidden rows and writes scratch only after the wait.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "sm103_ptx.cuh"
+#include "topk16.cuh"
+
+namespace route {
+namespace {
+
+constexpr uint32_t kBoxBytes = 64 * 64 * 2;         // one 64-column x 64-k weight box
+constexpr uint32_t kDAStageBytes = 4 * kBoxBytes;   // 256 columns x 64 k
+constexpr int kNumAcc = 4;                          // TMEM accumulator ring (k-blocks in flight)
+
+template <int BN>
+struct DecCfg {
+    static constexpr uint32_t kBStageBytes = BN * 128;  // BN rows x 64 k, BF16
+    static constexpr uint32_t kStageBytes = kDAStageBytes + kBStageBytes;
+    static constexpr int kStages = 6;
+    static constexpr uint32_t kAccCols = 2 * BN;       // two 128-column blocks per accumulator
+    static constexpr uint32_t kTmemCols = kNumAcc * kAccCols <= 128 ? 128 : 256;
+    static constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + 256;
+    // tcgen05 kind::f16: FP32 accumulator, BF16 A (MN-major) and B (K-major),
+    // N = BN token rows, M = 128 weight columns.
+    static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) |
+                                       ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+    static_assert(BN == 16 || BN == 32, "decode row tile");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+    static_assert(kNumAcc * kAccCols <= kTmemCols, "TMEM");
+};
+
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= 1ull << 46;  // descriptor version for tcgen05
+    d |= 2ull << 61;  // 128-byte swizzle
+    return d;
+}
+
+// Error-free addition (Knuth's TwoSum): hi + x = s + e exactly; e joins lo.
+__device__ __forceinline__ void two_sum_acc(float &hi, float &lo, float x) {
+    const float s = hi + x;
+    const float bp = s - hi;
+    const float e = (hi - (s - bp)) + (x - bp);
+    hi = s;
+    lo += e;
+}
+
+__device__ __forceinline__ int tile_blocks(int t) {  // 128-column MMA blocks in tile t
+    return t == kDTiles - 1 ? 1 : 2;
+}
+
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const DecodeArgs &a,
+                                           volatile int *abort_flag) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0u) {
+            if (*abort_flag) return false;
+            if (ptx::global_timer_ns() - t0 > a.timeout_ns) {
+                *abort_flag = 1;
+                atomicOr(a.status, kStatusTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, const DecodeArgs &a) {
+    const uint64_t t0 = ptx::global_timer_ns();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (ptx::global_timer_ns() - t0 > a.timeout_ns) {
+            atomicOr(a.status, kStatusTimeout);
+            return;
+        }
+    }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kProjThreads, 1)
+    decode_stream_kernel(const __grid_constant__ CUtensorMap map_h,
+                         const __grid_constant__ CUtensorMap map_wl,
+                         const __grid_constant__ CUtensorMap map_wr,
+                         const __grid_constant__ DecodeArgs args) {
+    using C = DecCfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint32_t s_tmem_base;
+    __shared__ volatile int s_abort;
+
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    const uint32_t bars = sbase + C::kStages * C::kStageBytes;
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (C::kStages + s); };
+    auto accfull_bar = [&](int b) { return bars + 8u * (2 * C::kStages + b); };
+    auto accempty_bar = [&](int b) { return bars + 8u * (2 * C::kStages + kNumAcc + b); };
+    const uint32_t drain_bar = bars + 8u * (2 * C::kStages + 2 * kNumAcc);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int g = blockIdx.x;
+    const int u0 = args.cta_unit[g];
+    const int u1 = args.cta_unit[g + 1];
+
+    if (threadIdx.x == 0) {
+        // Let the next kernel on the stream launch as soon as SMs free up.
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        s_abort = 0;
+        for (int s = 0; s < C::kStages; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < kNumAcc; ++b) {
+            ptx::mbar_init(accfull_bar(b), 1);
+            ptx::mbar_init(accempty_bar(b), 128);
+        }
+        ptx::mbar_init(drain_bar, 1);
+        ptx::fence_barrier_init();
+        ptx::prefetch_tensormap(&map_h);
+        ptx::prefetch_tensormap(&map_wl);
+        ptx::prefetch_tensormap(&map_wr);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_addr(&s_tmem_base), C::kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = s_tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer ----------------
+            const uint64_t pol_w = ptx::policy_evict_first();
+            const uint64_t pol_h = ptx::policy_evict_last();
+            const int n_units = u1 - u0;
+            const int n_pre = n_units < C::kStages ? n_units : C::kStages;
+            auto weights_of = [&](int u, uint32_t a, uint32_t bar) {
+                const int t = u / kKBlocks, kb = u % kKBlocks;
+                const bool lat = t < kDLatTiles;
+                const CUtensorMap *wmap = lat ? &map_wl : &map_wr;
+                const int x0 = (lat ? t : t - kDLatTiles) * kDTileCols;
+                const int nbox = 2 * tile_blocks(t);
+                for (int b = 0; b < nbox; ++b)
+                    ptx::tma_load_2d(a + b * kBoxBytes, wmap, bar, x0 + 64 * b, kb * kKBlock, pol_w);
+            };
+            auto stage_bytes = [&](int u) {
+                return (uint32_t)(2 * tile_blocks(u / kKBlocks)) * kBoxBytes + C::kBStageBytes;
+            };
+            uint32_t armed = 0u, armed_par = 0u;
+            // Weight boxes for the first stages go out before the grid
+            // dependency resolves (no predecessor writes the weights).
+            for (int i = 0; i < n_pre; ++i) {
+                const uint32_t a = sbase + i * C::kStageBytes;
+                ptx::mbar_arrive_expect_tx(full_bar(i), stage_bytes(u0 + i));
+                weights_of(u0 + i, a, full_bar(i));
+                armed |= 1u << i;
+            }
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            for (int i = 0; i < n_pre; ++i) {
+                const int kb = (u0 + i) % kKBlocks;
+                if (args.test_stall && i == n_units - 1) continue;  // test hook
+                ptx::tma_load_2d(sbase + i * C::kStageBytes + kDAStageBytes, &map_h, full_bar(i),
+                                 kb * kKBlock, 0, pol_h);
+            }
+            bool ok = true;
+            for (int i = n_pre; i < n_units; ++i) {
+                const int s = i % C::kStages;
+                const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
+                if (!wait_phase(empty_bar(s), ph ^ 1u, args, &s_abort)) {
+                    ok = false;
+                    break;
+                }
+                if (args.test_stall && i == n_units - 1) continue;  // test hook: never filled
+                const uint32_t a = sbase + s * C::kStageBytes;
+                ptx::mbar_arrive_expect_tx(full_bar(s), stage_bytes(u0 + i));
+                weights_of(u0 + i, a, full_bar(s));
+                ptx::tma_load_2d(a + kDAStageBytes, &map_h, full_bar(s), ((u0 + i) % kKBlocks) * kKBlock,
+                                 0, pol_h);
+                armed |= 1u << s;
+                armed_par = (armed_par & ~(1u << s)) | (ph << s);
+            }
+            if (!ok || s_abort) {  // let every issued copy land before the CTA may exit
+                for (int s = 0; s < C::kStages; ++s)
+                    if (armed & (1u << s)) wait_drain(full_bar(s), (armed_par >> s) & 1u, args);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer: one fresh accumulator per k-block ----------------
+            bool ok = true;
+            for (int i = 0; i < u1 - u0 && ok; ++i) {
+                const int t = (u0 + i) / kKBlocks;
+                const int s = i % C::kStages;
+                const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
+                const int buf = i % kNumAcc;
+                const uint32_t use = (uint32_t)(i / kNumAcc);
+                if (!wait_phase(accempty_bar(buf), (use & 1u) ^ 1u, args, &s_abort)) break;
+                if (!wait_phase(full_bar(s), ph, args, &s_abort)) break;
+                ptx::tc_fence_after();
+                const uint32_t a = sbase + s * C::kStageBytes;
+                const uint32_t b = a + kDAStageBytes;
+                const int nblk = tile_blocks(t);
+                for (int blk = 0; blk < nblk; ++blk) {
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(buf * C::kAccCols + blk * BN);
+#pragma unroll
+                    for (int kk = 0; kk < kKBlock / 16; ++kk) {
+                        // A: block blk is boxes 2blk, 2blk+1 (8192 B apart, LBO);
+                        //    k advances 16 rows = two 1024-B swizzle atoms (SBO 1024).
+                        // B: k advances 32 B within the 128-B swizzled row.
+                        const uint64_t da =
+                            smem_desc(a + blk * 2 * kBoxBytes + kk * 2048u, kBoxBytes, 1024u);
+                        const uint64_t db = smem_desc(b + kk * 32u, 16u, 1024u);
+                        ptx::mma_bf16(d_tmem, da, db, C::kIdesc, kk > 0 ? 1u : 0u);
+                    }
+                }
+                ptx::mma_commit(empty_bar(s));
+                ptx::mma_commit(accfull_bar(buf));
+                (void)ok;
+            }
+            ptx::mma_commit(drain_bar);  // every MMA retired before TMEM is freed
+            wait_drain(drain_bar, 0u, args);
+        }
+    } else {
+        // ---------------- epilogue: two-float sums of the k-block results ----------------
+        const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+        const int col = 32 * quarter + lane;
+        const int rows = args.rows;
+        asm volatile("griddepcontrol.wait;" ::: "memory");  // scratch may still be read by the predecessor
+        float hi[2][BN], lo[2][BN];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int r = 0; r < BN; ++r) hi[h][r] = lo[h][r] = 0.f;
+        for (int i = 0; i < u1 - u0; ++i) {
+            const int u = u0 + i;
+            const int t = u / kKBlocks;
+            const int buf = i % kNumAcc;
+            const uint32_t use = (uint32_t)(i / kNumAcc);
+            const bool ok = wait_phase(accfull_bar(buf), use & 1u, args, &s_abort);
+            if (!ptx::named_bar_and(1, 128, ok)) break;
+            ptx::tc_fence_after();
+            const int nblk = tile_blocks(t);
+            const uint32_t taddr =
+                tmem_base + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * C::kAccCols);
+            uint32_t v[2][BN];
+#pragma unroll
+            for (int ch = 0; ch < BN / 16; ++ch) {
+                ptx::tmem_ld_x16(taddr + ch * 16, *reinterpret_cast<uint32_t(*)[16]>(&v[0][ch * 16]));
+                if (nblk == 2)
+                    ptx::tmem_ld_x16(taddr + BN + ch * 16,
+                                     *reinterpret_cast<uint32_t(*)[16]>(&v[1][ch * 16]));
+            }
+            ptx::tmem_ld_wait();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(accempty_bar(buf));
+#pragma unroll
+            for (int r = 0; r < BN; ++r) two_sum_acc(hi[0][r], lo[0][r], __uint_as_float(v[0][r]));
+            if (nblk == 2) {
+#pragma unroll
+                for (int r = 0; r < BN; ++r) two_sum_acc(hi[1][r], lo[1][r], __uint_as_float(v[1][r]));
+            }
+            const bool seg_end = (i == u1 - u0 - 1) || ((u + 1) % kKBlocks == 0);
+            if (seg_end) {
+                const int slot = args.seg_base[t] + (g - args.cta_first[t]);
+                float2 *part = args.ws + (size_t)slot * kDecodeMaxRows * kDTileCols;
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int r = 0; r < BN; ++r) {
+                        if (r < rows && h < nblk)
+                            part[r * kDTileCols + h * 128 + col] = make_float2(hi[h][r], lo[h][r]);
+                        hi[h][r] = lo[h][r] = 0.f;
+                    }
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+// Sum the partial slots of one (tile, row) for the thread's column pair, in
+// segment order, as a two-float value.
+__device__ __forceinline__ void sum_slots(const DecodeArgs &a, int t, int r, int cc, float &h0,
+                                          float &l0, float &h1, float &l1) {
+    const int base = a.seg_base[t], n = a.seg_count[t];
+    h0 = l0 = h1 = l1 = 0.f;
+    for (int s0 = 0; s0 < n; s0 += 8) {
+        float4 p[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (s0 + j < n)
+                p[j] = __ldcg(reinterpret_cast<const float4 *>(
+                    a.ws + ((size_t)(base + s0 + j) * kDecodeMaxRows + r) * kDTileCols + cc));
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (s0 + j < n) {
+                two_sum_acc(h0, l0, p[j].x);
+                l0 += p[j].y;
+                two_sum_acc(h1, l1, p[j].z);
+                l1 += p[j].w;
+            }
+    }
+}
+
+__device__ __forceinline__ uint16_t bf16_bits(float x) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+// blocks [0, rows): router row + top-16;  blocks [rows, rows*15): (row, latent tile)
+__global__ void __launch_bounds__(128) decode_finish_kernel(const __grid_constant__ DecodeArgs a,
+                                                            int do_topk) {
+    __shared__ uint2 cand[kCandMax];
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the stream kernel's partials are complete
+    const int rows = a.rows;
+    const int tid = threadIdx.x;
+    if ((int)blockIdx.x < rows) {
+        const int r = blockIdx.x;
+        float *lrow = a.logits + (size_t)r * kExperts;
+        for (int i = tid; i < kExperts / 2; i += 128) {
+            const int c = 2 * i;
+            const int t = kDLatTiles + c / kDTileCols;
+            float h0, l0, h1, l1;
+            sum_slots(a, t, r, c % kDTileCols, h0, l0, h1, l1);
+            *reinterpret_cast<float2 *>(lrow + c) = make_float2(h0 + l0, h1 + l1);
+        }
+        if (!do_topk) return;
+        __threadfence();
+        __syncthreads();
+        if (tid < 32)
+            topk16_warp(lrow, a.ids + (size_t)r * kTopK, a.weights + (size_t)r * kTopK, tid, cand);
+    } else {
+        const int b = blockIdx.x - rows;
+        const int r = b / kDLatTiles, t = b % kDLatTiles;
+        const int cc = 2 * tid;
+        float h0, l0, h1, l1;
+        sum_slots(a, t, r, cc, h0, l0, h1, l1);
+        const uint32_t packed = (uint32_t)bf16_bits(h0 + l0) | ((uint32_t)bf16_bits(h1 + l1) << 16);
+        *reinterpret_cast<uint32_t *>(a.latent + (size_t)r * kLatent + t * kDTileCols + cc) = packed;
+    }
+}
+
+template <int BN>
+cudaError_t stream_configure() {
+    return cudaFuncSetAttribute(decode_stream_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)DecCfg<BN>::kSmemBytes);
+}
+
+cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              cudaLaunchAttribute *attr) {
+    cudaLaunchConfig_t c = {};
+    c.gridDim = grid;
+    c.blockDim = block;
+    c.dynamicSmemBytes = smem;
+    c.stream = stream;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    c.attrs = attr;
+    c.numAttrs = 1;
+    return c;
+}
+
+template <int BN>
+cudaError_t stream_launch(const CUtensorMap &mh, const CUtensorMap &ml, const CUtensorMap &mr,
+                          const DecodeArgs &a, cudaStream_t stream) {
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t c =
+        pdl_config(dim3(a.grid), dim3(kProjThreads), DecCfg<BN>::kSmemBytes, stream, attr);
+    return cudaLaunchKernelEx(&c, decode_stream_kernel<BN>, mh, ml, mr, a);
+}
+
+}  // namespace
+
+int decode_bn_for(int rows) { return rows <= 16 ? 16 : 32; }
+
+int decode_smem_bytes(int bn) {
+    return bn == 16 ? (int)DecCfg<16>::kSmemBytes : bn == 32 ? (int)DecCfg<32>::kSmemBytes : -1;
+}
+
+cudaError_t decode_configure(int bn) {
+    return bn == 16 ? stream_configure<16>() : bn == 32 ? stream_configure<32>() : cudaErrorInvalidValue;
+}
+
+cudaError_t decode_launch(int bn, const CUtensorMap &map_h, const CUtensorMap &map_wl,
+                          const CUtensorMap &map_wr, const DecodeArgs &args, int do_topk,
+                          cudaStream_t stream) {
+    cudaError_t e = bn == 16   ? stream_launch<16>(map_h, map_wl, map_wr, args, stream)
+                    : bn == 32 ? stream_launch<32>(map_h, map_wl, map_wr, args, stream)
+                               : cudaErrorInvalidValue;
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t c = pdl_config(dim3(args.rows * (1 + kDLatTiles)), dim3(128), 0, stream, attr);
+    return cudaLaunchKernelEx(&c, decode_finish_kernel, args, do_topk);
+}
+
+}  // namespace route

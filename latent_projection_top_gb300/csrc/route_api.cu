@@ -20,12 +20,13 @@ struct route_plan {
     int mode;
     int rows;
     int device;
-    int bn;
+    int bn;                   // decode: 16 or 32 token rows per MMA; prefill: 256
     int grid;
     int segments;
-    ProjArgs base;            // filled at prepare; per-call pointers added at launch
-    float *ws;                // decode split-K partials
-    unsigned *words;          // counters [kColTiles + 1] then status, zeroed at prepare
+    ProjArgs pre;             // prefill launch arguments (per-call pointers added at launch)
+    DecodeArgs dec;           // decode launch arguments, incl. the split-K partition
+    float2 *ws;               // decode split-K partials
+    unsigned *words;          // device status word (+ spare)
     uint8_t *staging;         // device staging for route_step_host
     size_t staging_bytes;
 };
@@ -150,26 +151,44 @@ route_status check_plan(const route_plan *p) {
     return ROUTE_OK;
 }
 
-route_status launch_proj(const route_plan *p, const void *hidden, const void *W_latent,
-                         const void *W_router, void *latent, float *logits, int32_t *ids,
-                         float *weights, int fuse, cudaStream_t stream) {
-    CUtensorMap mh, ml, mr;
+route_status encode_all(const route_plan *p, const void *hidden, const void *W_latent,
+                        const void *W_router, CUtensorMap *mh, CUtensorMap *ml, CUtensorMap *mr) {
     route_status st;
-    if ((st = encode_2d(&mh, hidden, kHidden, (uint64_t)p->rows, kKBlock, (uint32_t)p->bn,
+    if ((st = encode_2d(mh, hidden, kHidden, (uint64_t)p->rows, kKBlock, (uint32_t)p->bn,
                         "hidden")) != ROUTE_OK)
         return st;
-    if ((st = encode_2d(&ml, W_latent, kLatent, kHidden, 64, kKBlock, "W_latent")) != ROUTE_OK)
+    if ((st = encode_2d(ml, W_latent, kLatent, kHidden, 64, kKBlock, "W_latent")) != ROUTE_OK)
         return st;
-    if ((st = encode_2d(&mr, W_router, kExperts, kHidden, 64, kKBlock, "W_router")) != ROUTE_OK)
-        return st;
-    ProjArgs a = p->base;
-    a.latent = static_cast<uint16_t *>(latent);
-    a.logits = logits;
-    a.ids = ids;
-    a.weights = weights;
-    a.fuse_topk = fuse;
-    cudaError_t e = proj_launch(p->bn, mh, ml, mr, a, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "projection kernel launch");
+    return encode_2d(mr, W_router, kExperts, kHidden, 64, kKBlock, "W_router");
+}
+
+// The projection (and, for decode with do_topk, the top-16) of one step.
+route_status launch_forward(const route_plan *p, const void *hidden, const void *W_latent,
+                            const void *W_router, void *latent, float *logits, int32_t *ids,
+                            float *weights, int do_topk, cudaStream_t stream) {
+    CUtensorMap mh, ml, mr;
+    route_status st = encode_all(p, hidden, W_latent, W_router, &mh, &ml, &mr);
+    if (st != ROUTE_OK) return st;
+    cudaError_t e;
+    if (p->mode == ROUTE_DECODE) {
+        DecodeArgs a = p->dec;
+        a.latent = static_cast<uint16_t *>(latent);
+        a.logits = logits;
+        a.ids = ids;
+        a.weights = weights;
+        e = decode_launch(p->bn, mh, ml, mr, a, do_topk, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+    } else {
+        ProjArgs a = p->pre;
+        a.latent = static_cast<uint16_t *>(latent);
+        a.logits = logits;
+        e = prefill_launch(mh, ml, mr, a, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "prefill kernel launch");
+        if (do_topk) {
+            e = topk_launch(logits, p->rows, ids, weights, stream);
+            if (e != cudaSuccess) return cuda_fail(e, "top-16 kernel launch");
+        }
+    }
     return ROUTE_OK;
 }
 
@@ -199,14 +218,40 @@ route_status check_topk_args(const route_plan *p, const float *logits, const int
 route_status run_step(const route_plan *p, const void *hidden, const void *W_latent,
                       const void *W_router, void *latent, float *logits, int32_t *ids,
                       float *weights, cudaStream_t stream) {
-    if (p->mode == ROUTE_DECODE)
-        return launch_proj(p, hidden, W_latent, W_router, latent, logits, ids, weights, 1, stream);
-    route_status st =
-        launch_proj(p, hidden, W_latent, W_router, latent, logits, nullptr, nullptr, 0, stream);
-    if (st != ROUTE_OK) return st;
-    cudaError_t e = topk_launch(logits, p->rows, ids, weights, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "top-16 kernel launch");
-    return ROUTE_OK;
+    return launch_forward(p, hidden, W_latent, W_router, latent, logits, ids, weights, 1, stream);
+}
+
+// Decode split-K partition: CTA g owns a contiguous run of (tile, k-block)
+// units, balanced by bytes (the last router tile's units are half as wide).
+void decode_partition(DecodeArgs &a, int grid, int *segments) {
+    const int U = kDTiles * kKBlocks;
+    auto cost = [](int u) { return (u / kKBlocks) == kDTiles - 1 ? 1 : 2; };
+    long long total = 0;
+    for (int u = 0; u < U; ++u) total += cost(u);
+    a.grid = grid;
+    a.cta_unit[0] = 0;
+    long long acc = 0;
+    int u = 0;
+    for (int g = 1; g < grid; ++g) {
+        const long long target = total * g / grid;
+        while (u < U && acc + cost(u) <= target) acc += cost(u++);
+        a.cta_unit[g] = u;
+    }
+    a.cta_unit[grid] = U;
+    int slots = 0;
+    for (int t = 0; t < kDTiles; ++t) {
+        const int first_u = t * kKBlocks, last_u = first_u + kKBlocks - 1;
+        int g_first = -1, g_last = -1;
+        for (int g = 0; g < grid; ++g) {
+            if (a.cta_unit[g] <= first_u && first_u < a.cta_unit[g + 1]) g_first = g;
+            if (a.cta_unit[g] <= last_u && last_u < a.cta_unit[g + 1]) g_last = g;
+        }
+        a.cta_first[t] = g_first;
+        a.seg_count[t] = g_last - g_first + 1;
+        a.seg_base[t] = slots;
+        slots += a.seg_count[t];
+    }
+    *segments = slots;
 }
 
 }  // namespace
@@ -249,68 +294,51 @@ route_status route_prepare(int mode, int rows, int device, route_plan **out) {
     p->mode = mode;
     p->rows = rows;
     p->device = device;
-    p->bn = proj_bn_for(mode, rows);
-    const int smem = proj_smem_bytes(p->bn);
+    p->bn = mode == ROUTE_DECODE ? decode_bn_for(rows) : kPrefillBN;
+    const int smem = mode == ROUTE_DECODE ? decode_smem_bytes(p->bn) : prefill_smem_bytes();
     if (smem < 0 || (size_t)smem > prop.sharedMemPerBlockOptin) {
         free_plan(p);
         return fail(ROUTE_ERR_DEVICE, "kernel needs %d B of shared memory per block; device allows %zu",
                     smem, (size_t)prop.sharedMemPerBlockOptin);
     }
-    if ((e = proj_configure(p->bn)) != cudaSuccess) {
+    if ((e = mode == ROUTE_DECODE ? decode_configure(p->bn) : prefill_configure()) != cudaSuccess) {
         free_plan(p);
         return cuda_fail(e, "cudaFuncSetAttribute");
     }
-
-    ProjArgs &a = p->base;
-    memset(&a, 0, sizeof a);
-    a.rows = rows;
-    a.mode = mode;
-    a.timeout_ns = kDefaultTimeoutNs;
-    const int sms = prop.multiProcessorCount;
-    if (mode == ROUTE_DECODE) {
-        a.units = kColTiles * kKBlocks;
-        a.row_tiles = 1;
-        a.grid = sms < a.units ? sms : a.units;
-        // Split-K partition: CTA g owns units [g*U/G, (g+1)*U/G); unit u is
-        // (column tile u / 112, k-block u % 112).  Tables per column tile.
-        const long long U = a.units, G = a.grid;
-        int slots = 0;
-        for (int c = 0; c < kColTiles; ++c) {
-            const long long first_u = (long long)c * kKBlocks, last_u = first_u + kKBlocks - 1;
-            int g_first = -1, g_last = -1;
-            for (int g = 0; g < a.grid; ++g) {
-                const long long u0 = g * U / G, u1 = (g + 1) * U / G;
-                if (u0 <= first_u && first_u < u1) g_first = g;
-                if (u0 <= last_u && last_u < u1) g_last = g;
-            }
-            a.cta_first[c] = g_first;
-            a.seg_count[c] = g_last - g_first + 1;
-            a.seg_base[c] = slots;
-            slots += a.seg_count[c];
-        }
-        p->segments = slots;
-        const size_t ws_bytes = (size_t)slots * kDecodeMaxRows * kTileCols * sizeof(float);
-        if ((e = cudaMalloc(&p->ws, ws_bytes)) != cudaSuccess) {
-            free_plan(p);
-            return cuda_fail(e, "cudaMalloc(split-K scratch)");
-        }
-    } else {
-        a.units = 0;
-        a.row_tiles = (rows + p->bn - 1) / p->bn;
-        const int tiles = kColTiles * a.row_tiles;
-        a.grid = sms < tiles ? sms : tiles;
-        p->segments = tiles;
-    }
-    p->grid = a.grid;
     const size_t words = 64;
     if ((e = cudaMalloc(&p->words, words * sizeof(unsigned))) != cudaSuccess ||
         (e = cudaMemset(p->words, 0, words * sizeof(unsigned))) != cudaSuccess) {
         free_plan(p);
-        return cuda_fail(e, "cudaMalloc(counters)");
+        return cuda_fail(e, "cudaMalloc(status word)");
     }
-    a.ws = p->ws;
-    a.counters = p->words;
-    a.status = p->words + (kColTiles + 1);
+    const int sms = prop.multiProcessorCount;
+    memset(&p->pre, 0, sizeof p->pre);
+    memset(&p->dec, 0, sizeof p->dec);
+    if (mode == ROUTE_DECODE) {
+        DecodeArgs &a = p->dec;
+        a.rows = rows;
+        a.timeout_ns = kDefaultTimeoutNs;
+        const int grid = sms < kMaxGrid ? sms : kMaxGrid;
+        decode_partition(a, grid, &p->segments);
+        const size_t ws_bytes = (size_t)p->segments * kDecodeMaxRows * kDTileCols * sizeof(float2);
+        if ((e = cudaMalloc(&p->ws, ws_bytes)) != cudaSuccess) {
+            free_plan(p);
+            return cuda_fail(e, "cudaMalloc(split-K scratch)");
+        }
+        a.ws = p->ws;
+        a.status = p->words;
+        p->grid = a.grid;
+    } else {
+        ProjArgs &a = p->pre;
+        a.rows = rows;
+        a.timeout_ns = kDefaultTimeoutNs;
+        a.row_tiles = (rows + p->bn - 1) / p->bn;
+        const int tiles = kColTiles * a.row_tiles;
+        a.grid = sms < tiles ? sms : tiles;
+        a.status = p->words;
+        p->segments = tiles;
+        p->grid = a.grid;
+    }
     p->staging_bytes = staging_size(rows);
     if ((e = cudaMalloc(&p->staging, p->staging_bytes)) != cudaSuccess) {
         free_plan(p);
@@ -339,8 +367,8 @@ route_status latent_router_forward(const route_plan *plan, const void *hidden,
     if (st != ROUTE_OK) return st;
     DeviceGuard guard(plan->device);
     if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
-    return launch_proj(plan, hidden, W_latent, W_router, latent, logits, nullptr, nullptr, 0,
-                       static_cast<cudaStream_t>(stream));
+    return launch_forward(plan, hidden, W_latent, W_router, latent, logits, nullptr, nullptr, 0,
+                          static_cast<cudaStream_t>(stream));
 }
 
 route_status topk16_select(const route_plan *plan, const float *logits, int32_t *ids,
@@ -410,11 +438,11 @@ route_status route_device_status(const route_plan *plan) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
     unsigned status = 0;
-    if ((e = cudaMemcpy(&status, plan->base.status, sizeof status, cudaMemcpyDeviceToHost)) !=
+    if ((e = cudaMemcpy(&status, plan->words, sizeof status, cudaMemcpyDeviceToHost)) !=
         cudaSuccess)
         return cuda_fail(e, "read device status");
     if (status == 0) return ROUTE_OK;
-    cudaMemset(plan->words, 0, 64 * sizeof(unsigned));  // counters and status
+    cudaMemset(plan->words, 0, 64 * sizeof(unsigned));  // the status word
     cudaDeviceSynchronize();
     return fail(ROUTE_ERR_DEVICE_TIMEOUT,
                 "a kernel gave up waiting (status 0x%x); that launch's outputs are invalid", status);
@@ -423,8 +451,9 @@ route_status route_device_status(const route_plan *plan) {
 route_status route_test_stall(route_plan *plan, int enable, uint64_t timeout_ns) {
     route_status st = check_plan(plan);
     if (st != ROUTE_OK) return st;
-    plan->base.test_stall = enable ? 1 : 0;
-    plan->base.timeout_ns = enable ? (timeout_ns ? timeout_ns : 1000000ull) : kDefaultTimeoutNs;
+    const unsigned long long t = enable ? (timeout_ns ? timeout_ns : 1000000ull) : kDefaultTimeoutNs;
+    plan->pre.test_stall = plan->dec.test_stall = enable ? 1 : 0;
+    plan->pre.timeout_ns = plan->dec.timeout_ns = t;
     return ROUTE_OK;
 }
 

@@ -16,8 +16,9 @@
 // ties) take the same 16 picks over all 896 keys.  Both give the unique
 // ranking above.
 //
-// Weights: w_i = s_i / sum_j s_j, s_i = 1 / (1 + exp(-logit_i)), evaluated in
-// double and rounded once to FP32 (the library's stated convention).
+// Weights: w_i = s_i / sum_j s_j, s_i = 1 / (1 + exp(-logit_i)) (the
+// library's stated convention), in FP32 with compensated (two-float) steps
+// so that the only sizeable error left is that of expf.
 #pragma once
 
 #include <cstdint>
@@ -143,15 +144,47 @@ __device__ __forceinline__ void topk16_warp(const float *row, int32_t *ids_out, 
         }
     }
 
-    double s = 0.0;
-    if (lane < 16) s = 1.0 / (1.0 + exp(-(double)key_to_float(mine_key)));
-    double total_s = s;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) total_s += __shfl_xor_sync(0xFFFFFFFFu, total_s, off);
-    total_s = __shfl_sync(0xFFFFFFFFu, total_s, 0);  // one association order for every lane
+    // Routing weights, FP32 only: t = exp(-|v|) by expf (never overflows);
+    // 1 + t is kept exactly as a two-float (TwoSum), q = 1 / (1 + t) as a
+    // two-float (FMA residual), s = q (v >= 0) or t * q (v < 0); the 16 s are
+    // summed as two-floats in a fixed tree order; w = s / S is rounded once.
+    float s_hi = 0.f, s_lo = 0.f;
     if (lane < 16) {
+        const float v = key_to_float(mine_key);
+        const float t = expf(-fabsf(v));
+        const float d_hi = 1.0f + t;
+        const float bp = d_hi - 1.0f;
+        const float d_lo = (1.0f - (d_hi - bp)) + (t - bp);
+        const float q_hi = 1.0f / d_hi;
+        float r = fmaf(-q_hi, d_hi, 1.0f);
+        r = fmaf(-q_hi, d_lo, r);
+        const float q_lo = q_hi * r;
+        if (v >= 0.0f || v != v) {
+            s_hi = q_hi;
+            s_lo = q_lo;
+        } else {  // t * (q_hi + q_lo) as a two-float
+            s_hi = t * q_hi;
+            s_lo = fmaf(t, q_hi, -s_hi) + t * q_lo;
+        }
+    }
+    float tot_hi = s_hi, tot_lo = s_lo;
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) {
+        const float o_hi = __shfl_down_sync(0xFFFFFFFFu, tot_hi, off);
+        const float o_lo = __shfl_down_sync(0xFFFFFFFFu, tot_lo, off);
+        const float sum = tot_hi + o_hi;
+        const float bp = sum - tot_hi;
+        const float e = (tot_hi - (sum - bp)) + (o_hi - bp);
+        tot_hi = sum;
+        tot_lo = tot_lo + o_lo + e;
+    }
+    tot_hi = __shfl_sync(0xFFFFFFFFu, tot_hi, 0);  // lane 0 holds the fixed-order total
+    tot_lo = __shfl_sync(0xFFFFFFFFu, tot_lo, 0);
+    if (lane < 16) {
+        const float q0 = s_hi / tot_hi;
+        const float res = fmaf(-q0, tot_hi, s_hi) + s_lo - q0 * tot_lo;
         ids_out[lane] = (int32_t)mine_id;
-        w_out[lane] = (float)(s / total_s);
+        w_out[lane] = q0 + res / tot_hi;
     }
 }
 
