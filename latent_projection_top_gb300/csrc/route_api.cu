@@ -25,7 +25,7 @@ struct route_plan {
     int segments;
     ProjArgs pre;             // prefill launch arguments (per-call pointers added at launch)
     DecodeArgs dec;           // decode launch arguments, incl. the split-K partition
-    float2 *ws;               // decode split-K partials
+    float2 *ws;               // decode cluster partials
     unsigned *words;          // device status word (+ spare)
     uint8_t *staging;         // device staging for route_step_host
     size_t staging_bytes;
@@ -176,7 +176,8 @@ route_status launch_forward(const route_plan *p, const void *hidden, const void 
         a.logits = logits;
         a.ids = ids;
         a.weights = weights;
-        e = decode_launch(p->bn, mh, ml, mr, a, do_topk, stream);
+        a.fuse_topk = do_topk;
+        e = decode_launch(p->bn, mh, ml, mr, a, stream);
         if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
     } else {
         ProjArgs a = p->pre;
@@ -219,39 +220,6 @@ route_status run_step(const route_plan *p, const void *hidden, const void *W_lat
                       const void *W_router, void *latent, float *logits, int32_t *ids,
                       float *weights, cudaStream_t stream) {
     return launch_forward(p, hidden, W_latent, W_router, latent, logits, ids, weights, 1, stream);
-}
-
-// Decode split-K partition: CTA g owns a contiguous run of (tile, k-block)
-// units, balanced by bytes (the last router tile's units are half as wide).
-void decode_partition(DecodeArgs &a, int grid, int *segments) {
-    const int U = kDTiles * kKBlocks;
-    auto cost = [](int u) { return (u / kKBlocks) == kDTiles - 1 ? 1 : 2; };
-    long long total = 0;
-    for (int u = 0; u < U; ++u) total += cost(u);
-    a.grid = grid;
-    a.cta_unit[0] = 0;
-    long long acc = 0;
-    int u = 0;
-    for (int g = 1; g < grid; ++g) {
-        const long long target = total * g / grid;
-        while (u < U && acc + cost(u) <= target) acc += cost(u++);
-        a.cta_unit[g] = u;
-    }
-    a.cta_unit[grid] = U;
-    int slots = 0;
-    for (int t = 0; t < kDTiles; ++t) {
-        const int first_u = t * kKBlocks, last_u = first_u + kKBlocks - 1;
-        int g_first = -1, g_last = -1;
-        for (int g = 0; g < grid; ++g) {
-            if (a.cta_unit[g] <= first_u && first_u < a.cta_unit[g + 1]) g_first = g;
-            if (a.cta_unit[g] <= last_u && last_u < a.cta_unit[g + 1]) g_last = g;
-        }
-        a.cta_first[t] = g_first;
-        a.seg_count[t] = g_last - g_first + 1;
-        a.seg_base[t] = slots;
-        slots += a.seg_count[t];
-    }
-    *segments = slots;
 }
 
 }  // namespace
@@ -305,29 +273,40 @@ route_status route_prepare(int mode, int rows, int device, route_plan **out) {
         free_plan(p);
         return cuda_fail(e, "cudaFuncSetAttribute");
     }
-    const size_t words = 64;
-    if ((e = cudaMalloc(&p->words, words * sizeof(unsigned))) != cudaSuccess ||
-        (e = cudaMemset(p->words, 0, words * sizeof(unsigned))) != cudaSuccess) {
+    if ((e = cudaMalloc(&p->words, kWords * sizeof(unsigned))) != cudaSuccess ||
+        (e = cudaMemset(p->words, 0, kWords * sizeof(unsigned))) != cudaSuccess) {
         free_plan(p);
-        return cuda_fail(e, "cudaMalloc(status word)");
+        return cuda_fail(e, "cudaMalloc(device words)");
     }
     const int sms = prop.multiProcessorCount;
     memset(&p->pre, 0, sizeof p->pre);
     memset(&p->dec, 0, sizeof p->dec);
     if (mode == ROUTE_DECODE) {
+        // The decode kernel needs all 36 of its 4-CTA clusters resident at
+        // once (its top-16 CTAs wait for the router slices).
+        int clusters = 0;
+        if ((e = decode_max_clusters(p->bn, &clusters)) != cudaSuccess) {
+            free_plan(p);
+            return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
+        }
+        if (clusters < kDClusters) {
+            free_plan(p);
+            return fail(ROUTE_ERR_DEVICE,
+                        "decode needs %d co-resident 4-CTA clusters; device %d holds %d", kDClusters,
+                        device, clusters);
+        }
         DecodeArgs &a = p->dec;
         a.rows = rows;
         a.timeout_ns = kDefaultTimeoutNs;
-        const int grid = sms < kMaxGrid ? sms : kMaxGrid;
-        decode_partition(a, grid, &p->segments);
-        const size_t ws_bytes = (size_t)p->segments * kDecodeMaxRows * kDTileCols * sizeof(float2);
+        const size_t ws_bytes = (size_t)kDTiles * 2 * kDecodeMaxRows * kDTileCols * sizeof(float2);
         if ((e = cudaMalloc(&p->ws, ws_bytes)) != cudaSuccess) {
             free_plan(p);
             return cuda_fail(e, "cudaMalloc(split-K scratch)");
         }
         a.ws = p->ws;
-        a.status = p->words;
-        p->grid = a.grid;
+        a.words = p->words;
+        p->grid = kDGrid;
+        p->segments = kDGrid;
     } else {
         ProjArgs &a = p->pre;
         a.rows = rows;
@@ -335,7 +314,7 @@ route_status route_prepare(int mode, int rows, int device, route_plan **out) {
         a.row_tiles = (rows + p->bn - 1) / p->bn;
         const int tiles = kColTiles * a.row_tiles;
         a.grid = sms < tiles ? sms : tiles;
-        a.status = p->words;
+        a.status = p->words + kWordStatus;
         p->segments = tiles;
         p->grid = a.grid;
     }
@@ -442,7 +421,7 @@ route_status route_device_status(const route_plan *plan) {
         cudaSuccess)
         return cuda_fail(e, "read device status");
     if (status == 0) return ROUTE_OK;
-    cudaMemset(plan->words, 0, 64 * sizeof(unsigned));  // the status word
+    cudaMemset(plan->words, 0, kWords * sizeof(unsigned));  // status and counters
     cudaDeviceSynchronize();
     return fail(ROUTE_ERR_DEVICE_TIMEOUT,
                 "a kernel gave up waiting (status 0x%x); that launch's outputs are invalid", status);

@@ -12,9 +12,10 @@
 // largest of the 32 lane maxima is a lower bound on the 16th largest key
 // (at least 16 lanes hold a key >= T), so only keys >= T can be picked.
 // Those candidates (usually a few dozen) are compacted into shared memory and
-// the 16 picks are made among them; rows with more than 64 candidates (heavy
-// ties) take the same 16 picks over all 896 keys.  Both give the unique
-// ranking above.
+// each finds its rank among them by counting; ranks 0..15 are the picks.
+// Rows with more than 64 candidates (heavy ties) take 16 rounds of
+// (largest key, smallest id) warp reductions over all 896 keys instead.
+// Both give the unique ranking above.
 //
 // Weights: w_i = s_i / sum_j s_j, s_i = 1 / (1 + exp(-logit_i)) (the
 // library's stated convention), in FP32 with compensated (two-float) steps
@@ -92,24 +93,27 @@ __device__ __forceinline__ void topk16_warp(const float *row, int32_t *ids_out, 
         for (int j = 0; j < kPerLane; ++j)
             if (key[j] >= T) cand[pos++] = make_uint2(key[j], (uint32_t)(32 * j + lane));
         __syncwarp();
-        uint2 c0 = make_uint2(0u, 0xFFFFFFFFu), c1 = make_uint2(0u, 0xFFFFFFFFu);
-        if ((uint32_t)lane < total) c0 = cand[lane];
-        if ((uint32_t)lane + 32u < total) c1 = cand[lane + 32];
-        __syncwarp();
-#pragma unroll 1
-        for (int i = 0; i < 16; ++i) {
-            const bool second = c1.x > c0.x || (c1.x == c0.x && c1.y < c0.y);
-            const uint32_t bk = second ? c1.x : c0.x;
-            const uint32_t bi = second ? c1.y : c0.y;
-            const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, bk);
-            const uint32_t pick = __reduce_min_sync(0xFFFFFFFFu, bk == top ? bi : 0xFFFFFFFFu);
-            if (lane == i) {
-                mine_key = top;
-                mine_id = pick;
-            }
-            if (c0.y == pick) c0.x = 0u;
-            if (c1.y == pick) c1.x = 0u;
+        // Each candidate's rank = how many candidates precede it in the
+        // ranking; ranks are distinct (ids are), so rank < 16 places a pick.
+        const bool has0 = (uint32_t)lane < total, has1 = (uint32_t)lane + 32u < total;
+        const uint2 c0 = has0 ? cand[lane] : make_uint2(0u, 0xFFFFFFFFu);
+        const uint2 c1 = has1 ? cand[lane + 32] : make_uint2(0u, 0xFFFFFFFFu);
+        uint32_t rank0 = 0u, rank1 = 0u;
+#pragma unroll 4
+        for (uint32_t j = 0; j < total; ++j) {
+            const uint2 o = cand[j];
+            rank0 += (o.x > c0.x || (o.x == c0.x && o.y < c0.y)) ? 1u : 0u;
+            rank1 += (o.x > c1.x || (o.x == c1.x && o.y < c1.y)) ? 1u : 0u;
         }
+        __syncwarp();
+        if (has0 && rank0 < 16u) cand[rank0] = c0;
+        if (has1 && rank1 < 16u) cand[rank1] = c1;
+        __syncwarp();
+        if (lane < 16) {
+            mine_key = cand[lane].x;
+            mine_id = cand[lane].y;
+        }
+        __syncwarp();
     } else {
         uint32_t best = 0u;
         int best_j = 0;
