@@ -120,8 +120,9 @@ route_status topk16_select(const route_plan *plan, const float *logits, int32_t 
 /*
  * route_step: the whole route step (a1..a4) for the plan's rows, same
  * arguments and results as latent_router_forward followed by topk16_select.
- * Decode plans run it as ONE kernel: the CTA that completes the last router
- * column tile runs the top-16 for every row.
+ * Decode plans run it as two kernels: the weight stream, then one that
+ * finishes the split-K sums and runs the top-16 on the router logits while
+ * they are still in shared memory.
  */
 route_status route_step(const route_plan *plan, const void *hidden, const void *W_latent,
                         const void *W_router, void *latent, float *logits, int32_t *ids,
@@ -149,6 +150,20 @@ route_status route_step_host(const route_plan *plan, const void *hidden_host,
  * are invalid and the plan's split-K counters have been cleared).
  */
 route_status route_device_status(const route_plan *plan);
+
+/*
+ * route_set_overlap: let a decode plan's weight stream start before the
+ * preceding work on the stream has finished.  Every route kernel lets its
+ * successor launch early; by default the decode kernel still waits for its
+ * predecessor before it reads `hidden`.  With enable != 0 it reads `hidden`
+ * at once and waits only before it first writes its scratch, so a step's
+ * weight stream runs under the previous step's final reduction and top-16.
+ * Enable ONLY when `hidden` is never written by the route call issued
+ * immediately before on the same stream (it is safe whenever any other
+ * kernel or copy produces `hidden`: those do not release their successors
+ * early).  Prefill plans ignore the setting.  Default: disabled.
+ */
+route_status route_set_overlap(route_plan *plan, int enable);
 
 /*
  * route_test_stall: TEST HOOK for the bounded-wait path, not for production.

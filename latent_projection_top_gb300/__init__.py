@@ -45,6 +45,7 @@ EXPORTS = (
     "route_prepare", "route_destroy", "latent_router_forward", "topk16_select", "route_step",
     "route_step_host", "route_device_status", "route_plan_rows", "route_plan_mode",
     "route_plan_grid", "route_plan_segments", "route_last_error", "route_test_stall",
+    "route_set_overlap",
 )
 
 
@@ -78,6 +79,8 @@ def lib() -> ctypes.CDLL:
         L.route_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.route_step_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.route_device_status.argtypes = [vp]
+        L.route_set_overlap.argtypes = [vp, i32]
+        L.route_set_overlap.restype = i32
         L.route_test_stall.argtypes = [vp, i32, ctypes.c_uint64]
         L.route_test_stall.restype = i32
         for f in ("route_plan_rows", "route_plan_mode", "route_plan_grid", "route_plan_segments"):
@@ -246,6 +249,12 @@ def route_step_host(plan: Plan, hidden_host, W_latent, W_router, latent_host, lo
             _host_tensor(ids_host, "ids_host", (R, TOPK), (torch.int32,)),
             _host_tensor(weights_host, "weights_host", (R, TOPK), (torch.float32,)))
     _check(lib().route_step_host(plan.handle, *args, _stream(stream, d)))
+
+
+def route_set_overlap(plan: Plan, enable: bool) -> None:
+    """Let the decode weight stream overlap the previous route step's tail; only
+    when `hidden` is not written by the route call just before (include/route.h)."""
+    _check(lib().route_set_overlap(plan.handle, int(bool(enable))))
 
 
 def route_test_stall(plan: Plan, enable: bool, timeout_ns: int = 1_000_000) -> None:

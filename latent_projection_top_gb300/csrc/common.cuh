@@ -46,30 +46,29 @@ struct ProjArgs {
 };
 
 // Decode split-K: 18 column tiles of 256 columns (14 latent, 4 router -- the
-// last router tile holds 128 real columns) x 112 k-blocks.  Each tile is
-// covered by two clusters of four CTAs; each CTA streams 14 k-blocks.
+// last router tile holds 128 real columns) x 112 k-blocks.
 constexpr int kDTileCols = 256;
 constexpr int kDLatTiles = kLatent / kDTileCols;                           // 14
 constexpr int kDRouterTiles = (kExperts + kDTileCols - 1) / kDTileCols;    // 4
 constexpr int kDTiles = kDLatTiles + kDRouterTiles;                        // 18
-constexpr int kDClusterSize = 4;
-constexpr int kDClusters = 2 * kDTiles;                                    // 36
-constexpr int kDGrid = kDClusterSize * kDClusters;                         // 144
-constexpr int kDKPerCta = kKBlocks / (2 * kDClusterSize);                  // 14
-constexpr int kDSliceCols = kDTileCols / kDClusterSize;                    // 64
-constexpr int kDRouterSlices = kDRouterTiles * kDClusterSize;              // 16
-// device words: [0] status, [1] router slices done, [2] top-16 workers done,
-// [8 .. 8 + 72) per (tile, slice) arrival counters of the two clusters
-constexpr int kWordStatus = 0, kWordRouterDone = 1, kWordWorkersDone = 2, kWordPairs = 8;
-constexpr int kWords = 128;
+constexpr int kMaxGrid = 256;
+// device words: [0] status (the rest spare)
+constexpr int kWordStatus = 0;
+constexpr int kWords = 64;
 
 struct DecodeArgs {
     int rows;            // 1..20
+    int grid;            // CTAs of the stream kernel (<= kMaxGrid)
     int test_stall;      // test hook: skip each CTA's last copy so a wait must time out
-    int fuse_topk;       // run the top-16 in the kernel's tail
+    int overlap;         // read hidden before the grid dependency resolves
     unsigned long long timeout_ns;
-    float2 *ws;          // cluster partials [tile][half][kDecodeMaxRows][256] as (hi, lo)
-    unsigned *words;     // see kWord*
+    int cta_unit[kMaxGrid + 1];  // CTA g owns units [cta_unit[g], cta_unit[g+1]); unit u =
+                                 // (tile u / 112, k-block u % 112)
+    int seg_base[kDTiles];       // first partial slot of tile t
+    int seg_count[kDTiles];      // CTAs (partials) covering tile t
+    int cta_first[kDTiles];      // first CTA covering tile t
+    float2 *ws;                  // partials [slot][kDecodeMaxRows][256] as (hi, lo)
+    unsigned *words;             // device status word
     uint16_t *latent;
     float *logits;
     int32_t *ids;
@@ -87,9 +86,9 @@ constexpr int kPrefillBN = 256;
 int decode_bn_for(int rows);
 int decode_smem_bytes(int bn);
 cudaError_t decode_configure(int bn);
-cudaError_t decode_max_clusters(int bn, int *clusters);
 cudaError_t decode_launch(int bn, const CUtensorMap &map_h, const CUtensorMap &map_wl,
-                          const CUtensorMap &map_wr, const DecodeArgs &args, cudaStream_t stream);
+                          const CUtensorMap &map_wr, const DecodeArgs &args, int do_topk,
+                          cudaStream_t stream);
 
 cudaError_t topk_launch(const float *logits, int rows, int32_t *ids, float *weights,
                         cudaStream_t stream);

@@ -176,8 +176,7 @@ route_status launch_forward(const route_plan *p, const void *hidden, const void 
         a.logits = logits;
         a.ids = ids;
         a.weights = weights;
-        a.fuse_topk = do_topk;
-        e = decode_launch(p->bn, mh, ml, mr, a, stream);
+        e = decode_launch(p->bn, mh, ml, mr, a, do_topk, stream);
         if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
     } else {
         ProjArgs a = p->pre;
@@ -220,6 +219,28 @@ route_status run_step(const route_plan *p, const void *hidden, const void *W_lat
                       const void *W_router, void *latent, float *logits, int32_t *ids,
                       float *weights, cudaStream_t stream) {
     return launch_forward(p, hidden, W_latent, W_router, latent, logits, ids, weights, 1, stream);
+}
+
+// Decode split-K partition: CTA g owns a contiguous run of (tile, k-block)
+// units, the same number (+-1) for every CTA.
+void decode_partition(DecodeArgs &a, int grid, int *segments) {
+    const int U = kDTiles * kKBlocks;
+    a.grid = grid;
+    for (int g = 0; g <= grid; ++g) a.cta_unit[g] = (int)((long long)U * g / grid);
+    int slots = 0;
+    for (int t = 0; t < kDTiles; ++t) {
+        const int first_u = t * kKBlocks, last_u = first_u + kKBlocks - 1;
+        int g_first = -1, g_last = -1;
+        for (int g = 0; g < grid; ++g) {
+            if (a.cta_unit[g] <= first_u && first_u < a.cta_unit[g + 1]) g_first = g;
+            if (a.cta_unit[g] <= last_u && last_u < a.cta_unit[g + 1]) g_last = g;
+        }
+        a.cta_first[t] = g_first;
+        a.seg_count[t] = g_last - g_first + 1;
+        a.seg_base[t] = slots;
+        slots += a.seg_count[t];
+    }
+    *segments = slots;
 }
 
 }  // namespace
@@ -282,31 +303,19 @@ route_status route_prepare(int mode, int rows, int device, route_plan **out) {
     memset(&p->pre, 0, sizeof p->pre);
     memset(&p->dec, 0, sizeof p->dec);
     if (mode == ROUTE_DECODE) {
-        // The decode kernel needs all 36 of its 4-CTA clusters resident at
-        // once (its top-16 CTAs wait for the router slices).
-        int clusters = 0;
-        if ((e = decode_max_clusters(p->bn, &clusters)) != cudaSuccess) {
-            free_plan(p);
-            return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
-        }
-        if (clusters < kDClusters) {
-            free_plan(p);
-            return fail(ROUTE_ERR_DEVICE,
-                        "decode needs %d co-resident 4-CTA clusters; device %d holds %d", kDClusters,
-                        device, clusters);
-        }
         DecodeArgs &a = p->dec;
         a.rows = rows;
         a.timeout_ns = kDefaultTimeoutNs;
-        const size_t ws_bytes = (size_t)kDTiles * 2 * kDecodeMaxRows * kDTileCols * sizeof(float2);
+        const int grid = sms < kMaxGrid ? sms : kMaxGrid;
+        decode_partition(a, grid, &p->segments);
+        const size_t ws_bytes = (size_t)p->segments * kDecodeMaxRows * kDTileCols * sizeof(float2);
         if ((e = cudaMalloc(&p->ws, ws_bytes)) != cudaSuccess) {
             free_plan(p);
             return cuda_fail(e, "cudaMalloc(split-K scratch)");
         }
         a.ws = p->ws;
         a.words = p->words;
-        p->grid = kDGrid;
-        p->segments = kDGrid;
+        p->grid = a.grid;
     } else {
         ProjArgs &a = p->pre;
         a.rows = rows;
@@ -425,6 +434,13 @@ route_status route_device_status(const route_plan *plan) {
     cudaDeviceSynchronize();
     return fail(ROUTE_ERR_DEVICE_TIMEOUT,
                 "a kernel gave up waiting (status 0x%x); that launch's outputs are invalid", status);
+}
+
+route_status route_set_overlap(route_plan *plan, int enable) {
+    route_status st = check_plan(plan);
+    if (st != ROUTE_OK) return st;
+    plan->dec.overlap = enable ? 1 : 0;
+    return ROUTE_OK;
 }
 
 route_status route_test_stall(route_plan *plan, int enable, uint64_t timeout_ns) {

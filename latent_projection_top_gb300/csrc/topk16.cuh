@@ -59,15 +59,14 @@ __device__ __forceinline__ uint32_t warp_16th_largest(uint32_t v, int lane) {
     return __shfl_sync(0xFFFFFFFFu, v, 16);
 }
 
-// The calling warp selects row `row` (896 logits, read through L2 so that
-// values written by other CTAs of the same kernel are seen) and writes 16 ids
-// and weights.  All 32 lanes must call it; `cand` is this warp's shared
-// buffer of kCandMax entries.
+// The calling warp selects row `row` (896 logits in global or shared memory,
+// final before the call) and writes 16 ids and weights.  All 32 lanes must
+// call it; `cand` is this warp's shared buffer of kCandMax entries.
 __device__ __forceinline__ void topk16_warp(const float *row, int32_t *ids_out, float *w_out,
                                             int lane, uint2 *cand) {
     uint32_t key[kPerLane];
 #pragma unroll
-    for (int j = 0; j < kPerLane; ++j) key[j] = rank_key(__ldcg(row + 32 * j + lane));
+    for (int j = 0; j < kPerLane; ++j) key[j] = rank_key(row[32 * j + lane]);
 
     uint32_t lane_max = 0u;
 #pragma unroll

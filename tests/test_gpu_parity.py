@@ -138,13 +138,16 @@ def test_decode_batch_invariance_and_determinism():
                                   np.asarray(b)[:rows].view(np.uint8)), f"rows={rows}"
 
 
-def test_decode_bank_cycling_under_graph_replay():
-    """Eight banks cycled inside one captured CUDA graph give the eager bits."""
+@pytest.mark.parametrize("overlap", [False, True])
+def test_decode_bank_cycling_under_graph_replay(overlap):
+    """Banks cycled inside one captured CUDA graph give the eager bits, also
+    when consecutive steps overlap (hidden is not written by route calls)."""
     rows = 8
     banks = [bank("decode_r8", b) for b in range(3)]
     dev = [(to_dev_bf16(h[:rows]), to_dev_bf16(wl), to_dev_bf16(wr)) for h, wl, wr in banks]
     with route.Plan(route.DECODE, rows) as plan:
         eager = [run_step(plan, *d) for d in dev]
+        route.route_set_overlap(plan, overlap)
         outs = [outputs(rows) for _ in dev]
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
@@ -157,6 +160,7 @@ def test_decode_bank_cycling_under_graph_replay():
             for o in outs:
                 o[0].view(torch.int16).fill_(0x7FC0)
                 o[1].fill_(float("nan"))
+                o[2].fill_(-1)
             g.replay()
         torch.cuda.synchronize()
         route.route_device_status(plan)
@@ -164,6 +168,7 @@ def test_decode_bank_cycling_under_graph_replay():
             assert np.array_equal(bits_of(o[0]), e[0])
             assert np.array_equal(o[1].cpu().numpy().view(np.uint32), e[1].view(np.uint32))
             assert np.array_equal(o[2].cpu().numpy(), e[2])
+            assert np.array_equal(o[3].cpu().numpy().view(np.uint32), e[3].view(np.uint32))
 
 
 # ------------------------------------------------------------------- prefill
