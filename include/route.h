@@ -177,6 +177,34 @@ route_status route_set_overlap(route_plan *plan, int enable);
  */
 route_status route_test_stall(route_plan *plan, int enable, uint64_t timeout_ns);
 
+/*
+ * route_step_decode_noalloc: the decode route step (route_step for 1..20
+ * rows) without a plan and without allocating any memory.  The pages have no
+ * counterpart; this exists for callers that cannot allocate device memory:
+ * code running inside a host framework that owns all device memory and hands
+ * its plug-ins no allocator, and latency-critical paths where cudaMalloc's
+ * device-wide synchronisation is not acceptable.
+ *   rows     1..20 (the fixed scratch is sized for 20); anything else returns
+ *            ROUTE_ERR_ROWS before touching the device
+ *   hidden, W_latent, W_router, latent, logits, ids, weights: as route_step,
+ *            device pointers on the CURRENT device, 16-byte aligned
+ *   stream   cudaStream_t on the current device
+ * Results are the same as route_step's on a plan of the same rows (the same
+ * kernels and, on devices with up to 160 SMs, the same split-K partition).
+ * Scratch: one file-scope device array per device of about 7.25 MB (partials
+ * for 20 rows and up to 160 CTAs, plus a status word), held by every device
+ * that loads the library until the process exits.  Every call on a device
+ * shares it and it keeps the last call's contents, so calls whose work
+ * overlaps on the GPU (other streams, other host threads) race: serialise
+ * them, e.g. on one stream.  The first call on a device does a one-time
+ * set-up (the array's device address, the kernels' shared-memory limit):
+ * make that first call before any stream capture.  This entry point reports
+ * no device-side timeout status.
+ */
+route_status route_step_decode_noalloc(int rows, const void *hidden, const void *W_latent,
+                                       const void *W_router, void *latent, float *logits,
+                                       int32_t *ids, float *weights, void *stream);
+
 /* Plan properties: rows, mode, launch grid (CTAs) and split-K segments. */
 int route_plan_rows(const route_plan *plan);
 int route_plan_mode(const route_plan *plan);

@@ -45,7 +45,7 @@ EXPORTS = (
     "route_prepare", "route_destroy", "latent_router_forward", "topk16_select", "route_step",
     "route_step_host", "route_device_status", "route_plan_rows", "route_plan_mode",
     "route_plan_grid", "route_plan_segments", "route_last_error", "route_test_stall",
-    "route_set_overlap",
+    "route_set_overlap", "route_step_decode_noalloc",
 )
 
 
@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
         L.route_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.route_step_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.route_device_status.argtypes = [vp]
+        L.route_step_decode_noalloc.argtypes = [i32, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.route_step_decode_noalloc.restype = i32
         L.route_set_overlap.argtypes = [vp, i32]
         L.route_set_overlap.restype = i32
         L.route_test_stall.argtypes = [vp, i32, ctypes.c_uint64]

@@ -243,6 +243,80 @@ void decode_partition(DecodeArgs &a, int grid, int *segments) {
     *segments = slots;
 }
 
+// ---- allocation-free decode step ---------------------------------------
+//
+// route_step_decode_noalloc keeps its split-K scratch in this file-scope
+// device array instead of memory from cudaMalloc.  Layout: a 256-byte word
+// area (the kernels' status word) followed by the partial slots
+// [slot][20 rows][256 columns] of (hi, lo) floats.  The slot count bounds the
+// grid: a CTA's run spans at most two column tiles, so grid G needs at most
+// G + 17 slots; the grid is capped at kNoAllocMaxGrid CTAs.
+constexpr int kNoAllocMaxGrid = 160;
+constexpr int kNoAllocMaxSlots = kNoAllocMaxGrid + kDTiles - 1;  // 177
+constexpr size_t kNoAllocWordBytes = 256;
+constexpr size_t kNoAllocSlotBytes = (size_t)kDecodeMaxRows * kDTileCols * sizeof(float2);
+constexpr size_t kNoAllocScratchBytes = kNoAllocWordBytes + kNoAllocMaxSlots * kNoAllocSlotBytes;
+static_assert(kWords * sizeof(unsigned) <= kNoAllocWordBytes, "word area");
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Per-device set-up, done on the first call with that device current: the
+// device address of g_noalloc_scratch (host code may not use the symbol
+// itself), the kernels' shared-memory opt-in and the split-K partition.
+struct NoAllocDevice {
+    bool ready = false;
+    unsigned char *scratch = nullptr;
+    DecodeArgs base;
+};
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+NoAllocDevice g_noalloc[kNoAllocMaxDevices];
+
+route_status noalloc_setup(int device, NoAllocDevice **out) {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    NoAllocDevice &d = g_noalloc[device];
+    if (d.ready) {
+        *out = &d;
+        return ROUTE_OK;
+    }
+    cudaDeviceProp prop;
+    cudaError_t e = cudaGetDeviceProperties(&prop, device);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+    if (prop.major != 10 || prop.minor != 3)
+        return fail(ROUTE_ERR_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a only",
+                    device, prop.major, prop.minor);
+    if (prop.multiProcessorCount < kDTiles)
+        return fail(ROUTE_ERR_DEVICE, "decode needs at least %d SMs; device has %d", kDTiles,
+                    prop.multiProcessorCount);
+    for (int bn : {16, 32}) {
+        if ((size_t)decode_smem_bytes(bn) > prop.sharedMemPerBlockOptin)
+            return fail(ROUTE_ERR_DEVICE, "decode kernel needs %d B of shared memory per block",
+                        decode_smem_bytes(bn));
+        if ((e = decode_configure(bn)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    }
+    EncodeTiledFn enc;
+    route_status st = get_encode(&enc);
+    if (st != ROUTE_OK) return st;
+    void *ptr = nullptr;
+    if ((e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch)) != cudaSuccess)
+        return cuda_fail(e, "cudaGetSymbolAddress(no-allocation scratch)");
+    memset(&d.base, 0, sizeof d.base);
+    const int grid = prop.multiProcessorCount < kNoAllocMaxGrid ? prop.multiProcessorCount
+                                                                : kNoAllocMaxGrid;
+    int slots = 0;
+    decode_partition(d.base, grid, &slots);
+    if (slots > kNoAllocMaxSlots)
+        return fail(ROUTE_ERR_PLAN, "partition needs %d scratch slots; the array holds %d", slots,
+                    kNoAllocMaxSlots);
+    d.scratch = static_cast<unsigned char *>(ptr);
+    d.base.timeout_ns = kDefaultTimeoutNs;
+    d.base.words = reinterpret_cast<unsigned *>(d.scratch);
+    d.base.ws = reinterpret_cast<float2 *>(d.scratch + kNoAllocWordBytes);
+    d.ready = true;
+    *out = &d;
+    return ROUTE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -449,6 +523,46 @@ route_status route_test_stall(route_plan *plan, int enable, uint64_t timeout_ns)
     const unsigned long long t = enable ? (timeout_ns ? timeout_ns : 1000000ull) : kDefaultTimeoutNs;
     plan->pre.test_stall = plan->dec.test_stall = enable ? 1 : 0;
     plan->pre.timeout_ns = plan->dec.timeout_ns = t;
+    return ROUTE_OK;
+}
+
+route_status route_step_decode_noalloc(int rows, const void *hidden, const void *W_latent,
+                                       const void *W_router, void *latent, float *logits,
+                                       int32_t *ids, float *weights, void *stream) {
+    g_err[0] = '\0';
+    if (rows < 1 || rows > ROUTE_DECODE_MAX_ROWS)
+        return fail(ROUTE_ERR_ROWS,
+                    "route_step_decode_noalloc handles 1-%d rows (its fixed scratch is sized for "
+                    "%d); got %d",
+                    ROUTE_DECODE_MAX_ROWS, ROUTE_DECODE_MAX_ROWS, rows);
+    if (!hidden || !W_latent || !W_router || !latent || !logits || !ids || !weights)
+        return fail(ROUTE_ERR_NULL, "every pointer must be non-NULL");
+    if (!aligned16(hidden) || !aligned16(W_latent) || !aligned16(W_router) || !aligned16(latent) ||
+        !aligned16(logits) || !aligned16(ids) || !aligned16(weights))
+        return fail(ROUTE_ERR_ALIGN, "every device pointer must be 16-byte aligned");
+    int device = -1;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (device < 0 || device >= kNoAllocMaxDevices)
+        return fail(ROUTE_ERR_DEVICE, "device %d is out of range", device);
+    NoAllocDevice *d = nullptr;
+    route_status st = noalloc_setup(device, &d);
+    if (st != ROUTE_OK) return st;
+    const int bn = decode_bn_for(rows);
+    CUtensorMap mh, ml, mr;
+    if ((st = encode_2d(&mh, hidden, kHidden, (uint64_t)rows, kKBlock, (uint32_t)bn, "hidden")) !=
+            ROUTE_OK ||
+        (st = encode_2d(&ml, W_latent, kLatent, kHidden, 64, kKBlock, "W_latent")) != ROUTE_OK ||
+        (st = encode_2d(&mr, W_router, kExperts, kHidden, 64, kKBlock, "W_router")) != ROUTE_OK)
+        return st;
+    DecodeArgs a = d->base;
+    a.rows = rows;
+    a.latent = static_cast<uint16_t *>(latent);
+    a.logits = logits;
+    a.ids = ids;
+    a.weights = weights;
+    e = decode_launch(bn, mh, ml, mr, a, 1, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
     return ROUTE_OK;
 }
 
