@@ -14,27 +14,29 @@
 //   (+-1) for every CTA.  256-column tiles put 512 contiguous bytes per weight
 //   row in flight, which the HBM needs to run at full speed.  Per unit a TMA
 //   producer brings four 64x64 weight boxes and the hidden box (BN = 16 or 32
-//   rows, zero-filled past `rows`) into a 6-stage shared-memory ring; one
+//   rows, zero-filled past `rows`) into a 5-stage shared-memory ring; one
 //   thread issues tcgen05 MMAs (128 weight columns on M, token rows on N) into
-//   a fresh TMEM accumulator per k-block; four epilogue warps add each
+//   a fresh TMEM accumulator per k-block; eight epilogue warps add each
 //   k-block's FP32 result into a two-float (TwoSum) running sum, so the only
-//   rounding left is the tensor core's inside one 64-long block.  At the end
-//   of a run within a tile the CTA stores its two-float partial in a slot of
-//   the plan's scratch and exits.
+//   rounding left is the tensor core's inside one 64-long block.  A CTA's run
+//   covers at most two tiles; the first run's partial waits in shared memory
+//   and both are stored to their scratch slots when the CTA's stream ends.
 //
-// decode_finish_kernel -- 5 CTAs of 448 threads per row.  One sums the row's
-//   896 router logits over their slots, keeps them in shared memory and runs
-//   the top-16 there; four sum the row's 3584 latent columns.  Slots are
-//   summed in segment order as two-floats and rounded once, so results are
-//   bitwise reproducible and a row's bits do not depend on the row count
-//   (the partition depends only on the grid).
+// decode_finish_kernel -- at most one small CTA per SM, so that it fits next
+//   to a stream CTA: one CTA per row sums the row's 896 router logits and
+//   runs the top-16 on them from shared memory; the others sum the latent
+//   tiles, two (row, tile) items at a time.  Slots are summed in segment
+//   order as two-floats and rounded once, so results are bitwise reproducible
+//   and a row's bits do not depend on the row count (the partition depends
+//   only on the grid).
 //
 // Programmatic dependent launch: both kernels let their successor launch at
 // once.  The stream kernel prefetches its first weight boxes (model
 // parameters, which no predecessor writes) before `griddepcontrol.wait`.  By
 // default it reads the hidden rows only after the wait; with `overlap` set it
-// reads them at once and waits only before it first writes scratch, so one
-// step's weight stream runs under the previous step's finish kernel.
+// reads them at once and waits only before it writes scratch (at the end of
+// its stream), so one step's weight stream runs under the previous step's
+// finish kernel.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -46,23 +48,35 @@ namespace {
 
 constexpr uint32_t kBoxBytes = 64 * 64 * 2;         // one 64-column x 64-k weight box
 constexpr uint32_t kDAStageBytes = 4 * kBoxBytes;   // 256 columns x 64 k
-constexpr int kNumAcc = 8;                          // TMEM accumulator ring (k-blocks in flight)
+// Warps: 0 TMA producer, 1 MMA issuer, 2..9 epilogue -- warp w drains TMEM
+// lanes 32*(w % 4) .. +31 of column block (w - 2) / 4.  The running two-float
+// sums stay in TMEM, not registers, so that the small finish CTAs of the
+// previous step fit on the same SM.
+constexpr int kDecThreads = 320;
+constexpr int kEpiThreads = 256;
 
 template <int BN>
 struct DecCfg {
     static constexpr uint32_t kBStageBytes = BN * 128;  // BN rows x 64 k, BF16
     static constexpr uint32_t kStageBytes = kDAStageBytes + kBStageBytes;
-    static constexpr int kStages = 6;
+    static constexpr int kStages = 5;
     static constexpr uint32_t kAccCols = 2 * BN;       // two 128-column blocks per accumulator
-    static constexpr uint32_t kTmemCols = kNumAcc * kAccCols <= 256 ? 256 : 512;
-    static constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + 256;
+    // TMEM columns: kNumAcc accumulators (k-blocks in flight), then the
+    // running sums, per column block BN hi columns and BN lo columns.
+    static constexpr int kNumAcc = BN == 16 ? 8 : 6;
+    static constexpr uint32_t kStateCol = kNumAcc * kAccCols;
+    // a CTA's first-run partial waits here until its last run is done, so
+    // global scratch is written only at the end of the CTA's stream
+    static constexpr uint32_t kStashBytes = kDecodeMaxRows * kDTileCols * 8;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + kStashBytes + 256;
     // tcgen05 kind::f16: FP32 accumulator, BF16 A (MN-major) and B (K-major),
     // N = BN token rows, M = 128 weight columns.
     static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) |
                                        ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
     static_assert(BN == 16 || BN == 32, "decode row tile");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
-    static_assert(kNumAcc * kAccCols <= kTmemCols, "TMEM");
+    static_assert(kStateCol + 4 * BN <= kTmemCols, "TMEM");
 };
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -118,8 +132,10 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, const 
     }
 }
 
+// Register caps (the most each variant compiles to without spilling) leave
+// room on every SM sub-partition for two warps of a finish CTA.
 template <int BN>
-__global__ void __launch_bounds__(kProjThreads, 1)
+__global__ void __maxnreg__(BN == 16 ? 72 : 80)
     decode_stream_kernel(const __grid_constant__ CUtensorMap map_h,
                          const __grid_constant__ CUtensorMap map_wl,
                          const __grid_constant__ CUtensorMap map_wr,
@@ -131,12 +147,14 @@ __global__ void __launch_bounds__(kProjThreads, 1)
 
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
-    const uint32_t bars = sbase + C::kStages * C::kStageBytes;
+    float2 *const stash =
+        reinterpret_cast<float2 *>(smem_raw + (sbase - raw) + C::kStages * C::kStageBytes);
+    const uint32_t bars = sbase + C::kStages * C::kStageBytes + C::kStashBytes;
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (C::kStages + s); };
     auto accfull_bar = [&](int b) { return bars + 8u * (2 * C::kStages + b); };
-    auto accempty_bar = [&](int b) { return bars + 8u * (2 * C::kStages + kNumAcc + b); };
-    const uint32_t drain_bar = bars + 8u * (2 * C::kStages + 2 * kNumAcc);
+    auto accempty_bar = [&](int b) { return bars + 8u * (2 * C::kStages + C::kNumAcc + b); };
+    const uint32_t drain_bar = bars + 8u * (2 * C::kStages + 2 * C::kNumAcc);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -153,9 +171,9 @@ __global__ void __launch_bounds__(kProjThreads, 1)
             ptx::mbar_init(full_bar(s), 1);
             ptx::mbar_init(empty_bar(s), 1);
         }
-        for (int b = 0; b < kNumAcc; ++b) {
+        for (int b = 0; b < C::kNumAcc; ++b) {
             ptx::mbar_init(accfull_bar(b), 1);
-            ptx::mbar_init(accempty_bar(b), 128);
+            ptx::mbar_init(accempty_bar(b), kEpiThreads);
         }
         ptx::mbar_init(drain_bar, 1);
         ptx::fence_barrier_init();
@@ -229,8 +247,8 @@ __global__ void __launch_bounds__(kProjThreads, 1)
             for (int i = 0; i < n_units; ++i) {
                 const int s = i % C::kStages;
                 const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
-                const int buf = i % kNumAcc;
-                const uint32_t use = (uint32_t)(i / kNumAcc);
+                const int buf = i % C::kNumAcc;
+                const uint32_t use = (uint32_t)(i / C::kNumAcc);
                 if (!wait_phase(accempty_bar(buf), (use & 1u) ^ 1u, args, &s_abort)) break;
                 if (!wait_phase(full_bar(s), ph, args, &s_abort)) break;
                 ptx::tc_fence_after();
@@ -258,58 +276,78 @@ __global__ void __launch_bounds__(kProjThreads, 1)
         }
     } else {
         // ---------------- epilogue: two-float sums of the k-block results ----------------
-        const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
-        const int col = 32 * quarter + lane;
+        const int quarter = warp & 3;        // TMEM lanes 32*quarter .. +31
+        const int blk = (warp - 2) >> 2;     // column block 0 or 1 of the tile
+        const int col = blk * 128 + 32 * quarter + lane;
         const int rows = args.rows;
-        bool waited = false;
-        float hi[2][BN], lo[2][BN];
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int r = 0; r < BN; ++r) hi[h][r] = lo[h][r] = 0.f;
+        const uint32_t lanes = tmem_base + ((uint32_t)(32 * quarter) << 16);
+        const uint32_t sum_hi = lanes + C::kStateCol + (uint32_t)(blk * 2 * BN);
+        const uint32_t sum_lo = sum_hi + BN;
+        int first_slot = -1;
+        bool run_start = true;
         for (int i = 0; i < n_units; ++i) {
             const int u = u0 + i;
             const int t = u / kKBlocks;
-            const int buf = i % kNumAcc;
-            const uint32_t use = (uint32_t)(i / kNumAcc);
+            const int buf = i % C::kNumAcc;
+            const uint32_t use = (uint32_t)(i / C::kNumAcc);
             // Each warp waits on its own; an abort seen by one is seen by all.
             if (!wait_phase(accfull_bar(buf), use & 1u, args, &s_abort)) break;
             ptx::tc_fence_after();
-            const uint32_t taddr =
-                tmem_base + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * C::kAccCols);
-            uint32_t v[2][BN];
+            const bool last = i == n_units - 1;
+            const bool run_end = last || (u + 1) % kKBlocks == 0;
+            // Scratch may still be read by the predecessor's finish kernel.
+            if (last) asm volatile("griddepcontrol.wait;" ::: "memory");
+            const int slot = args.seg_base[t] + (g - args.cta_first[t]);
+            float2 *const out =
+                last ? args.ws + (size_t)slot * kDecodeMaxRows * kDTileCols : stash;
+            const uint32_t acc = lanes + (uint32_t)(buf * C::kAccCols + blk * BN);
 #pragma unroll
             for (int ch = 0; ch < BN / 16; ++ch) {
-                ptx::tmem_ld_x16(taddr + ch * 16, *reinterpret_cast<uint32_t(*)[16]>(&v[0][ch * 16]));
-                ptx::tmem_ld_x16(taddr + BN + ch * 16,
-                                 *reinterpret_cast<uint32_t(*)[16]>(&v[1][ch * 16]));
-            }
-            ptx::tmem_ld_wait();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(accempty_bar(buf));
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int r = 0; r < BN; ++r) two_sum_acc(hi[h][r], lo[h][r], __uint_as_float(v[h][r]));
-            const bool seg_end = (i == n_units - 1) || ((u + 1) % kKBlocks == 0);
-            if (seg_end) {
-                if (!waited) {  // scratch may still be read by the predecessor's finish kernel
-                    asm volatile("griddepcontrol.wait;" ::: "memory");
-                    waited = true;
+                uint32_t v[16], h[16], l[16];
+                ptx::tmem_ld_x16(acc + ch * 16, v);
+                if (!run_start) {
+                    ptx::tmem_ld_x16(sum_hi + ch * 16, h);
+                    ptx::tmem_ld_x16(sum_lo + ch * 16, l);
                 }
-                const int slot = args.seg_base[t] + (g - args.cta_first[t]);
-                float2 *part = args.ws + (size_t)slot * kDecodeMaxRows * kDTileCols;
+                ptx::tmem_ld_wait();
+                if (ch == BN / 16 - 1) {  // the accumulator is free for the next k-block
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(accempty_bar(buf));
+                }
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
-#pragma unroll
-                    for (int r = 0; r < BN; ++r) {
-                        if (r < rows)
-                            part[r * kDTileCols + h * 128 + col] = make_float2(hi[h][r], lo[h][r]);
-                        hi[h][r] = lo[h][r] = 0.f;
+                for (int j = 0; j < 16; ++j) {
+                    float hf = __uint_as_float(v[j]), lf = 0.f;
+                    if (!run_start) {
+                        hf = __uint_as_float(h[j]);
+                        lf = __uint_as_float(l[j]);
+                        two_sum_acc(hf, lf, __uint_as_float(v[j]));
                     }
+                    h[j] = __float_as_uint(hf);
+                    l[j] = __float_as_uint(lf);
+                }
+                if (!run_end) {
+                    ptx::tmem_st_x16(sum_hi + ch * 16, h);
+                    ptx::tmem_st_x16(sum_lo + ch * 16, l);
+                } else {
+                    // The run's partial: the first of two runs waits in shared
+                    // memory (each thread reads back only its own entries).
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (ch * 16 + j < rows)
+                            out[(ch * 16 + j) * kDTileCols + col] =
+                                make_float2(__uint_as_float(h[j]), __uint_as_float(l[j]));
+                }
             }
+            if (!run_end) ptx::tmem_st_wait();  // the next k-block reads these sums back
+            if (run_end && !last) first_slot = slot;
+            if (last && first_slot >= 0) {
+                float2 *p0 = args.ws + (size_t)first_slot * kDecodeMaxRows * kDTileCols;
+                for (int r = 0; r < rows; ++r) p0[r * kDTileCols + col] = stash[r * kDTileCols + col];
+            }
+            run_start = run_end;
         }
-        if (!waited) asm volatile("griddepcontrol.wait;" ::: "memory");
+        // Every kernel of the chain waits for its predecessor before it ends.
+        asm volatile("griddepcontrol.wait;" ::: "memory");
     }
 
     ptx::tc_fence_before();
@@ -320,67 +358,111 @@ __global__ void __launch_bounds__(kProjThreads, 1)
     }
 }
 
-// Sum the partial slots of one (tile, row) for the thread's column pair, in
-// segment order, as a two-float value.  Every slot is loaded before any is
-// added (one memory round trip for up to kFinishBatch slots).
-constexpr int kFinishBatch = 12;
+// Split-K sums.  A thread sums NP column pairs of one row, each over its
+// tile's partial slots in slot order, as two-floats rounded once at the end.
+// All slots of all NP pairs are loaded before any is added (one memory round
+// trip for up to kFinishBatch slots), at immediate offsets from one pointer
+// per pair.
+constexpr int kFinishBatch = 10;
+constexpr int kSlotF4 = kDecodeMaxRows * kDTileCols / 2;  // float4 (two columns) per slot
 
-__device__ __forceinline__ void sum_slots(const DecodeArgs &a, int t, int r, int cc, float &y0,
-                                          float &y1) {
-    const int base = a.seg_base[t], n = a.seg_count[t];
-    float h0 = 0.f, l0 = 0.f, h1 = 0.f, l1 = 0.f;
-    for (int s0 = 0; s0 < n; s0 += kFinishBatch) {
-        float4 p[kFinishBatch];
+template <int NP>
+__device__ __forceinline__ void sum_slot_pairs(const DecodeArgs &a, int r, const int (&t)[NP],
+                                               const int (&cc)[NP], float2 (&y)[NP]) {
+    const float4 *p[NP];
+    int n[NP], nmax = 0;
+    float h[2 * NP], l[2 * NP];
 #pragma unroll
-        for (int j = 0; j < kFinishBatch; ++j)
-            if (s0 + j < n)
-                p[j] = __ldcg(reinterpret_cast<const float4 *>(
-                    a.ws + ((size_t)(base + s0 + j) * kDecodeMaxRows + r) * kDTileCols + cc));
-#pragma unroll
-        for (int j = 0; j < kFinishBatch; ++j)
-            if (s0 + j < n) {
-                two_sum_acc(h0, l0, p[j].x);
-                l0 += p[j].y;
-                two_sum_acc(h1, l1, p[j].z);
-                l1 += p[j].w;
-            }
+    for (int q = 0; q < NP; ++q) {
+        p[q] = reinterpret_cast<const float4 *>(a.ws) +
+               ((size_t)a.seg_base[t[q]] * kDecodeMaxRows + r) * (kDTileCols / 2) + cc[q] / 2;
+        n[q] = a.seg_count[t[q]];
+        nmax = n[q] > nmax ? n[q] : nmax;
+        h[2 * q] = h[2 * q + 1] = l[2 * q] = l[2 * q + 1] = 0.f;
     }
-    y0 = h0 + l0;
-    y1 = h1 + l1;
+    for (int s0 = 0; s0 < nmax; s0 += kFinishBatch) {
+        float4 v[NP][kFinishBatch];
+#pragma unroll
+        for (int j = 0; j < kFinishBatch; ++j)
+#pragma unroll
+            for (int q = 0; q < NP; ++q)
+                if (s0 + j < n[q]) v[q][j] = __ldcg(p[q] + j * kSlotF4);
+#pragma unroll
+        for (int j = 0; j < kFinishBatch; ++j)
+#pragma unroll
+            for (int q = 0; q < NP; ++q)
+                if (s0 + j < n[q]) {
+                    two_sum_acc(h[2 * q], l[2 * q], v[q][j].x);
+                    l[2 * q] += v[q][j].y;
+                    two_sum_acc(h[2 * q + 1], l[2 * q + 1], v[q][j].z);
+                    l[2 * q + 1] += v[q][j].w;
+                }
+#pragma unroll
+        for (int q = 0; q < NP; ++q) p[q] += kFinishBatch * kSlotF4;
+    }
+#pragma unroll
+    for (int q = 0; q < NP; ++q) y[q] = make_float2(h[2 * q] + l[2 * q], h[2 * q + 1] + l[2 * q + 1]);
 }
 
-constexpr int kFinishThreads = kExperts / 2;           // 448: one column pair per thread
-constexpr int kFinishLatBlocks = kLatent / (2 * kFinishThreads);  // 4 latent CTAs per row
+// Small CTAs that fit on an SM next to a stream CTA: with overlap, the finish
+// of one step runs under the next step's weight stream, and the next stream
+// stores its partials only once this kernel is complete.  Under that load a
+// round trip to memory takes microseconds, so a CTA makes as few as it can.
+// The grid is at most one CTA per SM: CTA r < rows sums row r's 896 router
+// logits (224 threads, two column pairs each) and runs the row's top-16 from
+// shared memory; the other CTAs sum latent items (row, 256-column tile), two
+// at a time (128 threads, one column pair each).
+constexpr int kRouterThreads = kExperts / 4;    // 224
+constexpr int kLatentThreads = kDTileCols / 2;  // 128 per latent item
+constexpr int kFinishThreads = 2 * kLatentThreads;
 
-// blocks [0, rows): router row + top-16;  then 4 latent CTAs per row
-__global__ void __launch_bounds__(kFinishThreads) decode_finish_kernel(
-    const __grid_constant__ DecodeArgs a, int do_topk) {
+// rows router CTAs + enough latent CTAs for one pass over the 14 * rows
+// latent items, capped at the stream grid (one CTA per SM), with at least one
+// latent CTA.
+int finish_grid(const DecodeArgs &a) {
+    int g = a.rows + (kDLatTiles * a.rows + 1) / 2;
+    if (g > a.grid) g = a.grid;
+    if (g < a.rows + 1) g = a.rows + 1;
+    return g;
+}
+
+__global__ void __maxnreg__(112) decode_finish_kernel(const __grid_constant__ DecodeArgs a,
+                                                      int do_topk) {
     __shared__ float s_logits[kExperts];
     __shared__ uint2 s_cand[kCandMax];
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the stream kernel's partials are complete
     const int rows = a.rows;
     const int tid = threadIdx.x;
-    const int c = 2 * tid;
-    if ((int)blockIdx.x < rows) {
-        const int r = blockIdx.x;
-        float y0, y1;
-        sum_slots(a, kDLatTiles + c / kDTileCols, r, c % kDTileCols, y0, y1);
-        *reinterpret_cast<float2 *>(a.logits + (size_t)r * kExperts + c) = make_float2(y0, y1);
-        s_logits[c] = y0;
-        s_logits[c + 1] = y1;
+    const int b = blockIdx.x;
+    if (b < rows) {
+        if (tid >= kRouterThreads) return;  // the named barrier below counts only router threads
+        const int r = b;
+        const int c0 = 2 * tid, c1 = c0 + kExperts / 2;  // columns c0, c0+1 and c1, c1+1
+        const int t[2] = {kDLatTiles + c0 / kDTileCols, kDLatTiles + c1 / kDTileCols};
+        const int cc[2] = {c0 % kDTileCols, c1 % kDTileCols};
+        float2 y[2];
+        sum_slot_pairs<2>(a, r, t, cc, y);
+        float *lrow = a.logits + (size_t)r * kExperts;
+        *reinterpret_cast<float2 *>(lrow + c0) = y[0];
+        *reinterpret_cast<float2 *>(lrow + c1) = y[1];
         if (!do_topk) return;
-        __syncthreads();
+        *reinterpret_cast<float2 *>(s_logits + c0) = y[0];
+        *reinterpret_cast<float2 *>(s_logits + c1) = y[1];
+        asm volatile("bar.sync 1, %0;" ::"n"(kRouterThreads) : "memory");
         if (tid < 32)
             topk16_warp(s_logits, a.ids + (size_t)r * kTopK, a.weights + (size_t)r * kTopK, tid, s_cand);
     } else {
-        const int b = blockIdx.x - rows;
-        const int r = b / kFinishLatBlocks;
-        const int n = (b % kFinishLatBlocks) * (2 * kFinishThreads) + c;  // latent column pair
-        float y0, y1;
-        sum_slots(a, n / kDTileCols, r, n % kDTileCols, y0, y1);
-        *reinterpret_cast<uint32_t *>(a.latent + (size_t)r * kLatent + n) =
-            (uint32_t)bf16_bits(y0) | ((uint32_t)bf16_bits(y1) << 16);
+        const int n_items = kDLatTiles * rows;
+        const int stride = 2 * ((int)gridDim.x - rows);
+        for (int i = 2 * (b - rows) + tid / kLatentThreads; i < n_items; i += stride) {
+            const int r = i / kDLatTiles;
+            const int t[1] = {i % kDLatTiles}, cc[1] = {2 * (tid % kLatentThreads)};
+            float2 y[1];
+            sum_slot_pairs<1>(a, r, t, cc, y);
+            *reinterpret_cast<uint32_t *>(a.latent + (size_t)r * kLatent + t[0] * kDTileCols + cc[0]) =
+                (uint32_t)bf16_bits(y[0].x) | ((uint32_t)bf16_bits(y[0].y) << 16);
+        }
     }
 }
 
@@ -409,7 +491,7 @@ cudaError_t launch_bn(const CUtensorMap &mh, const CUtensorMap &ml, const CUtens
                       const DecodeArgs &a, cudaStream_t stream) {
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t c =
-        pdl_config(dim3(a.grid), dim3(kProjThreads), DecCfg<BN>::kSmemBytes, stream, attr);
+        pdl_config(dim3(a.grid), dim3(kDecThreads), DecCfg<BN>::kSmemBytes, stream, attr);
     return cudaLaunchKernelEx(&c, decode_stream_kernel<BN>, mh, ml, mr, a);
 }
 
@@ -433,8 +515,8 @@ cudaError_t decode_launch(int bn, const CUtensorMap &map_h, const CUtensorMap &m
                                : cudaErrorInvalidValue;
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t c = pdl_config(dim3(args.rows * (1 + kFinishLatBlocks)),
-                                      dim3(kFinishThreads), 0, stream, attr);
+    cudaLaunchConfig_t c =
+        pdl_config(dim3(finish_grid(args)), dim3(kFinishThreads), 0, stream, attr);
     return cudaLaunchKernelEx(&c, decode_finish_kernel, args, do_topk);
 }
 

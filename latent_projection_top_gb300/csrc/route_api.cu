@@ -221,6 +221,18 @@ route_status run_step(const route_plan *p, const void *hidden, const void *W_lat
     return launch_forward(p, hidden, W_latent, W_router, latent, logits, ids, weights, 1, stream);
 }
 
+// Decode stream grid: the largest CTA count, at most one per SM and at most
+// `cap`, that divides the 18 * 112 (tile, k-block) units evenly, so that every
+// CTA streams the same number of bytes (144 CTAs of 14 units on 152 SMs).
+// Never below the tile count, which route_prepare requires of the device.
+int decode_grid(int sms, int cap) {
+    const int U = kDTiles * kKBlocks;
+    const int hi = sms < cap ? sms : cap;
+    for (int g = hi; g > kDTiles; --g)
+        if (U % g == 0) return g;
+    return kDTiles;
+}
+
 // Decode split-K partition: CTA g owns a contiguous run of (tile, k-block)
 // units, the same number (+-1) for every CTA.
 void decode_partition(DecodeArgs &a, int grid, int *segments) {
@@ -301,8 +313,7 @@ route_status noalloc_setup(int device, NoAllocDevice **out) {
     if ((e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch)) != cudaSuccess)
         return cuda_fail(e, "cudaGetSymbolAddress(no-allocation scratch)");
     memset(&d.base, 0, sizeof d.base);
-    const int grid = prop.multiProcessorCount < kNoAllocMaxGrid ? prop.multiProcessorCount
-                                                                : kNoAllocMaxGrid;
+    const int grid = decode_grid(prop.multiProcessorCount, kNoAllocMaxGrid);
     int slots = 0;
     decode_partition(d.base, grid, &slots);
     if (slots > kNoAllocMaxSlots)
@@ -380,8 +391,7 @@ route_status route_prepare(int mode, int rows, int device, route_plan **out) {
         DecodeArgs &a = p->dec;
         a.rows = rows;
         a.timeout_ns = kDefaultTimeoutNs;
-        const int grid = sms < kMaxGrid ? sms : kMaxGrid;
-        decode_partition(a, grid, &p->segments);
+        decode_partition(a, decode_grid(sms, kMaxGrid), &p->segments);
         const size_t ws_bytes = (size_t)p->segments * kDecodeMaxRows * kDTileCols * sizeof(float2);
         if ((e = cudaMalloc(&p->ws, ws_bytes)) != cudaSuccess) {
             free_plan(p);
