@@ -47,12 +47,14 @@ ROW_BYTES = K_HIDDEN * 2 + N_LATENT * 2 + N_EXPERTS * 4 + TOPK * 8   # 25,216
 FLOP_PER_ROW = 2 * K_HIDDEN * (N_LATENT + N_EXPERTS)          # 64,225,280
 GRAPH_LEN = 64
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["latent_projection_top_gb300/csrc/decode_kernel.cu",
-                  "latent_projection_top_gb300/csrc/prefill_kernel.cu",
-                  "latent_projection_top_gb300/csrc/topk16.cuh",
-                  "latent_projection_top_gb300/csrc/topk_kernel.cu",
-                  "latent_projection_top_gb300/csrc/sm103_ptx.cuh",
-                  "latent_projection_top_gb300/csrc/common.cuh"]
+_CSRC = "latent_projection_top_gb300/csrc/"
+# the sources each profiled kernel is built from: a recorded DRAM traffic
+# figure stands only while these files are unchanged
+KERNEL_SOURCES = {
+    "decode_stream_kernel": [_CSRC + f for f in ("decode_kernel.cu", "topk16.cuh", "sm103_ptx.cuh",
+                                                 "common.cuh")],
+    "prefill_kernel": [_CSRC + f for f in ("prefill_kernel.cu", "sm103_ptx.cuh", "common.cuh")],
+}
 
 
 def parse_args():
@@ -86,9 +88,9 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_sha():
+def kernel_source_sha(kernel: str):
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -102,7 +104,7 @@ def recorded_traffic(kernel: str, workload: str):
         with open(path) as f:
             d = json.load(f)
         e = d[f"{kernel}:{workload}"]
-        if e.get("source_sha") != kernel_source_sha():
+        if e.get("source_sha") != kernel_source_sha(kernel):
             return None
         return float(e["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
