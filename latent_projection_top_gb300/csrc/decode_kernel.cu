@@ -97,6 +97,13 @@ __device__ __forceinline__ void two_sum_acc(float &hi, float &lo, float x) {
     lo += e;
 }
 
+// The value of a two-float sum.  An infinite high part is the value itself:
+// once a sum reaches +-Inf its error term is Inf - Inf = NaN and must not be
+// added (a NaN high part stays NaN).
+__device__ __forceinline__ float two_float_value(float hi, float lo) {
+    return fabsf(hi) == __int_as_float(0x7F800000) ? hi : hi + lo;
+}
+
 __device__ __forceinline__ uint16_t bf16_bits(float x) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
@@ -401,7 +408,8 @@ __device__ __forceinline__ void sum_slot_pairs(const DecodeArgs &a, int r, const
         for (int q = 0; q < NP; ++q) p[q] += kFinishBatch * kSlotF4;
     }
 #pragma unroll
-    for (int q = 0; q < NP; ++q) y[q] = make_float2(h[2 * q] + l[2 * q], h[2 * q + 1] + l[2 * q + 1]);
+    for (int q = 0; q < NP; ++q) y[q] = make_float2(two_float_value(h[2 * q], l[2 * q]),
+                                                    two_float_value(h[2 * q + 1], l[2 * q + 1]));
 }
 
 // Small CTAs that fit on an SM next to a stream CTA: with overlap, the finish
@@ -412,6 +420,7 @@ __device__ __forceinline__ void sum_slot_pairs(const DecodeArgs &a, int r, const
 // logits (224 threads, two column pairs each) and runs the row's top-16 from
 // shared memory; the other CTAs sum latent items (row, 256-column tile), two
 // at a time (128 threads, one column pair each).
+static_assert(kExpertsTopk == kExperts, "top-16 row width");
 constexpr int kRouterThreads = kExperts / 4;    // 224
 constexpr int kLatentThreads = kDTileCols / 2;  // 128 per latent item
 constexpr int kFinishThreads = 2 * kLatentThreads;
@@ -428,15 +437,14 @@ int finish_grid(const DecodeArgs &a) {
 
 __global__ void __maxnreg__(112) decode_finish_kernel(const __grid_constant__ DecodeArgs a,
                                                       int do_topk) {
-    __shared__ float s_logits[kExperts];
-    __shared__ uint2 s_cand[kCandMax];
+    __shared__ TopkBlockSmem s_topk;
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the stream kernel's partials are complete
     const int rows = a.rows;
     const int tid = threadIdx.x;
     const int b = blockIdx.x;
     if (b < rows) {
-        if (tid >= kRouterThreads) return;  // the named barrier below counts only router threads
+        if (tid >= kRouterThreads) return;  // the named barriers below count only router threads
         const int r = b;
         const int c0 = 2 * tid, c1 = c0 + kExperts / 2;  // columns c0, c0+1 and c1, c1+1
         const int t[2] = {kDLatTiles + c0 / kDTileCols, kDLatTiles + c1 / kDTileCols};
@@ -447,11 +455,12 @@ __global__ void __maxnreg__(112) decode_finish_kernel(const __grid_constant__ De
         *reinterpret_cast<float2 *>(lrow + c0) = y[0];
         *reinterpret_cast<float2 *>(lrow + c1) = y[1];
         if (!do_topk) return;
-        *reinterpret_cast<float2 *>(s_logits + c0) = y[0];
-        *reinterpret_cast<float2 *>(s_logits + c1) = y[1];
-        asm volatile("bar.sync 1, %0;" ::"n"(kRouterThreads) : "memory");
-        if (tid < 32)
-            topk16_warp(s_logits, a.ids + (size_t)r * kTopK, a.weights + (size_t)r * kTopK, tid, s_cand);
+        // a3/a4 over the row by all 224 threads (the heavy-tie fallback
+        // re-reads the logits this CTA just stored, ordered by the barriers)
+        const float v[4] = {y[0].x, y[0].y, y[1].x, y[1].y};
+        const int id[4] = {c0, c0 + 1, c1, c1 + 1};
+        topk16_block(v, id, lrow, tid, 1, s_topk, a.ids + (size_t)r * kTopK,
+                     a.weights + (size_t)r * kTopK);
     } else {
         const int n_items = kDLatTiles * rows;
         const int stride = 2 * ((int)gridDim.x - rows);

@@ -26,7 +26,8 @@
 
 namespace route {
 
-constexpr int kPerLane = 896 / 32;  // 28 logits per lane; lane l holds ids 32*j + l
+constexpr int kExpertsTopk = 896;
+constexpr int kPerLane = kExpertsTopk / 32;  // 28 logits per lane; lane l holds ids 32*j + l
 constexpr int kCandMax = 64;        // candidate buffer per warp (two per lane)
 
 // Order-preserving key: NaN -> 1 (below -Inf), -0 -> +0, removed entries -> 0.
@@ -59,98 +60,42 @@ __device__ __forceinline__ uint32_t warp_16th_largest(uint32_t v, int lane) {
     return __shfl_sync(0xFFFFFFFFu, v, 16);
 }
 
-// The calling warp selects row `row` (896 logits in global or shared memory,
-// final before the call) and writes 16 ids and weights.  All 32 lanes must
-// call it; `cand` is this warp's shared buffer of kCandMax entries.
-__device__ __forceinline__ void topk16_warp(const float *row, int32_t *ids_out, float *w_out,
-                                            int lane, uint2 *cand) {
-    uint32_t key[kPerLane];
-#pragma unroll
-    for (int j = 0; j < kPerLane; ++j) key[j] = rank_key(row[32 * j + lane]);
-
-    uint32_t lane_max = 0u;
-#pragma unroll
-    for (int j = 0; j < kPerLane; ++j) lane_max = max(lane_max, key[j]);
-    const uint32_t T = warp_16th_largest(lane_max, lane);
-
-    uint32_t cnt = 0u;
-#pragma unroll
-    for (int j = 0; j < kPerLane; ++j) cnt += (key[j] >= T) ? 1u : 0u;
-    uint32_t incl = cnt;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-        if (lane >= off) incl += y;
-    }
-    const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-
-    uint32_t mine_key = 0u;  // lane i keeps the i-th pick (i < 16)
-    uint32_t mine_id = 0u;
-    if (total <= (uint32_t)kCandMax) {
-        uint32_t pos = incl - cnt;
-#pragma unroll
-        for (int j = 0; j < kPerLane; ++j)
-            if (key[j] >= T) cand[pos++] = make_uint2(key[j], (uint32_t)(32 * j + lane));
-        __syncwarp();
-        // Each candidate's rank = how many candidates precede it in the
-        // ranking; ranks are distinct (ids are), so rank < 16 places a pick.
-        const bool has0 = (uint32_t)lane < total, has1 = (uint32_t)lane + 32u < total;
-        const uint2 c0 = has0 ? cand[lane] : make_uint2(0u, 0xFFFFFFFFu);
-        const uint2 c1 = has1 ? cand[lane + 32] : make_uint2(0u, 0xFFFFFFFFu);
-        uint32_t rank0 = 0u, rank1 = 0u;
+// Rank the `total` (<= kCandMax) candidates in `cand` (shared memory, final
+// before the call): each candidate's rank is the number of candidates that
+// precede it in the ranking; ranks are distinct (ids are), so rank < 16
+// places a pick.  Lane i < 16 returns the i-th pick.  All 32 lanes call it.
+__device__ __forceinline__ void pick16_from_candidates(uint2 *cand, uint32_t total, int lane,
+                                                       uint32_t &mine_key, uint32_t &mine_id) {
+    const bool has0 = (uint32_t)lane < total, has1 = (uint32_t)lane + 32u < total;
+    const uint2 c0 = has0 ? cand[lane] : make_uint2(0u, 0xFFFFFFFFu);
+    const uint2 c1 = has1 ? cand[lane + 32] : make_uint2(0u, 0xFFFFFFFFu);
+    uint32_t rank0 = 0u, rank1 = 0u;
 #pragma unroll 4
-        for (uint32_t j = 0; j < total; ++j) {
-            const uint2 o = cand[j];
-            rank0 += (o.x > c0.x || (o.x == c0.x && o.y < c0.y)) ? 1u : 0u;
-            rank1 += (o.x > c1.x || (o.x == c1.x && o.y < c1.y)) ? 1u : 0u;
-        }
-        __syncwarp();
-        if (has0 && rank0 < 16u) cand[rank0] = c0;
-        if (has1 && rank1 < 16u) cand[rank1] = c1;
-        __syncwarp();
-        if (lane < 16) {
-            mine_key = cand[lane].x;
-            mine_id = cand[lane].y;
-        }
-        __syncwarp();
-    } else {
-        uint32_t best = 0u;
-        int best_j = 0;
-#pragma unroll
-        for (int j = 0; j < kPerLane; ++j)
-            if (key[j] > best) {
-                best = key[j];
-                best_j = j;
-            }
-#pragma unroll 1
-        for (int i = 0; i < 16; ++i) {
-            const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, best);
-            const uint32_t c = (best == top) ? (uint32_t)(32 * best_j + lane) : 0xFFFFFFFFu;
-            const uint32_t pick = __reduce_min_sync(0xFFFFFFFFu, c);
-            if (lane == i) {
-                mine_key = top;
-                mine_id = pick;
-            }
-            if ((int)(pick & 31u) == lane) {  // the owner removes the pick and rescans
-                const int js = (int)(pick >> 5);
-                best = 0u;
-                best_j = 0;
-#pragma unroll
-                for (int j = 0; j < kPerLane; ++j) {
-                    if (j == js) key[j] = 0u;
-                    if (key[j] > best) {
-                        best = key[j];
-                        best_j = j;
-                    }
-                }
-            }
-        }
+    for (uint32_t j = 0; j < total; ++j) {
+        const uint2 o = cand[j];
+        rank0 += (o.x > c0.x || (o.x == c0.x && o.y < c0.y)) ? 1u : 0u;
+        rank1 += (o.x > c1.x || (o.x == c1.x && o.y < c1.y)) ? 1u : 0u;
     }
+    __syncwarp();
+    if (has0 && rank0 < 16u) cand[rank0] = c0;
+    if (has1 && rank1 < 16u) cand[rank1] = c1;
+    __syncwarp();
+    mine_key = 0u;
+    mine_id = 0u;
+    if (lane < 16) {
+        mine_key = cand[lane].x;
+        mine_id = cand[lane].y;
+    }
+    __syncwarp();
+}
 
-    // Routing weights, FP32 only: t = exp(-|v|) by expf (never overflows);
-    // 1 + t is kept exactly as a two-float (TwoSum), q = 1 / (1 + t) as a
-    // two-float (FMA residual), s = q (v >= 0) or t * q (v < 0); the 16 s are
-    // summed as two-floats in a fixed tree order; w = s / S is rounded once.
+// Routing weights of the 16 picks (lane i < 16 holds pick i) and the
+// stores.  FP32 only: t = exp(-|v|) by expf (never overflows); 1 + t is kept
+// exactly as a two-float (TwoSum), q = 1 / (1 + t) as a two-float (FMA
+// residual), s = q (v >= 0) or t * q (v < 0); the 16 s are summed as
+// two-floats in a fixed tree order; w = s / S is rounded once.
+__device__ __forceinline__ void weights16_store(uint32_t mine_key, uint32_t mine_id, int lane,
+                                                int32_t *ids_out, float *w_out) {
     float s_hi = 0.f, s_lo = 0.f;
     if (lane < 16) {
         const float v = key_to_float(mine_key);
@@ -189,6 +134,135 @@ __device__ __forceinline__ void topk16_warp(const float *row, int32_t *ids_out, 
         ids_out[lane] = (int32_t)mine_id;
         w_out[lane] = q0 + res / tot_hi;
     }
+}
+
+// The calling warp selects row `row` (896 logits in global or shared memory,
+// final before the call) and writes 16 ids and weights.  All 32 lanes must
+// call it; `cand` is this warp's shared buffer of kCandMax entries.
+__device__ __forceinline__ void topk16_warp(const float *row, int32_t *ids_out, float *w_out,
+                                            int lane, uint2 *cand) {
+    uint32_t key[kPerLane];
+#pragma unroll
+    for (int j = 0; j < kPerLane; ++j) key[j] = rank_key(row[32 * j + lane]);
+
+    uint32_t lane_max = 0u;
+#pragma unroll
+    for (int j = 0; j < kPerLane; ++j) lane_max = max(lane_max, key[j]);
+    const uint32_t T = warp_16th_largest(lane_max, lane);
+
+    uint32_t cnt = 0u;
+#pragma unroll
+    for (int j = 0; j < kPerLane; ++j) cnt += (key[j] >= T) ? 1u : 0u;
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+
+    uint32_t mine_key = 0u;  // lane i keeps the i-th pick (i < 16)
+    uint32_t mine_id = 0u;
+    if (total <= (uint32_t)kCandMax) {
+        uint32_t pos = incl - cnt;
+#pragma unroll
+        for (int j = 0; j < kPerLane; ++j)
+            if (key[j] >= T) cand[pos++] = make_uint2(key[j], (uint32_t)(32 * j + lane));
+        __syncwarp();
+        pick16_from_candidates(cand, total, lane, mine_key, mine_id);
+    } else {
+        uint32_t best = 0u;
+        int best_j = 0;
+#pragma unroll
+        for (int j = 0; j < kPerLane; ++j)
+            if (key[j] > best) {
+                best = key[j];
+                best_j = j;
+            }
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, best);
+            const uint32_t c = (best == top) ? (uint32_t)(32 * best_j + lane) : 0xFFFFFFFFu;
+            const uint32_t pick = __reduce_min_sync(0xFFFFFFFFu, c);
+            if (lane == i) {
+                mine_key = top;
+                mine_id = pick;
+            }
+            if ((int)(pick & 31u) == lane) {  // the owner removes the pick and rescans
+                const int js = (int)(pick >> 5);
+                best = 0u;
+                best_j = 0;
+#pragma unroll
+                for (int j = 0; j < kPerLane; ++j) {
+                    if (j == js) key[j] = 0u;
+                    if (key[j] > best) {
+                        best = key[j];
+                        best_j = j;
+                    }
+                }
+            }
+        }
+    }
+    weights16_store(mine_key, mine_id, lane, ids_out, w_out);
+}
+
+// Shared memory of topk16_block.
+struct TopkBlockSmem {
+    uint32_t tmax[kExpertsTopk / 4];  // one key maximum per thread
+    uint32_t T;
+    uint32_t count;
+    uint2 cand[kCandMax];
+};
+
+// The same selection by the 224 threads that hold a row, four logits each
+// (v[j] with ids id[j]), so that the threshold and the candidate compaction
+// take every thread's share at once.  The threshold is the one above: each
+// lane of warp 0 takes the maximum of seven threads' maxima (28 logits), and
+// T = the 16th largest of those 32.  Candidates >= T are compacted with a
+// shared counter (their order is not fixed; the ranking is).  Rows with more
+// than kCandMax candidates fall back to topk16_warp over `row`, the same 896
+// logits in shared memory.  Every one of the 224 threads calls it; it uses
+// named barrier `bar`.
+__device__ __forceinline__ void topk16_block(const float (&v)[4], const int (&id)[4],
+                                             const float *row, int tid, int bar,
+                                             TopkBlockSmem &sh, int32_t *ids_out,
+                                             float *w_out) {
+    constexpr int kThreads = kExpertsTopk / 4;
+    uint32_t key[4];
+    uint32_t m = 0u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        key[j] = rank_key(v[j]);
+        m = max(m, key[j]);
+    }
+    sh.tmax[tid] = m;
+    if (tid == 0) sh.count = 0u;
+    asm volatile("bar.sync %0, %1;" ::"r"(bar), "n"(kThreads) : "memory");
+    if (tid < 32) {
+        uint32_t lm = 0u;
+#pragma unroll
+        for (int j = 0; j < kThreads / 32; ++j) lm = max(lm, sh.tmax[tid + 32 * j]);
+        const uint32_t T = warp_16th_largest(lm, tid);
+        if (tid == 0) sh.T = T;
+    }
+    asm volatile("bar.sync %0, %1;" ::"r"(bar), "n"(kThreads) : "memory");
+    const uint32_t T = sh.T;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        if (key[j] >= T) {
+            const uint32_t pos = atomicAdd(&sh.count, 1u);
+            if (pos < (uint32_t)kCandMax) sh.cand[pos] = make_uint2(key[j], (uint32_t)id[j]);
+        }
+    asm volatile("bar.sync %0, %1;" ::"r"(bar), "n"(kThreads) : "memory");
+    if (tid >= 32) return;
+    const uint32_t total = sh.count;
+    if (total > (uint32_t)kCandMax) {
+        topk16_warp(row, ids_out, w_out, tid, sh.cand);
+        return;
+    }
+    uint32_t mine_key, mine_id;
+    pick16_from_candidates(sh.cand, total, tid, mine_key, mine_id);
+    weights16_store(mine_key, mine_id, tid, ids_out, w_out);
 }
 
 }  // namespace route

@@ -91,6 +91,31 @@ def test_topk_bit_exact_random(R, mode):
     check_topk_exact(ids, w, ids_ref, w_ref)
 
 
+def test_decode_fused_topk_on_special_logits():
+    """The decode step's own top-16 (the block-wide selection in its finish
+    kernel, including the fallback for rows with heavy ties) on logits with
+    ties, +-0, +-Inf and NaN.  A one-hot hidden row makes the logits equal one
+    row of W_router (all other rows zero), so the special values pass through
+    the projection unchanged."""
+    K, E = route.K_HIDDEN, route.N_EXPERTS
+    h = np.zeros((1, K), np.uint16)
+    h[0, 0] = 0x3F80  # 1.0
+    dh = to_dev_bf16(h)
+    dwl = to_dev_bf16(np.zeros((K, route.N_LATENT), np.uint16))
+    with route.Plan(route.DECODE, 1) as plan:
+        for i, p in enumerate(special_rows()):
+            wr = np.zeros((K, E), np.uint16)
+            wr[0] = oracle.bf16_rne(p)
+            lat, lg, ids, w = run_step(plan, dh, dwl, to_dev_bf16(wr))
+            want = (wr[0].astype(np.uint32) << 16).view(np.float32)
+            nan = np.isnan(want)
+            assert np.array_equal(np.isnan(lg[0]), nan), f"pattern {i}: NaN positions"
+            assert np.array_equal(lg[0][~nan], want[~nan]), f"pattern {i}: logits"
+            assert not lat.any(), f"pattern {i}: latent of a zero W_latent"
+            ids_o, w_o = oracle.topk(lg)
+            check_topk_exact(ids, w, ids_o, w_o)
+
+
 # ------------------------------------------------------------ decode (G1-G5)
 
 DECODE_CASES = [("decode_r1", 1), ("decode_r8", 8), ("decode_sweep", 9), ("decode_sweep", 12),
