@@ -75,6 +75,7 @@ struct DecCfg {
     static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) |
                                        ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
     static_assert(BN == 16 || BN == 32, "decode row tile");
+    static_assert(kDecodeMaxRows > 16 && kDecodeMaxRows - 16 == 4, "BN = 32 drains rows 16..19");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
     static_assert(kStateCol + 4 * BN <= kTmemCols, "TMEM");
 };
@@ -106,6 +107,51 @@ __device__ __forceinline__ float two_float_value(float hi, float lo) {
 
 __device__ __forceinline__ uint16_t bf16_bits(float x) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+// One chunk of W rows (TMEM columns r0 .. r0+W-1) of the epilogue: add the
+// k-block result at `acc` into the running two-float sums at s_hi / s_lo
+// (or start them, on the first k-block of a run); at the end of a run store
+// the sums for rows < `rows` to `out` instead.  `release` frees the
+// accumulator once its columns are in registers.
+template <int W>
+__device__ __forceinline__ void epi_chunk(uint32_t acc, uint32_t s_hi, uint32_t s_lo, int r0,
+                                          bool run_start, bool run_end, bool release,
+                                          uint32_t accempty, float2 *out, int col, int rows) {
+    uint32_t v[W], h[W], l[W];
+    ptx::tmem_ld(acc + r0, v);
+    if (!run_start) {
+        ptx::tmem_ld(s_hi + r0, h);
+        ptx::tmem_ld(s_lo + r0, l);
+    }
+    ptx::tmem_ld_wait();
+    if (release) {  // the accumulator is free for the next k-block
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(accempty);
+    }
+#pragma unroll
+    for (int j = 0; j < W; ++j) {
+        float hf = __uint_as_float(v[j]), lf = 0.f;
+        if (!run_start) {
+            hf = __uint_as_float(h[j]);
+            lf = __uint_as_float(l[j]);
+            two_sum_acc(hf, lf, __uint_as_float(v[j]));
+        }
+        h[j] = __float_as_uint(hf);
+        l[j] = __float_as_uint(lf);
+    }
+    if (!run_end) {
+        ptx::tmem_st(s_hi + r0, h);
+        ptx::tmem_st(s_lo + r0, l);
+    } else {
+        // The run's partial: the first of two runs waits in shared memory
+        // (each thread reads back only its own entries).
+#pragma unroll
+        for (int j = 0; j < W; ++j)
+            if (r0 + j < rows)
+                out[(r0 + j) * kDTileCols + col] =
+                    make_float2(__uint_as_float(h[j]), __uint_as_float(l[j]));
+    }
 }
 
 __device__ __forceinline__ void fail_timeout(const DecodeArgs &a, volatile int *abort_flag) {
@@ -308,43 +354,13 @@ __global__ void __maxnreg__(BN == 16 ? 72 : 80)
             float2 *const out =
                 last ? args.ws + (size_t)slot * kDecodeMaxRows * kDTileCols : stash;
             const uint32_t acc = lanes + (uint32_t)(buf * C::kAccCols + blk * BN);
-#pragma unroll
-            for (int ch = 0; ch < BN / 16; ++ch) {
-                uint32_t v[16], h[16], l[16];
-                ptx::tmem_ld_x16(acc + ch * 16, v);
-                if (!run_start) {
-                    ptx::tmem_ld_x16(sum_hi + ch * 16, h);
-                    ptx::tmem_ld_x16(sum_lo + ch * 16, l);
-                }
-                ptx::tmem_ld_wait();
-                if (ch == BN / 16 - 1) {  // the accumulator is free for the next k-block
-                    ptx::tc_fence_before();
-                    ptx::mbar_arrive(accempty_bar(buf));
-                }
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    float hf = __uint_as_float(v[j]), lf = 0.f;
-                    if (!run_start) {
-                        hf = __uint_as_float(h[j]);
-                        lf = __uint_as_float(l[j]);
-                        two_sum_acc(hf, lf, __uint_as_float(v[j]));
-                    }
-                    h[j] = __float_as_uint(hf);
-                    l[j] = __float_as_uint(lf);
-                }
-                if (!run_end) {
-                    ptx::tmem_st_x16(sum_hi + ch * 16, h);
-                    ptx::tmem_st_x16(sum_lo + ch * 16, l);
-                } else {
-                    // The run's partial: the first of two runs waits in shared
-                    // memory (each thread reads back only its own entries).
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (ch * 16 + j < rows)
-                            out[(ch * 16 + j) * kDTileCols + col] =
-                                make_float2(__uint_as_float(h[j]), __uint_as_float(l[j]));
-                }
-            }
+            // Rows 0..15, then (BN = 32) rows 16..19: no row past the
+            // 20-row envelope is ever read from TMEM.
+            epi_chunk<16>(acc, sum_hi, sum_lo, 0, run_start, run_end, BN == 16,
+                          accempty_bar(buf), out, col, rows);
+            if constexpr (BN == 32)
+                epi_chunk<kDecodeMaxRows - 16>(acc, sum_hi, sum_lo, 16, run_start, run_end, true,
+                                               accempty_bar(buf), out, col, rows);
             if (!run_end) ptx::tmem_st_wait();  // the next k-block reads these sums back
             if (run_end && !last) first_slot = slot;
             if (last && first_slot >= 0) {

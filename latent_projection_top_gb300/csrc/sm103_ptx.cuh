@@ -149,6 +149,24 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&v)[16]) {
         : "r"(taddr));
 }
 
+// Each thread of the warp reads 4 consecutive 32-bit TMEM columns of its lane.
+__device__ __forceinline__ void tmem_ld_x4(uint32_t taddr, uint32_t (&v)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+                 : "r"(taddr));
+}
+
+// Each thread of the warp writes 4 consecutive 32-bit TMEM columns of its lane.
+__device__ __forceinline__ void tmem_st_x4(uint32_t taddr, const uint32_t (&v)[4]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr),
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
+                 : "memory");
+}
+
+// Overloads by width, for code templated on it.
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&v)[16]) { tmem_ld_x16(taddr, v); }
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&v)[4]) { tmem_ld_x4(taddr, v); }
+
 // Each thread of the warp writes 16 consecutive 32-bit TMEM columns of its lane.
 __device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&v)[16]) {
     asm volatile(
@@ -159,6 +177,9 @@ __device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&v)[
         "r"(v[15])
         : "memory");
 }
+
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t (&v)[16]) { tmem_st_x16(taddr, v); }
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t (&v)[4]) { tmem_st_x4(taddr, v); }
 
 // Wait until this thread's earlier tcgen05.st have completed.
 __device__ __forceinline__ void tmem_st_wait() {
