@@ -14,7 +14,7 @@
 //   (+-1) for every CTA.  256-column tiles put 512 contiguous bytes per weight
 //   row in flight, which the HBM needs to run at full speed.  Per unit a TMA
 //   producer brings four 64x64 weight boxes and the hidden box (BN = 16 or 32
-//   rows, zero-filled past `rows`) into a 5-stage shared-memory ring; one
+//   rows, zero-filled past `rows`) into a 4-stage shared-memory ring; one
 //   thread issues tcgen05 MMAs (128 weight columns on M, token rows on N) into
 //   a fresh TMEM accumulator per k-block; eight epilogue warps add each
 //   k-block's FP32 result into a two-float (TwoSum) running sum, so the only
@@ -59,7 +59,7 @@ template <int BN>
 struct DecCfg {
     static constexpr uint32_t kBStageBytes = BN * 128;  // BN rows x 64 k, BF16
     static constexpr uint32_t kStageBytes = kDAStageBytes + kBStageBytes;
-    static constexpr int kStages = 5;
+    static constexpr int kStages = 4;  // measured: 4 (and 3) beat 5 and 6 under back-to-back steps
     static constexpr uint32_t kAccCols = 2 * BN;       // two 128-column blocks per accumulator
     // TMEM columns: kNumAcc accumulators (k-blocks in flight), then the
     // running sums, per column block BN hi columns and BN lo columns.
