@@ -18,14 +18,16 @@ constexpr int kExperts = 896;
 constexpr int kTopK = 16;
 constexpr int kDecodeMaxRows = 20;
 
-// Prefill tiling: one tile = 128 weight columns (the MMA M side) x 256 token
-// rows (the MMA N side); K is consumed 64 at a time.
-constexpr int kTileCols = 128;
+// K is consumed 64 at a time.
 constexpr int kKBlock = 64;
 constexpr int kKBlocks = kHidden / kKBlock;                 // 112
-constexpr int kLatentTiles = kLatent / kTileCols;           // 28
-constexpr int kRouterTiles = kExperts / kTileCols;          // 7
-constexpr int kColTiles = kLatentTiles + kRouterTiles;      // 35 (prefill tiles)
+// Prefill tiling: one tile = 256 weight columns (the MMA M side, split over a
+// pair of CTAs) x 256 token rows (the MMA N side; each CTA of the pair loads
+// 128 of them): 14 latent + 4 router column tiles, the last with 128 real
+// columns.
+constexpr int kPrefillBN = 256;
+constexpr int kPrefillColTiles = 18;
+constexpr int kPrefillHiddenBoxRows = 128;
 constexpr int kProjThreads = 192;                           // 6 warps
 
 enum Mode : int { kDecode = 0, kPrefill = 1 };
@@ -36,8 +38,8 @@ constexpr unsigned kStatusTimeout = 1u;
 // Everything the prefill projection kernel needs besides its tensor maps.
 struct ProjArgs {
     int rows;            // token rows in this call
-    int row_tiles;       // ceil(rows / BN)
-    int grid;            // persistent CTAs launched
+    int row_tiles;       // ceil(rows / kPrefillBN)
+    int grid;            // persistent CTAs launched (pairs of CTAs: even)
     int test_stall;      // test hook: skip each CTA's last copy so a wait must time out
     unsigned long long timeout_ns;  // bound on every wait inside the kernel
     unsigned *status;          // device status word
@@ -81,7 +83,6 @@ int prefill_smem_bytes();
 cudaError_t prefill_configure();
 cudaError_t prefill_launch(const CUtensorMap &map_h, const CUtensorMap &map_wl,
                            const CUtensorMap &map_wr, const ProjArgs &args, cudaStream_t stream);
-constexpr int kPrefillBN = 256;
 
 int decode_bn_for(int rows);
 int decode_smem_bytes(int bn);

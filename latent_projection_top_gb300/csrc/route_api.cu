@@ -154,8 +154,11 @@ route_status check_plan(const route_plan *p) {
 route_status encode_all(const route_plan *p, const void *hidden, const void *W_latent,
                         const void *W_router, CUtensorMap *mh, CUtensorMap *ml, CUtensorMap *mr) {
     route_status st;
-    if ((st = encode_2d(mh, hidden, kHidden, (uint64_t)p->rows, kKBlock, (uint32_t)p->bn,
-                        "hidden")) != ROUTE_OK)
+    // decode: one box holds the step's rows; prefill: each CTA of a pair
+    // loads half of a tile's token rows
+    const uint32_t hbox = p->mode == ROUTE_DECODE ? (uint32_t)p->bn : (uint32_t)kPrefillHiddenBoxRows;
+    if ((st = encode_2d(mh, hidden, kHidden, (uint64_t)p->rows, kKBlock, hbox, "hidden")) !=
+        ROUTE_OK)
         return st;
     if ((st = encode_2d(ml, W_latent, kLatent, kHidden, 64, kKBlock, "W_latent")) != ROUTE_OK)
         return st;
@@ -405,8 +408,8 @@ route_status route_prepare(int mode, int rows, int device, route_plan **out) {
         a.rows = rows;
         a.timeout_ns = kDefaultTimeoutNs;
         a.row_tiles = (rows + p->bn - 1) / p->bn;
-        const int tiles = kColTiles * a.row_tiles;
-        a.grid = sms < tiles ? sms : tiles;
+        const int tiles = kPrefillColTiles * a.row_tiles;  // tiles of a CTA pair
+        a.grid = 2 * (sms / 2 < tiles ? sms / 2 : tiles);
         a.status = p->words + kWordStatus;
         p->segments = tiles;
         p->grid = a.grid;
