@@ -78,6 +78,12 @@ def parse_args():
 
 # ---------------------------------------------------------------- plumbing
 
+def whole_job_rows_per_s(world: int, steps: int, rows: int, ms: float) -> float:
+    """Rows of every replica over the slowest replica's time (ms, max over
+    ranks): each of the `world` ranks runs `steps` layers of `rows` rows."""
+    return world * steps * rows / (ms / 1e3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -391,7 +397,7 @@ def main_ours(args):
     ms, clocks = rb.run(steps, args.steps, args.warmup, dist, sampler_index=dev)
     ms = dist.max(ms)
     step_s = ms / 1e3 / args.steps
-    value = dist.world * args.steps * rows / (ms / 1e3)
+    value = whole_job_rows_per_s(dist.world, args.steps, rows, ms)
 
     # roofline of the dominant kernel
     if decode:
