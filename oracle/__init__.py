@@ -17,6 +17,8 @@ What each function follows (page title, section):
 * ``topk`` -- "Kimi K3.1 recipe: route 9..20 decode rows through the pushed
   pair gather and standalone top-16", commit message: the standalone top-16
   and its routing weights.
+* ``latent_sumsq`` -- the first page's Reviewer Notes: the FP32 sum of squares
+  per row that the latent norm needs.
 
 Readings where the pages are silent are stated in ``route_oracle.c``.
 Every function is pinned by tests in ``tests/test_oracle_pins.py``.
@@ -77,6 +79,7 @@ def _load():
                                                  c_int, u16p, f32p, f64p, f64p]
             lib.oracle_latent_ksplit.argtypes = [u16p, u16p, c_int, c_int, c_int, c_int, u16p]
             lib.oracle_topk.argtypes = [f32p, c_int, c_int, c_int, i32p, f32p]
+            lib.oracle_latent_sumsq.argtypes = [u16p, c_int, c_int, f32p]
             lib.oracle_bf16_rne.argtypes = [ctypes.c_float]
             lib.oracle_bf16_rne.restype = ctypes.c_uint16
             lib.oracle_fp32_rne.argtypes = [ctypes.c_double]
@@ -160,6 +163,16 @@ def topk(logits, k: int = TOPK):
     _load().oracle_topk(_ptr(lg, ctypes.c_float), R, E, k, _ptr(ids, ctypes.c_int32),
                         _ptr(w, ctypes.c_float))
     return ids, w
+
+
+def latent_sumsq(latent_bits) -> np.ndarray:
+    """Per-row sum of squares of BF16 latent values [R, N]: float64 sum,
+    rounded once to FP32.  Returns float32 [R]."""
+    lat = _bits(latent_bits)
+    R, N = lat.shape
+    out = np.empty(R, np.float32)
+    _load().oracle_latent_sumsq(_ptr(lat, ctypes.c_uint16), R, N, _ptr(out, ctypes.c_float))
+    return out
 
 
 def bf16_rne(x) -> np.ndarray:

@@ -28,7 +28,9 @@
  *     -0 == +0) go to the lower expert id; output is in rank order;
  *     NaN ranks below every number (below -Inf);
  *   - routing weight w_i = s_i / sum_j s_j with s_i = 1 / (1 + exp(-logit)),
- *     over the 16 picked experts, computed in double, rounded to FP32.
+ *     over the 16 picked experts, computed in double, rounded to FP32;
+ *   - the latent sum of squares is taken over the BF16 latent values the
+ *     step returns (what a following norm reads), rounded once to FP32.
  */
 #include <math.h>
 #include <stdint.h>
@@ -197,4 +199,22 @@ void oracle_topk(const float *logits, int R, int E, int k, int32_t *ids, float *
     }
     free(s);
     free(buf);
+}
+
+/* ---- latent sum of squares per row [P2-Rev] ---------------------------- */
+
+/* ss[r] = fp32_rne( sum_{n < N} v[r, n]^2 ), v = the value of the BF16 bits
+ * latent[r, n], summed in float64 with n ascending.  A BF16 value has an
+ * 8-bit significand, so its square is exact in double; the running double sum
+ * is the only rounding before the final one to FP32. */
+void oracle_latent_sumsq(const uint16_t *latent, int R, int N, float *ss)
+{
+    for (int r = 0; r < R; ++r) {
+        double acc = 0.0;
+        for (int n = 0; n < N; ++n) {
+            double v = oracle_bf16_to_double(latent[(size_t)r * N + n]);
+            acc += v * v;
+        }
+        ss[r] = oracle_fp32_rne(acc);
+    }
 }

@@ -313,3 +313,54 @@ def test_topk_permutation_invariance():
     ids_p, w_p = oracle.topk(logits[:, perm])
     assert np.array_equal(ids_p, inv[ids])
     assert np.array_equal(w_p, w)
+
+
+# --------------------------------------------------------------------------
+# latent sum of squares ("Optionally gather the Kimi3 prefill latent instead
+# of reducing it", Reviewer Notes: an FP32 sum of squares per row for the
+# latent norm)
+
+def _f32_nearest_even(q: Fraction) -> np.float32:
+    """The FP32 value nearest to the rational q, ties to the even significand
+    (exact: candidates around a double approximation, compared as rationals)."""
+    c = np.float32(float(q))
+    cands = [np.nextafter(c, np.float32(-np.inf)), c, np.nextafter(c, np.float32(np.inf))]
+    best = min(cands, key=lambda x: (abs(Fraction(float(x)) - q),
+                                     int(np.asarray(x).view(np.uint32)) & 1))
+    return np.float32(best)
+
+
+def test_sumsq_closed_forms():
+    N = oracle.N_LATENT
+    rows = np.stack([
+        np.ones(N, np.float32),
+        np.full(N, 2.0, np.float32),
+        np.where(np.arange(N) % 2 == 0, 1.5, -1.5).astype(np.float32),
+        np.zeros(N, np.float32),
+        np.where(np.arange(N) == 7, -3.0, 0.0).astype(np.float32),
+    ])
+    got = oracle.latent_sumsq(torch_bf16_bits(rows))
+    assert got.tolist() == [N, 4.0 * N, 2.25 * N, 0.0, 9.0]
+
+
+def test_sumsq_rounds_once():
+    # 1.0 followed by 3583 values of 2^-12 (squares 2^-24, half an FP32 ulp
+    # of 1): a running FP32 sum never moves off 1.0; the exact sum does.
+    N = oracle.N_LATENT
+    row = np.full((1, N), 2.0 ** -12, np.float32)
+    row[0, 0] = 1.0
+    got = oracle.latent_sumsq(torch_bf16_bits(row))[0]
+    want = _f32_nearest_even(1 + Fraction(N - 1, 2 ** 24))
+    assert got == want and got > np.float32(1.0)
+
+
+@pytest.mark.parametrize("N", [1, 31, 257, 3584])
+def test_sumsq_against_exact_rationals(N):
+    rng = np.random.default_rng(N)
+    vals = (rng.standard_normal((4, N)) * np.exp2(rng.integers(-20, 20, (4, N)))).astype(np.float32)
+    bits = torch_bf16_bits(vals)
+    got = oracle.latent_sumsq(bits)
+    v = bits.astype(np.uint32) << 16
+    for r in range(4):
+        exact = sum(Fraction(float(x)) ** 2 for x in v[r].view(np.float32))
+        assert got[r] == _f32_nearest_even(exact), r
