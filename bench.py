@@ -213,6 +213,50 @@ class Dist:
             self.dist.destroy_process_group()
 
 
+# ------------------------------------------------------------- watchdog
+
+class Watchdog:
+    """Ends the process if a GPU phase runs far past any plausible time, so
+    that a kernel that never completes cannot hold the GPU: the process exits
+    with status 3 and a message naming the phase (its context is torn down)."""
+
+    def __init__(self, limit_s: float = 180.0):
+        self.limit = limit_s
+        self.phase = None
+        self.t0 = 0.0
+        threading.Thread(target=self._watch, daemon=True).start()
+
+    def _watch(self):
+        while True:
+            time.sleep(1.0)
+            ph = self.phase
+            if ph is not None and time.time() - self.t0 > self.limit:
+                sys.stderr.write(f"bench: GPU phase '{ph}' exceeded {self.limit:.0f} s; exiting\n")
+                sys.stderr.flush()
+                os._exit(3)
+
+    def __call__(self, phase: str):
+        wd = self
+
+        class _Phase:
+            def __enter__(self):
+                wd.phase, wd.t0 = phase, time.time()
+
+            def __exit__(self, *exc):
+                wd.phase = None
+        return _Phase()
+
+
+WATCHDOG = None
+
+
+def guarded(phase: str):
+    global WATCHDOG
+    if WATCHDOG is None:
+        WATCHDOG = Watchdog()
+    return WATCHDOG(phase)
+
+
 # ---------------------------------------------------------------- our arm
 
 class RouteBench:
@@ -254,7 +298,7 @@ class RouteBench:
                 torch.empty((rows, route.TOPK), dtype=torch.float32, device=self.dev))
 
     def make_steps(self, workload: str, rows: int, nbanks: int, gemm_only: bool = False,
-                   overlap: bool = False):
+                   overlap: bool = False, sumsq: bool = False):
         """Closures, one per bank, each enqueuing one layer's route step."""
         route = self.route
         mode = route.DECODE if workload.startswith("decode") else route.PREFILL
@@ -269,6 +313,10 @@ class RouteBench:
             if gemm_only:
                 steps.append(lambda s, h=h, wl=wl, wr=wr, o=o:
                              route.latent_router_forward(plan, h, wl, wr, o[0], o[1], stream=s))
+            elif sumsq:
+                ss = self.torch.empty((rows,), dtype=self.torch.float32, device=self.dev)
+                steps.append(lambda s, h=h, wl=wl, wr=wr, o=o, ss=ss:
+                             route.route_step_sumsq(plan, h, wl, wr, *o, ss, stream=s))
             else:
                 steps.append(lambda s, h=h, wl=wl, wr=wr, o=o:
                              route.route_step(plan, h, wl, wr, *o, stream=s))
@@ -287,6 +335,10 @@ class RouteBench:
     def run(self, steps, k: int, warmup: int, dist=None, sampler_index=None, graph_len=GRAPH_LEN):
         """Time exactly k steps (after `warmup` steps) as graph replays.
         Returns (elapsed_ms, clocks)."""
+        with guarded(f"{k} timed steps"):
+            return self._run(steps, k, warmup, dist, sampler_index, graph_len)
+
+    def _run(self, steps, k, warmup, dist, sampler_index, graph_len):
         torch = self.torch
         s = torch.cuda.Stream(device=self.dev)
         s.wait_stream(torch.cuda.current_stream(self.dev))
@@ -327,6 +379,10 @@ class RouteBench:
 
     def e2e(self, workload: str, rows: int, k: int, dist):
         """route_step_host: H2D hidden + step + D2H results, every step."""
+        with guarded("e2e"):
+            return self._e2e(workload, rows, k, dist)
+
+    def _e2e(self, workload: str, rows: int, k: int, dist):
         torch, route, np = self.torch, self.route, self.np
         mode = route.DECODE if workload.startswith("decode") else route.PREFILL
         wl, wr = self.weight_banks("decode" if mode == route.DECODE else "prefill", 8)[0]
@@ -395,6 +451,7 @@ def main_ours(args):
     overlap = decode and not args.no_overlap
     plan, steps, launches = rb.make_steps(wk, rows, nbanks, overlap=overlap)
     ms, clocks = rb.run(steps, args.steps, args.warmup, dist, sampler_index=dev)
+    rb.route.route_device_status(plan)  # raises if any launch hit a bounded-wait timeout
     ms = dist.max(ms)
     step_s = ms / 1e3 / args.steps
     value = whole_job_rows_per_s(dist.world, args.steps, rows, ms)
@@ -472,6 +529,7 @@ def sweep(rb, dist, peaks, args):
         for ov in (True, False):
             plan, steps, _ = rb.make_steps(wk, rows, 8, overlap=ov)
             ms, _ = rb.run(steps, 64 * 64, 64 * 8, dist)
+            rb.route.route_device_status(plan)
             t = dist.max(ms) / 1e3 / (64 * 64)
             plan.close()
             sfx = "" if ov else "_without_overlap"
@@ -488,6 +546,8 @@ def sweep(rb, dist, peaks, args):
         t = ms / 1e3 / (92 * 5)
         p2, gsteps, _ = rb.make_steps(wk, rows, nb, gemm_only=True)
         gms, _ = rb.run(gsteps, 92 * 5, 92 * 2, dist, graph_len=92)
+        rb.route.route_device_status(plan)
+        rb.route.route_device_status(p2)
         tg = dist.max(gms) / 1e3 / (92 * 5)
         flop = FLOP_PER_ROW * rows
         res.append({"workload": wk, "rows": rows, "us_per_layer": round(t * 1e6, 3),
@@ -498,6 +558,23 @@ def sweep(rb, dist, peaks, args):
                     "weight_banks": nb})
         plan.close()
         p2.close()
+    # the route step that also returns each latent row's sum of squares
+    for wk, rows, ov in [("decode_r8", 8, True), ("decode_sweep", 20, True),
+                         ("prefill_r3072", 3072, False)]:
+        decode = wk.startswith("decode")
+        nb = 8 if decode else args.prefill_banks
+        plan, steps, _ = rb.make_steps(wk, rows, nb, overlap=ov, sumsq=True)
+        n, w, gl = (64 * 64, 64 * 8, 64) if decode else (92 * 5, 92 * 2, 92)
+        ms, _ = rb.run(steps, n, w, dist, graph_len=gl)
+        rb.route.route_device_status(plan)
+        t = dist.max(ms) / 1e3 / n
+        plan.close()
+        e = {"workload": wk, "rows": rows, "call": "route_step_sumsq", "overlap": ov,
+             "us_per_layer": round(t * 1e6, 3), "rows_per_s": round(rows / t, 1)}
+        if decode:
+            algo = WEIGHT_BYTES + rows * (ROW_BYTES + 4)
+            e.update({"bound": "hbm", "frac": round(algo / t / 1e9 / peaks["hbm_gbs"], 4)})
+        res.append(e)
     return res
 
 

@@ -129,6 +129,22 @@ route_status route_step(const route_plan *plan, const void *hidden, const void *
                         float *weights, void *stream);
 
 /*
+ * route_step_sumsq: route_step that also writes latent_sumsq [rows] FP32
+ * (device, 4-byte aligned, caller-owned): for each row, the sum of the
+ * squares of the BF16 latent values this step stores, the per-row statistic
+ * the latent's RMS norm needs ("Optionally gather the Kimi3 prefill latent
+ * instead of reducing it", Reviewer Notes: an FP32 sum of squares for the
+ * latent norm).  The squares are exact in FP32 and are summed as two-floats
+ * in a fixed order, then rounded once, so the result is bitwise reproducible.
+ * Prefill computes it in the top-16 kernel; decode in the kernel that
+ * finishes the split-K sums.  latent, logits, ids and weights are exactly
+ * those route_step writes.  NULL latent_sumsq: ROUTE_ERR_NULL.
+ */
+route_status route_step_sumsq(const route_plan *plan, const void *hidden, const void *W_latent,
+                              const void *W_router, void *latent, float *logits, int32_t *ids,
+                              float *weights, float *latent_sumsq, void *stream);
+
+/*
  * route_step_host: route_step with the per-step tensors in HOST memory.
  * hidden_host [rows, 7168] BF16 is copied to the device, the step runs, and
  * latent_host, logits_host, ids_host, weights_host receive the results.

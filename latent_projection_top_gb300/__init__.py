@@ -45,7 +45,7 @@ EXPORTS = (
     "route_prepare", "route_destroy", "latent_router_forward", "topk16_select", "route_step",
     "route_step_host", "route_device_status", "route_plan_rows", "route_plan_mode",
     "route_plan_grid", "route_plan_segments", "route_last_error", "route_test_stall",
-    "route_set_overlap", "route_step_decode_noalloc",
+    "route_set_overlap", "route_step_decode_noalloc", "route_step_sumsq",
 )
 
 
@@ -78,6 +78,7 @@ def lib() -> ctypes.CDLL:
         L.topk16_select.argtypes = [vp, vp, vp, vp, vp]
         L.route_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.route_step_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.route_step_sumsq.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.route_device_status.argtypes = [vp]
         L.route_step_decode_noalloc.argtypes = [i32, vp, vp, vp, vp, vp, vp, vp, vp]
         L.route_step_decode_noalloc.restype = i32
@@ -91,7 +92,7 @@ def lib() -> ctypes.CDLL:
         L.route_last_error.argtypes = []
         L.route_last_error.restype = ctypes.c_char_p
         for f in ("route_prepare", "route_destroy", "latent_router_forward", "topk16_select",
-                  "route_step", "route_step_host", "route_device_status"):
+                  "route_step", "route_step_host", "route_step_sumsq", "route_device_status"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -236,6 +237,16 @@ def route_step(plan: Plan, hidden, W_latent, W_router, latent, logits, ids, weig
     p = _proj_ptrs(plan, hidden, W_latent, W_router, latent, logits)
     i, w = _topk_ptrs(plan, ids, weights)
     _check(lib().route_step(plan.handle, *p, i, w, _stream(stream, plan.device)))
+
+
+def route_step_sumsq(plan: Plan, hidden, W_latent, W_router, latent, logits, ids, weights,
+                     latent_sumsq, stream=None) -> None:
+    """route_step that also writes each latent row's sum of squares (FP32 [rows])."""
+    torch = _torch()
+    p = _proj_ptrs(plan, hidden, W_latent, W_router, latent, logits)
+    i, w = _topk_ptrs(plan, ids, weights)
+    ss = _dev_tensor(latent_sumsq, "latent_sumsq", (plan.rows,), (torch.float32,), plan.device)
+    _check(lib().route_step_sumsq(plan.handle, *p, i, w, ss, _stream(stream, plan.device)))
 
 
 def route_step_host(plan: Plan, hidden_host, W_latent, W_router, latent_host, logits_host,

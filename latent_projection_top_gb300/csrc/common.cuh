@@ -56,7 +56,9 @@ constexpr int kDTiles = kDLatTiles + kDRouterTiles;                        // 18
 constexpr int kMaxGrid = 256;
 // device words: [0] status (the rest spare)
 constexpr int kWordStatus = 0;
+constexpr int kWordSsCount = 8;  // [8, 8 + 20): per-row arrivals of latent sum-of-squares parts
 constexpr int kWords = 64;
+static_assert(kWordSsCount + kDecodeMaxRows <= kWords, "word area");
 
 struct DecodeArgs {
     int rows;            // 1..20
@@ -75,6 +77,8 @@ struct DecodeArgs {
     float *logits;
     int32_t *ids;
     float *weights;
+    float *sumsq;                // optional [rows]: sum of squares of each latent row
+    float2 *ss_part;             // with sumsq: [kDecodeMaxRows][14] per-tile parts (hi, lo)
 };
 
 // Internal launchers (defined next to their kernels).  Every launch uses
@@ -91,7 +95,9 @@ cudaError_t decode_launch(int bn, const CUtensorMap &map_h, const CUtensorMap &m
                           const CUtensorMap &map_wr, const DecodeArgs &args, int do_topk,
                           cudaStream_t stream);
 
+// The top-16 of each row; with `sumsq` non-null also the row's latent sum
+// of squares (read from `latent`, which the same predecessor wrote).
 cudaError_t topk_launch(const float *logits, int rows, int32_t *ids, float *weights,
-                        cudaStream_t stream);
+                        const uint16_t *latent, float *sumsq, cudaStream_t stream);
 
 }  // namespace route

@@ -42,6 +42,7 @@
 #include "common.cuh"
 #include "sm103_ptx.cuh"
 #include "topk16.cuh"
+#include "twofloat.cuh"
 
 namespace route {
 namespace {
@@ -87,22 +88,6 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
     d |= 1ull << 46;  // descriptor version for tcgen05
     d |= 2ull << 61;  // 128-byte swizzle
     return d;
-}
-
-// Error-free addition (Knuth's TwoSum): hi + x = s + e exactly; e joins lo.
-__device__ __forceinline__ void two_sum_acc(float &hi, float &lo, float x) {
-    const float s = hi + x;
-    const float bp = s - hi;
-    const float e = (hi - (s - bp)) + (x - bp);
-    hi = s;
-    lo += e;
-}
-
-// The value of a two-float sum.  An infinite high part is the value itself:
-// once a sum reaches +-Inf its error term is Inf - Inf = NaN and must not be
-// added (a NaN high part stays NaN).
-__device__ __forceinline__ float two_float_value(float hi, float lo) {
-    return fabsf(hi) == __int_as_float(0x7F800000) ? hi : hi + lo;
 }
 
 __device__ __forceinline__ uint16_t bf16_bits(float x) {
@@ -345,6 +330,7 @@ __global__ void __maxnreg__(BN == 16 ? 72 : 80)
             const uint32_t use = (uint32_t)(i / C::kNumAcc);
             // Each warp waits on its own; an abort seen by one is seen by all.
             if (!wait_phase(accfull_bar(buf), use & 1u, args, &s_abort)) break;
+            __syncwarp();  // the TMEM loads below are warp-wide (.sync.aligned)
             ptx::tc_fence_after();
             const bool last = i == n_units - 1;
             const bool run_end = last || (u + 1) % kKBlocks == 0;
@@ -451,9 +437,60 @@ int finish_grid(const DecodeArgs &a) {
     return g;
 }
 
+// The latent's per-row sum of squares ("Optionally gather the Kimi3 prefill
+// latent instead of reducing it", Reviewer Notes: the FP32 statistic the
+// latent norm needs), from the BF16 values just stored.  Each (row, tile)
+// item sums its 256 squares (exact in FP32) as a two-float in a fixed order
+// (warp tree, then its 4 warps in order) and stores that part; the item that
+// completes a row (a per-row arrival counter) adds the row's 14 parts in tile
+// order and rounds once, then re-arms the counter for the next launch.  The
+// 128 threads of one item call it together; `ss` is their shared scratch for
+// this iteration, `half` names their barrier.
+__device__ __forceinline__ void latent_sumsq_part(const DecodeArgs &a, int r, int t, uint16_t b0,
+                                                  uint16_t b1, int half, int ht, float2 *ss) {
+    const float v0 = __uint_as_float((uint32_t)b0 << 16), v1 = __uint_as_float((uint32_t)b1 << 16);
+    float hi = v0 * v0, lo = 0.f;
+    two_sum_acc(hi, lo, v1 * v1);
+    warp_two_sum(hi, lo);
+    if ((ht & 31) == 0) ss[ht >> 5] = make_float2(hi, lo);
+    if (half == 0)
+        asm volatile("barrier.sync 2, %0;" ::"n"(kLatentThreads) : "memory");
+    else
+        asm volatile("barrier.sync 3, %0;" ::"n"(kLatentThreads) : "memory");
+    if (ht != 0) return;
+    hi = ss[0].x;
+    lo = ss[0].y;
+#pragma unroll
+    for (int w = 1; w < kLatentThreads / 32; ++w) {
+        two_sum_acc(hi, lo, ss[w].x);
+        lo += ss[w].y;
+    }
+    a.ss_part[r * kDLatTiles + t] = make_float2(hi, lo);
+    // acq_rel: this part is visible before the arrival counts, and the last
+    // arrival sees every other part
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                 : "=r"(old)
+                 : "l"(a.words + kWordSsCount + r)
+                 : "memory");
+    if (old != (unsigned)(kDLatTiles - 1)) return;
+    const float2 p0 = __ldcg(a.ss_part + r * kDLatTiles);
+    hi = p0.x;
+    lo = p0.y;
+#pragma unroll
+    for (int u = 1; u < kDLatTiles; ++u) {
+        const float2 p = __ldcg(a.ss_part + r * kDLatTiles + u);
+        two_sum_acc(hi, lo, p.x);
+        lo += p.y;
+    }
+    a.sumsq[r] = two_float_value(hi, lo);
+    a.words[kWordSsCount + r] = 0u;
+}
+
 __global__ void __maxnreg__(112) decode_finish_kernel(const __grid_constant__ DecodeArgs a,
                                                       int do_topk) {
     __shared__ TopkBlockSmem s_topk;
+    __shared__ float2 s_ss[2][2][kLatentThreads / 32];  // [iteration parity][half][warp]
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the stream kernel's partials are complete
     const int rows = a.rows;
@@ -480,13 +517,18 @@ __global__ void __maxnreg__(112) decode_finish_kernel(const __grid_constant__ De
     } else {
         const int n_items = kDLatTiles * rows;
         const int stride = 2 * ((int)gridDim.x - rows);
-        for (int i = 2 * (b - rows) + tid / kLatentThreads; i < n_items; i += stride) {
+        const int half = tid / kLatentThreads;
+        int parity = 0;
+        for (int i = 2 * (b - rows) + half; i < n_items; i += stride, parity ^= 1) {
             const int r = i / kDLatTiles;
             const int t[1] = {i % kDLatTiles}, cc[1] = {2 * (tid % kLatentThreads)};
             float2 y[1];
             sum_slot_pairs<1>(a, r, t, cc, y);
+            const uint16_t b0 = bf16_bits(y[0].x), b1 = bf16_bits(y[0].y);
             *reinterpret_cast<uint32_t *>(a.latent + (size_t)r * kLatent + t[0] * kDTileCols + cc[0]) =
-                (uint32_t)bf16_bits(y[0].x) | ((uint32_t)bf16_bits(y[0].y) << 16);
+                (uint32_t)b0 | ((uint32_t)b1 << 16);
+            if (a.sumsq != nullptr)
+                latent_sumsq_part(a, r, t[0], b0, b1, half, tid % kLatentThreads, s_ss[parity][half]);
         }
     }
 }

@@ -21,8 +21,11 @@
 //
 // Warp roles (192 threads, persistent, one CTA per SM, pairs = clusters):
 //   warp 0      TMA producer (both CTAs): its halves into a 6-stage ring;
-//               completion is counted on the leader CTA's barrier
+//               completion is counted on the leader CTA's barrier, which the
+//               leader arms for both CTAs' bytes before either may fill the
+//               stage (so its transaction count never goes below zero)
 //   warp 1      TMEM owner (both CTAs); the leader's lane 0 issues the MMAs
+//               and re-arms each stage's barrier once it has consumed it
 //   warps 2..5  epilogue (both CTAs): TMEM -> registers -> global
 // Pairs walk the (column tile, row tile) grid with stride = number of pairs;
 // two TMEM accumulators let one tile's epilogue overlap the next main loop.
@@ -52,10 +55,7 @@ constexpr uint32_t kBHalfBytes = kHalf * 128;              // 128 token rows x 6
 constexpr uint32_t kAHalfBytes = 2 * kABoxBytes;           // 128 weight columns x 64 k
 constexpr uint32_t kStageBytes = kBHalfBytes + kAHalfBytes;  // B half first, then A half
 constexpr int kStages = 6;
-// The ring is followed by 16 KB that nothing fills, so that every operand
-// read the MMA can make from a stage stays inside this CTA's allocation.
-constexpr uint32_t kGuardBytes = 16384;
-constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + kGuardBytes + 256;
+constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + 256;
 constexpr uint32_t kTmemCols = 512;                        // two accumulators of 256 columns
 constexpr int kLatPairTiles = kLatent / kPairCols;         // 14
 constexpr int kPairColTiles = kLatPairTiles + (kExperts + kPairCols - 1) / kPairCols;  // 18
@@ -142,7 +142,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
     // one names the same operand or barrier in the other.
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
-    const uint32_t bars = sbase + kStages * kStageBytes + kGuardBytes;
+    const uint32_t bars = sbase + kStages * kStageBytes;
     auto full_bar = [&](int s) { return bars + 8u * s; };                 // leader's are used
     auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
     auto accfull_bar = [&](int b) { return bars + 8u * (2 * kStages + b); };
@@ -169,6 +169,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
             ptx::mbar_init(accempty_bar(b), 2);  // one arrival from each CTA's epilogue
         }
         ptx::mbar_init(drain_bar, 1);
+        // the leader arms the first round of every stage that will be filled
+        const int first = nseg * kKBlocks < kStages ? nseg * kKBlocks : kStages;
+        if (leader)
+            for (int s = 0; s < first; ++s) ptx::mbar_arrive_expect_tx(full_bar(s), 2 * kStageBytes);
         ptx::fence_barrier_init();
         ptx::prefetch_tensormap(&map_h);
         ptx::prefetch_tensormap(&map_wl);
@@ -210,9 +214,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
             // Weight boxes of the first stages go out before the grid
             // dependency resolves (no predecessor writes the weights).
             for (int it = 0; it < n_pre; ++it) {
-                const uint32_t fb = ptx::map_to_rank(full_bar(it), 0u);
-                if (leader) ptx::mbar_arrive_expect_tx(full_bar(it), 2 * kStageBytes);
-                weights_of(it, sbase + it * kStageBytes, fb);
+                weights_of(it, sbase + it * kStageBytes, ptx::map_to_rank(full_bar(it), 0u));
                 armed |= 1u << it;
             }
             asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -231,7 +233,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
                 if (args.test_stall && leader && it == total - 1) continue;  // test hook
                 const uint32_t st = sbase + s * kStageBytes;
                 const uint32_t fb = ptx::map_to_rank(full_bar(s), 0u);
-                if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), 2 * kStageBytes);
                 weights_of(it, st, fb);
                 hidden_of(it, st, fb);
                 armed |= 1u << s;
@@ -276,6 +277,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
                         const uint64_t db = smem_desc(b + kk * 32u, 16u, 1024u);
                         ptx::mma_bf16_pair(d_tmem, da, db, kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
                     }
+                    // re-arm stage s for its next round before it is freed:
+                    // the copies that fill it can only start after the commit
+                    if (it + kStages < (uint32_t)(nseg * kKBlocks))
+                        ptx::mbar_arrive_expect_tx(full_bar(s), 2 * kStageBytes);
                     ptx::mma_commit_pair(empty_bar(s), 0x3);  // frees stage s in both CTAs
                 }
                 if (ok) ptx::mma_commit_pair(accfull_bar(buf), 0x3);
@@ -295,6 +300,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
             const uint32_t use = (uint32_t)(i >> 1);
             const bool ok = wait_phase(accfull_bar(buf), use & 1u, args, &s_abort);
             if (!ptx::named_bar_and(1, 128, ok)) break;
+            __syncwarp();  // the TMEM loads below are warp-wide (.sync.aligned)
             ptx::tc_fence_after();
             const uint32_t taddr =
                 tmem_base + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * kPairRows);

@@ -25,7 +25,7 @@ struct route_plan {
     int segments;
     ProjArgs pre;             // prefill launch arguments (per-call pointers added at launch)
     DecodeArgs dec;           // decode launch arguments, incl. the split-K partition
-    float2 *ws;               // decode cluster partials
+    float2 *ws;               // decode split-K partials, then the sum-of-squares parts
     unsigned *words;          // device status word (+ spare)
     uint8_t *staging;         // device staging for route_step_host
     size_t staging_bytes;
@@ -168,7 +168,7 @@ route_status encode_all(const route_plan *p, const void *hidden, const void *W_l
 // The projection (and, for decode with do_topk, the top-16) of one step.
 route_status launch_forward(const route_plan *p, const void *hidden, const void *W_latent,
                             const void *W_router, void *latent, float *logits, int32_t *ids,
-                            float *weights, int do_topk, cudaStream_t stream) {
+                            float *weights, int do_topk, float *sumsq, cudaStream_t stream) {
     CUtensorMap mh, ml, mr;
     route_status st = encode_all(p, hidden, W_latent, W_router, &mh, &ml, &mr);
     if (st != ROUTE_OK) return st;
@@ -179,6 +179,7 @@ route_status launch_forward(const route_plan *p, const void *hidden, const void 
         a.logits = logits;
         a.ids = ids;
         a.weights = weights;
+        a.sumsq = sumsq;
         e = decode_launch(p->bn, mh, ml, mr, a, do_topk, stream);
         if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
     } else {
@@ -188,7 +189,8 @@ route_status launch_forward(const route_plan *p, const void *hidden, const void 
         e = prefill_launch(mh, ml, mr, a, stream);
         if (e != cudaSuccess) return cuda_fail(e, "prefill kernel launch");
         if (do_topk) {
-            e = topk_launch(logits, p->rows, ids, weights, stream);
+            e = topk_launch(logits, p->rows, ids, weights, static_cast<const uint16_t *>(latent),
+                            sumsq, stream);
             if (e != cudaSuccess) return cuda_fail(e, "top-16 kernel launch");
         }
     }
@@ -220,8 +222,9 @@ route_status check_topk_args(const route_plan *p, const float *logits, const int
 
 route_status run_step(const route_plan *p, const void *hidden, const void *W_latent,
                       const void *W_router, void *latent, float *logits, int32_t *ids,
-                      float *weights, cudaStream_t stream) {
-    return launch_forward(p, hidden, W_latent, W_router, latent, logits, ids, weights, 1, stream);
+                      float *weights, cudaStream_t stream, float *sumsq = nullptr) {
+    return launch_forward(p, hidden, W_latent, W_router, latent, logits, ids, weights, 1, sumsq,
+                          stream);
 }
 
 // Decode stream grid: the largest CTA count, at most one per SM and at most
@@ -396,11 +399,13 @@ route_status route_prepare(int mode, int rows, int device, route_plan **out) {
         a.timeout_ns = kDefaultTimeoutNs;
         decode_partition(a, decode_grid(sms, kMaxGrid), &p->segments);
         const size_t ws_bytes = (size_t)p->segments * kDecodeMaxRows * kDTileCols * sizeof(float2);
-        if ((e = cudaMalloc(&p->ws, ws_bytes)) != cudaSuccess) {
+        const size_t ss_bytes = (size_t)kDecodeMaxRows * kDLatTiles * sizeof(float2);
+        if ((e = cudaMalloc(&p->ws, ws_bytes + ss_bytes)) != cudaSuccess) {
             free_plan(p);
             return cuda_fail(e, "cudaMalloc(split-K scratch)");
         }
         a.ws = p->ws;
+        a.ss_part = reinterpret_cast<float2 *>(reinterpret_cast<uint8_t *>(p->ws) + ws_bytes);
         a.words = p->words;
         p->grid = a.grid;
     } else {
@@ -443,6 +448,7 @@ route_status latent_router_forward(const route_plan *plan, const void *hidden,
     DeviceGuard guard(plan->device);
     if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
     return launch_forward(plan, hidden, W_latent, W_router, latent, logits, nullptr, nullptr, 0,
+                          nullptr,
                           static_cast<cudaStream_t>(stream));
 }
 
@@ -452,7 +458,8 @@ route_status topk16_select(const route_plan *plan, const float *logits, int32_t 
     if (st != ROUTE_OK) return st;
     DeviceGuard guard(plan->device);
     if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
-    cudaError_t e = topk_launch(logits, plan->rows, ids, weights, static_cast<cudaStream_t>(stream));
+    cudaError_t e = topk_launch(logits, plan->rows, ids, weights, nullptr, nullptr,
+                                static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "top-16 kernel launch");
     return ROUTE_OK;
 }
@@ -467,6 +474,21 @@ route_status route_step(const route_plan *plan, const void *hidden, const void *
     if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
     return run_step(plan, hidden, W_latent, W_router, latent, logits, ids, weights,
                     static_cast<cudaStream_t>(stream));
+}
+
+route_status route_step_sumsq(const route_plan *plan, const void *hidden, const void *W_latent,
+                              const void *W_router, void *latent, float *logits, int32_t *ids,
+                              float *weights, float *latent_sumsq, void *stream) {
+    route_status st = check_forward_args(plan, hidden, W_latent, W_router, latent, logits);
+    if (st != ROUTE_OK) return st;
+    if ((st = check_topk_args(plan, logits, ids, weights)) != ROUTE_OK) return st;
+    if (!latent_sumsq) return fail(ROUTE_ERR_NULL, "latent_sumsq must be non-NULL");
+    if ((reinterpret_cast<uintptr_t>(latent_sumsq) & 3u) != 0)
+        return fail(ROUTE_ERR_ALIGN, "latent_sumsq must be 4-byte aligned");
+    DeviceGuard guard(plan->device);
+    if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+    return run_step(plan, hidden, W_latent, W_router, latent, logits, ids, weights,
+                    static_cast<cudaStream_t>(stream), latent_sumsq);
 }
 
 route_status route_step_host(const route_plan *plan, const void *hidden_host,

@@ -291,8 +291,10 @@ __device__ __forceinline__ float4 ld_cluster_f4(uint32_t cluster_addr) {
 
 // ---- named barrier over a subset of the CTA's warps ---------------------------
 
+// Non-aligned form: lanes of a warp may arrive separately (after divergent
+// waits), which the aligned bar.sync does not allow.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+    asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 // Barrier that also ANDs a predicate across the participating threads.

@@ -237,7 +237,7 @@ __device__ __forceinline__ void topk16_block(const float (&v)[4], const int (&id
     }
     sh.tmax[tid] = m;
     if (tid == 0) sh.count = 0u;
-    asm volatile("bar.sync %0, %1;" ::"r"(bar), "n"(kThreads) : "memory");
+    asm volatile("barrier.sync %0, %1;" ::"r"(bar), "n"(kThreads) : "memory");
     if (tid < 32) {
         uint32_t lm = 0u;
 #pragma unroll
@@ -245,7 +245,7 @@ __device__ __forceinline__ void topk16_block(const float (&v)[4], const int (&id
         const uint32_t T = warp_16th_largest(lm, tid);
         if (tid == 0) sh.T = T;
     }
-    asm volatile("bar.sync %0, %1;" ::"r"(bar), "n"(kThreads) : "memory");
+    asm volatile("barrier.sync %0, %1;" ::"r"(bar), "n"(kThreads) : "memory");
     const uint32_t T = sh.T;
 #pragma unroll
     for (int j = 0; j < 4; ++j)
@@ -253,7 +253,7 @@ __device__ __forceinline__ void topk16_block(const float (&v)[4], const int (&id
             const uint32_t pos = atomicAdd(&sh.count, 1u);
             if (pos < (uint32_t)kCandMax) sh.cand[pos] = make_uint2(key[j], (uint32_t)id[j]);
         }
-    asm volatile("bar.sync %0, %1;" ::"r"(bar), "n"(kThreads) : "memory");
+    asm volatile("barrier.sync %0, %1;" ::"r"(bar), "n"(kThreads) : "memory");
     if (tid >= 32) return;
     const uint32_t total = sh.count;
     if (total > (uint32_t)kCandMax) {
