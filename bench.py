@@ -298,13 +298,15 @@ class RouteBench:
                 torch.empty((rows, route.TOPK), dtype=torch.float32, device=self.dev))
 
     def make_steps(self, workload: str, rows: int, nbanks: int, gemm_only: bool = False,
-                   overlap: bool = False, sumsq: bool = False):
+                   overlap: bool = False, sumsq: bool = False, ksplit: bool = False):
         """Closures, one per bank, each enqueuing one layer's route step."""
         route = self.route
         mode = route.DECODE if workload.startswith("decode") else route.PREFILL
         plan = route.Plan(mode, rows, self.device)
         if overlap:
             route.route_set_overlap(plan, True)
+        if ksplit:
+            route.route_set_latent_ksplit(plan, True)
         banks = self.weight_banks("decode" if mode == route.DECODE else "prefill", nbanks)
         hs = self.hidden(workload, rows, nbanks)
         outs = [self.outputs(rows) for _ in range(nbanks)]
@@ -575,6 +577,18 @@ def sweep(rb, dist, peaks, args):
             algo = WEIGHT_BYTES + rows * (ROW_BYTES + 4)
             e.update({"bound": "hbm", "frac": round(algo / t / 1e9 / peaks["hbm_gbs"], 4)})
         res.append(e)
+    # the decode step with the general path's K-split latent arithmetic
+    for wk, rows in [("decode_r8", 8), ("decode_sweep", 20)]:
+        plan, steps, _ = rb.make_steps(wk, rows, 8, overlap=True, ksplit=True)
+        ms, _ = rb.run(steps, 64 * 64, 64 * 8, dist)
+        rb.route.route_device_status(plan)
+        t = dist.max(ms) / 1e3 / (64 * 64)
+        plan.close()
+        algo = WEIGHT_BYTES + rows * ROW_BYTES
+        res.append({"workload": wk, "rows": rows, "latent": "k-split (8 BF16 partials)",
+                    "overlap": True, "us_per_layer": round(t * 1e6, 3),
+                    "rows_per_s": round(rows / t, 1), "bound": "hbm",
+                    "frac": round(algo / t / 1e9 / peaks["hbm_gbs"], 4)})
     return res
 
 

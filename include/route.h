@@ -182,6 +182,21 @@ route_status route_device_status(const route_plan *plan);
 route_status route_set_overlap(route_plan *plan, int enable);
 
 /*
+ * route_set_latent_ksplit: compute a decode plan's latent with the general
+ * (K-split) path's arithmetic instead of one full-K sum: K is cut into eight
+ * 896-deep slices, each slice's FP32 partial is rounded to BF16, the eight
+ * BF16 partials are summed in FP32 in slice order and the sum is rounded to
+ * BF16 again ("Optionally gather the Kimi3 prefill latent instead of reducing
+ * it", Description, Numerics bullet and commit body: the path whose numbers
+ * existing captured packages were made with).  Logits, ids and weights are
+ * unchanged.  Needs the decode split-K partition to give each CTA exactly one
+ * K slice of a latent tile (it does on a 152-SM GB300: 144 CTAs of 14
+ * k-blocks); otherwise ROUTE_ERR_PLAN.  Prefill plans: ROUTE_ERR_MODE.
+ * Default: disabled (full-K latent).
+ */
+route_status route_set_latent_ksplit(route_plan *plan, int enable);
+
+/*
  * route_test_stall: TEST HOOK for the bounded-wait path, not for production.
  * With enable != 0, each CTA of the plan's projection kernel skips its last
  * weight copy, so its MMA warp waits for data that never arrives; after

@@ -46,6 +46,7 @@ EXPORTS = (
     "route_step_host", "route_device_status", "route_plan_rows", "route_plan_mode",
     "route_plan_grid", "route_plan_segments", "route_last_error", "route_test_stall",
     "route_set_overlap", "route_step_decode_noalloc", "route_step_sumsq",
+    "route_set_latent_ksplit",
 )
 
 
@@ -84,6 +85,8 @@ def lib() -> ctypes.CDLL:
         L.route_step_decode_noalloc.restype = i32
         L.route_set_overlap.argtypes = [vp, i32]
         L.route_set_overlap.restype = i32
+        L.route_set_latent_ksplit.argtypes = [vp, i32]
+        L.route_set_latent_ksplit.restype = i32
         L.route_test_stall.argtypes = [vp, i32, ctypes.c_uint64]
         L.route_test_stall.restype = i32
         for f in ("route_plan_rows", "route_plan_mode", "route_plan_grid", "route_plan_segments"):
@@ -268,6 +271,12 @@ def route_set_overlap(plan: Plan, enable: bool) -> None:
     """Let the decode weight stream overlap the previous route step's tail; only
     when `hidden` is not written by the route call just before (include/route.h)."""
     _check(lib().route_set_overlap(plan.handle, int(bool(enable))))
+
+
+def route_set_latent_ksplit(plan: Plan, enable: bool) -> None:
+    """Decode latent with the general path's K-split arithmetic (eight BF16-rounded
+    K-slice partials, FP32 sum, BF16 again); see include/route.h."""
+    _check(lib().route_set_latent_ksplit(plan.handle, int(bool(enable))))
 
 
 def route_test_stall(plan: Plan, enable: bool, timeout_ns: int = 1_000_000) -> None:

@@ -21,6 +21,7 @@ constexpr int kDecodeMaxRows = 20;
 // K is consumed 64 at a time.
 constexpr int kKBlock = 64;
 constexpr int kKBlocks = kHidden / kKBlock;                 // 112
+constexpr int kKSplitSlices = 8;                            // the general path's K slices (896 deep)
 // Prefill tiling: one tile = 256 weight columns (the MMA M side, split over a
 // pair of CTAs) x 256 token rows (the MMA N side; each CTA of the pair loads
 // 128 of them): 14 latent + 4 router column tiles, the last with 128 real
@@ -65,6 +66,7 @@ struct DecodeArgs {
     int grid;            // CTAs of the stream kernel (<= kMaxGrid)
     int test_stall;      // test hook: skip each CTA's last copy so a wait must time out
     int overlap;         // read hidden before the grid dependency resolves
+    int ksplit;          // latent with the general path's K-split arithmetic
     unsigned long long timeout_ns;
     int cta_unit[kMaxGrid + 1];  // CTA g owns units [cta_unit[g], cta_unit[g+1]); unit u =
                                  // (tile u / 112, k-block u % 112)

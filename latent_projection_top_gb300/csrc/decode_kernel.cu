@@ -414,6 +414,31 @@ __device__ __forceinline__ void sum_slot_pairs(const DecodeArgs &a, int r, const
                                                     two_float_value(h[2 * q + 1], l[2 * q + 1]));
 }
 
+// The general path's latent arithmetic ("Optionally gather the Kimi3 prefill
+// latent instead of reducing it", Description, Numerics bullet, and commit
+// body: eight K-slice partials, each rounded to BF16, summed in FP32, rounded
+// to BF16 again).  With the partition aligned to the eight 896-deep K slices
+// (checked on the host), slot j of a latent tile is slice j: each slot's
+// two-float partial is rounded to FP32 and then to BF16, and the BF16 values
+// are added in FP32 in slice order; the caller rounds the sum to BF16.
+__device__ __forceinline__ float2 ksplit_slot_pair(const DecodeArgs &a, int r, int t, int cc) {
+    const float4 *p = reinterpret_cast<const float4 *>(a.ws) +
+                      ((size_t)a.seg_base[t] * kDecodeMaxRows + r) * (kDTileCols / 2) + cc / 2;
+    const int n = a.seg_count[t];
+    float4 v[kFinishBatch];
+#pragma unroll
+    for (int j = 0; j < kFinishBatch; ++j)
+        if (j < n) v[j] = __ldcg(p + j * kSlotF4);
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < kFinishBatch; ++j)
+        if (j < n) {
+            s0 += __uint_as_float((uint32_t)bf16_bits(two_float_value(v[j].x, v[j].y)) << 16);
+            s1 += __uint_as_float((uint32_t)bf16_bits(two_float_value(v[j].z, v[j].w)) << 16);
+        }
+    return make_float2(s0, s1);
+}
+
 // Small CTAs that fit on an SM next to a stream CTA: with overlap, the finish
 // of one step runs under the next step's weight stream, and the next stream
 // stores its partials only once this kernel is complete.  Under that load a
@@ -523,7 +548,10 @@ __global__ void __maxnreg__(112) decode_finish_kernel(const __grid_constant__ De
             const int r = i / kDLatTiles;
             const int t[1] = {i % kDLatTiles}, cc[1] = {2 * (tid % kLatentThreads)};
             float2 y[1];
-            sum_slot_pairs<1>(a, r, t, cc, y);
+            if (a.ksplit)
+                y[0] = ksplit_slot_pair(a, r, t[0], cc[0]);
+            else
+                sum_slot_pairs<1>(a, r, t, cc, y);
             const uint16_t b0 = bf16_bits(y[0].x), b1 = bf16_bits(y[0].y);
             *reinterpret_cast<uint32_t *>(a.latent + (size_t)r * kLatent + t[0] * kDTileCols + cc[0]) =
                 (uint32_t)b0 | ((uint32_t)b1 << 16);

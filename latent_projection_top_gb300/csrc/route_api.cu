@@ -552,6 +552,29 @@ route_status route_set_overlap(route_plan *plan, int enable) {
     return ROUTE_OK;
 }
 
+route_status route_set_latent_ksplit(route_plan *plan, int enable) {
+    route_status st = check_plan(plan);
+    if (st != ROUTE_OK) return st;
+    if (plan->mode != ROUTE_DECODE)
+        return fail(ROUTE_ERR_MODE, "the K-split latent is available for decode plans only");
+    if (enable) {
+        // every CTA that touches a latent tile must own exactly one K slice of it
+        constexpr int kSlice = kKBlocks / kKSplitSlices;  // 14 k-blocks = 896 of K
+        const DecodeArgs &a = plan->dec;
+        for (int g = 0; g < a.grid; ++g) {
+            const int u0 = a.cta_unit[g], u1 = a.cta_unit[g + 1];
+            if (u0 >= kDLatTiles * kKBlocks) break;
+            if (u0 % kSlice != 0 || u1 - u0 != kSlice)
+                return fail(ROUTE_ERR_PLAN,
+                            "this device's split-K partition (%d CTAs) does not align with the %d "
+                            "K slices the K-split latent needs",
+                            a.grid, kKSplitSlices);
+        }
+    }
+    plan->dec.ksplit = enable ? 1 : 0;
+    return ROUTE_OK;
+}
+
 route_status route_test_stall(route_plan *plan, int enable, uint64_t timeout_ns) {
     route_status st = check_plan(plan);
     if (st != ROUTE_OK) return st;
