@@ -577,18 +577,22 @@ def sweep(rb, dist, peaks, args):
             algo = WEIGHT_BYTES + rows * (ROW_BYTES + 4)
             e.update({"bound": "hbm", "frac": round(algo / t / 1e9 / peaks["hbm_gbs"], 4)})
         res.append(e)
-    # the decode step with the general path's K-split latent arithmetic
-    for wk, rows in [("decode_r8", 8), ("decode_sweep", 20)]:
-        plan, steps, _ = rb.make_steps(wk, rows, 8, overlap=True, ksplit=True)
-        ms, _ = rb.run(steps, 64 * 64, 64 * 8, dist)
+    # the step with the general path's K-split latent arithmetic
+    for wk, rows in [("decode_r8", 8), ("decode_sweep", 20), ("prefill_r3072", 3072)]:
+        decode = wk.startswith("decode")
+        nb = 8 if decode else args.prefill_banks
+        plan, steps, _ = rb.make_steps(wk, rows, nb, overlap=decode, ksplit=True)
+        n, w, gl = (64 * 64, 64 * 8, 64) if decode else (92 * 5, 92 * 2, 92)
+        ms, _ = rb.run(steps, n, w, dist, graph_len=gl)
         rb.route.route_device_status(plan)
-        t = dist.max(ms) / 1e3 / (64 * 64)
+        t = dist.max(ms) / 1e3 / n
         plan.close()
-        algo = WEIGHT_BYTES + rows * ROW_BYTES
-        res.append({"workload": wk, "rows": rows, "latent": "k-split (8 BF16 partials)",
-                    "overlap": True, "us_per_layer": round(t * 1e6, 3),
-                    "rows_per_s": round(rows / t, 1), "bound": "hbm",
-                    "frac": round(algo / t / 1e9 / peaks["hbm_gbs"], 4)})
+        e = {"workload": wk, "rows": rows, "latent": "k-split (8 BF16 partials)",
+             "overlap": decode, "us_per_layer": round(t * 1e6, 3), "rows_per_s": round(rows / t, 1)}
+        if decode:
+            algo = WEIGHT_BYTES + rows * ROW_BYTES
+            e.update({"bound": "hbm", "frac": round(algo / t / 1e9 / peaks["hbm_gbs"], 4)})
+        res.append(e)
     return res
 
 

@@ -189,10 +189,11 @@ route_status route_set_overlap(route_plan *plan, int enable);
  * BF16 again ("Optionally gather the Kimi3 prefill latent instead of reducing
  * it", Description, Numerics bullet and commit body: the path whose numbers
  * existing captured packages were made with).  Logits, ids and weights are
- * unchanged.  Needs the decode split-K partition to give each CTA exactly one
- * K slice of a latent tile (it does on a 152-SM GB300: 144 CTAs of 14
- * k-blocks); otherwise ROUTE_ERR_PLAN.  Prefill plans: ROUTE_ERR_MODE.
- * Default: disabled (full-K latent).
+ * unchanged.  Decode plans need their split-K partition to give each CTA
+ * exactly one K slice of a latent tile (it does on a 152-SM GB300: 144 CTAs
+ * of 14 k-blocks); otherwise ROUTE_ERR_PLAN.  Prefill plans drain and re-start
+ * each latent tile's accumulator at every slice boundary (slower: the tensor
+ * cores wait for each slice's drain).  Default: disabled (full-K latent).
  */
 route_status route_set_latent_ksplit(route_plan *plan, int enable);
 

@@ -22,6 +22,7 @@ constexpr int kDecodeMaxRows = 20;
 constexpr int kKBlock = 64;
 constexpr int kKBlocks = kHidden / kKBlock;                 // 112
 constexpr int kKSplitSlices = 8;                            // the general path's K slices (896 deep)
+static_assert(kKBlocks % kKSplitSlices == 0, "K slices of whole k-blocks");
 // Prefill tiling: one tile = 256 weight columns (the MMA M side, split over a
 // pair of CTAs) x 256 token rows (the MMA N side; each CTA of the pair loads
 // 128 of them): 14 latent + 4 router column tiles, the last with 128 real
@@ -42,6 +43,7 @@ struct ProjArgs {
     int row_tiles;       // ceil(rows / kPrefillBN)
     int grid;            // persistent CTAs launched (pairs of CTAs: even)
     int test_stall;      // test hook: skip each CTA's last copy so a wait must time out
+    int ksplit;          // latent with the general path's K-split arithmetic
     unsigned long long timeout_ns;  // bound on every wait inside the kernel
     unsigned *status;          // device status word
     uint16_t *latent;          // [rows, 3584] BF16 bits

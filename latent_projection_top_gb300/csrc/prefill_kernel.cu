@@ -248,42 +248,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             // ---------------- MMA issuer (leader CTA) ----------------
-            uint32_t it = 0;
+            uint32_t it = 0, job = 0;
             bool ok = true;
             for (int i = 0; i < nseg && ok; ++i) {
-                const int buf = i & 1;
-                const uint32_t use = (uint32_t)(i >> 1);
-                if (!wait_phase(accempty_bar(buf), (use & 1u) ^ 1u, args, &s_abort)) break;
-                ptx::tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kPairRows);
-                for (int kb = 0; kb < kKBlocks; ++kb, ++it) {
-                    const int s = (int)(it % kStages);
-                    const uint32_t ph = (it / kStages) & 1u;
-                    if (!wait_phase(full_bar(s), ph, args, &s_abort)) {
+                const Tile tl = tile_get(args, pair, npairs, i);
+                const int njobs = (args.ksplit && tl.c < kLatPairTiles) ? kKSplitSlices : 1;
+                const int kb_per_job = kKBlocks / njobs;
+                for (int j = 0; j < njobs && ok; ++j, ++job) {
+                    const int buf = args.ksplit ? 0 : (int)(job & 1u);
+                    const uint32_t use = args.ksplit ? job : (job >> 1);
+                    if (!wait_phase(accempty_bar(buf), (use & 1u) ^ 1u, args, &s_abort)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t b = sbase + s * kStageBytes;
-                    const uint32_t a = b + kBHalfBytes;
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kPairRows);
+                    for (int kb = 0; kb < kb_per_job; ++kb, ++it) {
+                        const int s = (int)(it % kStages);
+                        const uint32_t ph = (it / kStages) & 1u;
+                        if (!wait_phase(full_bar(s), ph, args, &s_abort)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        const uint32_t b = sbase + s * kStageBytes;
+                        const uint32_t a = b + kBHalfBytes;
 #pragma unroll
-                    for (int kk = 0; kk < kKBlock / 16; ++kk) {
-                        // A: k advances 16 rows = two 8-row swizzle atoms (2048 B);
-                        //    the two 64-column boxes are 8192 B apart (LBO),
-                        //    8-row k groups 1024 B apart (SBO).
-                        // B: k advances 32 B inside the 128-byte swizzled row;
-                        //    8-row groups of token rows are 1024 B apart (SBO).
-                        const uint64_t da = smem_desc(a + kk * 2048u, kABoxBytes, 1024u);
-                        const uint64_t db = smem_desc(b + kk * 32u, 16u, 1024u);
-                        ptx::mma_bf16_pair(d_tmem, da, db, kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < kKBlock / 16; ++kk) {
+                            // A: k advances 16 rows = two 8-row swizzle atoms (2048 B);
+                            //    the two 64-column boxes are 8192 B apart (LBO),
+                            //    8-row k groups 1024 B apart (SBO).
+                            // B: k advances 32 B inside the 128-byte swizzled row;
+                            //    8-row groups of token rows are 1024 B apart (SBO).
+                            const uint64_t da = smem_desc(a + kk * 2048u, kABoxBytes, 1024u);
+                            const uint64_t db = smem_desc(b + kk * 32u, 16u, 1024u);
+                            ptx::mma_bf16_pair(d_tmem, da, db, kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        // re-arm stage s for its next round before it is freed:
+                        // the copies that fill it can only start after the commit
+                        if (it + kStages < (uint32_t)(nseg * kKBlocks))
+                            ptx::mbar_arrive_expect_tx(full_bar(s), 2 * kStageBytes);
+                        ptx::mma_commit_pair(empty_bar(s), 0x3);  // frees stage s in both CTAs
                     }
-                    // re-arm stage s for its next round before it is freed:
-                    // the copies that fill it can only start after the commit
-                    if (it + kStages < (uint32_t)(nseg * kKBlocks))
-                        ptx::mbar_arrive_expect_tx(full_bar(s), 2 * kStageBytes);
-                    ptx::mma_commit_pair(empty_bar(s), 0x3);  // frees stage s in both CTAs
+                    if (ok) ptx::mma_commit_pair(accfull_bar(buf), 0x3);
                 }
-                if (ok) ptx::mma_commit_pair(accfull_bar(buf), 0x3);
             }
             ptx::mma_commit_pair(drain_bar, 0x3);  // every MMA retired before TMEM is freed
             wait_drain(drain_bar, 0u, args);
@@ -294,46 +302,85 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
         const int col = 32 * quarter + lane;
         const int rows = args.rows;
         asm volatile("griddepcontrol.wait;" ::: "memory");  // outputs may still be read by the predecessor
-        for (int i = 0; i < nseg; ++i) {
+        uint32_t job = 0;
+        bool go = true;
+        for (int i = 0; i < nseg && go; ++i) {
             const Tile tl = tile_get(args, pair, npairs, i);
-            const int buf = i & 1;
-            const uint32_t use = (uint32_t)(i >> 1);
-            const bool ok = wait_phase(accfull_bar(buf), use & 1u, args, &s_abort);
-            if (!ptx::named_bar_and(1, 128, ok)) break;
-            __syncwarp();  // the TMEM loads below are warp-wide (.sync.aligned)
-            ptx::tc_fence_after();
-            const uint32_t taddr =
-                tmem_base + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * kPairRows);
             const bool lat = tl.c < kLatPairTiles;
+            const int njobs = (args.ksplit && lat) ? kKSplitSlices : 1;
             const int ncol = (lat ? tl.c : tl.c - kLatPairTiles) * kPairCols + (int)rank * kHalf + col;
             const bool valid = lat || ncol < kExperts;
-#pragma unroll 1
-            for (int ch = 0; ch < kPairRows / 16; ++ch) {
-                uint32_t u[16];
-                ptx::tmem_ld_x16(taddr + ch * 16, u);
-                ptx::tmem_ld_wait();
-                const int r0 = tl.rt * kPairRows + ch * 16;
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int r = r0 + j;
-                    if (valid && r < rows) {
-                        const float x = __uint_as_float(u[j]);
-                        if (lat)
-                            args.latent[(size_t)r * kLatent + ncol] = bf16_bits(x);
-                        else
-                            args.logits[(size_t)r * kExperts + ncol] = x;
-                    }
+            for (int j = 0; j < njobs; ++j, ++job) {
+                const int buf = args.ksplit ? 0 : (int)(job & 1u);
+                const uint32_t use = args.ksplit ? job : (job >> 1);
+                const bool ok = wait_phase(accfull_bar(buf), use & 1u, args, &s_abort);
+                if (!ptx::named_bar_and(1, 128, ok)) {
+                    go = false;
+                    break;
                 }
-            }
-            // all 128 epilogue threads are done with this accumulator: one
-            // arrival from this CTA on the leader's barrier
-            ptx::tc_fence_before();
-            ptx::named_bar_sync(2, 128);
-            if (threadIdx.x == 64) {
-                if (leader)
-                    ptx::mbar_arrive(accempty_bar(buf));
-                else
-                    ptx::mbar_arrive_remote(ptx::map_to_rank(accempty_bar(buf), 0u));
+                __syncwarp();  // the TMEM loads below are warp-wide (.sync.aligned)
+                ptx::tc_fence_after();
+                const uint32_t lanes = tmem_base + ((uint32_t)(32 * quarter) << 16);
+                const uint32_t taddr = lanes + (uint32_t)(buf * kPairRows);
+                if (njobs == 1) {
+#pragma unroll 1
+                    for (int ch = 0; ch < kPairRows / 16; ++ch) {
+                        uint32_t u[16];
+                        ptx::tmem_ld_x16(taddr + ch * 16, u);
+                        ptx::tmem_ld_wait();
+                        const int r0 = tl.rt * kPairRows + ch * 16;
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const int r = r0 + jj;
+                            if (valid && r < rows) {
+                                const float x = __uint_as_float(u[jj]);
+                                if (lat)
+                                    args.latent[(size_t)r * kLatent + ncol] = bf16_bits(x);
+                                else
+                                    args.logits[(size_t)r * kExperts + ncol] = x;
+                            }
+                        }
+                    }
+                } else {
+                    // K-split latent: slice j's partial, rounded to BF16, is
+                    // added in FP32 to the running sum kept in the other half
+                    // of TMEM; the last slice rounds the sum to BF16 and stores.
+                    const uint32_t tsum = lanes + (uint32_t)kPairRows;
+                    const bool last = j == njobs - 1;
+#pragma unroll 1
+                    for (int ch = 0; ch < kPairRows / 16; ++ch) {
+                        uint32_t u[16], acc[16];
+                        ptx::tmem_ld_x16(taddr + ch * 16, u);
+                        if (j > 0) ptx::tmem_ld_x16(tsum + ch * 16, acc);
+                        ptx::tmem_ld_wait();
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const float part = __uint_as_float((uint32_t)bf16_bits(__uint_as_float(u[jj])) << 16);
+                            acc[jj] = __float_as_uint(j > 0 ? __uint_as_float(acc[jj]) + part : part);
+                        }
+                        if (!last) {
+                            ptx::tmem_st_x16(tsum + ch * 16, acc);
+                        } else {
+                            const int r0 = tl.rt * kPairRows + ch * 16;
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj)
+                                if (r0 + jj < rows)
+                                    args.latent[(size_t)(r0 + jj) * kLatent + ncol] =
+                                        bf16_bits(__uint_as_float(acc[jj]));
+                        }
+                    }
+                    if (!last) ptx::tmem_st_wait();  // the next slice reads these sums back
+                }
+                // all 128 epilogue threads are done with this accumulator: one
+                // arrival from this CTA on the leader's barrier
+                ptx::tc_fence_before();
+                ptx::named_bar_sync(2, 128);
+                if (threadIdx.x == 64) {
+                    if (leader)
+                        ptx::mbar_arrive(accempty_bar(buf));
+                    else
+                        ptx::mbar_arrive_remote(ptx::map_to_rank(accempty_bar(buf), 0u));
+                }
             }
         }
     }

@@ -555,8 +555,10 @@ route_status route_set_overlap(route_plan *plan, int enable) {
 route_status route_set_latent_ksplit(route_plan *plan, int enable) {
     route_status st = check_plan(plan);
     if (st != ROUTE_OK) return st;
-    if (plan->mode != ROUTE_DECODE)
-        return fail(ROUTE_ERR_MODE, "the K-split latent is available for decode plans only");
+    if (plan->mode == ROUTE_PREFILL) {  // K slices of 14 k-blocks split every prefill tile evenly
+        plan->pre.ksplit = enable ? 1 : 0;
+        return ROUTE_OK;
+    }
     if (enable) {
         // every CTA that touches a latent tile must own exactly one K slice of it
         constexpr int kSlice = kKBlocks / kKSplitSlices;  // 14 k-blocks = 896 of K

@@ -62,8 +62,30 @@ def test_ksplit_latent_matches_the_general_path(workload, rows):
     assert _rel_rms(got[0], y64) > _rel_rms(full[0], y64)
 
 
-def test_ksplit_is_refused_for_prefill():
-    with route.Plan(route.PREFILL, 40) as plan:
-        with pytest.raises(route.RouteError) as err:
-            route.route_set_latent_ksplit(plan, True)
-        assert err.value.status == 2  # ROUTE_ERR_MODE
+def _check_ksplit(got_bits, h_bits, wl):
+    ref = oracle.latent_ksplit(h_bits, wl, SLICES)
+    sl = h_bits.shape[1] // SLICES
+    parts = np.stack([oracle.dot64(h_bits[:, s * sl:(s + 1) * sl], wl[s * sl:(s + 1) * sl])
+                      for s in range(SLICES)])
+    g, r = bf16_vals(got_bits), bf16_vals(ref)
+    miss = g != r
+    bound = ulp_bf16(np.abs(parts)).max(axis=0) + ulp_bf16(np.abs(r))
+    assert miss.mean() <= 2e-3, miss.mean()
+    assert np.all(np.abs(g - r)[miss] <= bound[miss])
+
+
+@pytest.mark.parametrize("rows,sample", [(40, None), (1024, (0, 1, 2, 3, 17, 255, 256, 500, 777, 1023))])
+def test_prefill_ksplit_latent_matches_the_general_path(rows, sample):
+    hid, wl, wr = bank("prefill_r1024", 0)
+    h_bits = np.ascontiguousarray(hid[:rows])
+    h, dwl, dwr = to_dev_bf16(h_bits), to_dev_bf16(wl), to_dev_bf16(wr)
+    with route.Plan(route.PREFILL, rows) as plan:
+        full = run_step(plan, h, dwl, dwr)
+        route.route_set_latent_ksplit(plan, True)
+        got = run_step(plan, h, dwl, dwr)
+        again = run_step(plan, h, dwl, dwr)
+    for name, a, b in zip(("logits", "ids", "weights"), got[1:], full[1:]):
+        assert np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8)), name
+    assert np.array_equal(got[0], again[0])
+    idx = list(range(rows)) if sample is None else list(sample)
+    _check_ksplit(got[0][idx], np.ascontiguousarray(h_bits[idx]), wl)
