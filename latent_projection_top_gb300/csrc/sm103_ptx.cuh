@@ -280,15 +280,6 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t ran
     return out;
 }
 
-__device__ __forceinline__ float4 ld_cluster_f4(uint32_t cluster_addr) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(cluster_addr)
-                 : "memory");
-    return v;
-}
-
 // ---- named barrier over a subset of the CTA's warps ---------------------------
 
 // Non-aligned form: lanes of a warp may arrive separately (after divergent
