@@ -258,6 +258,30 @@ def test_prefill_3072_sampled_and_deterministic():
     check_topk_exact(ids, w, ids_o, w_o)
 
 
+def test_prefill_8192_rows_sampled_and_position_independent():
+    """A chunk well past the pages' largest (8192 rows, 7.6 waves of CTA-pair
+    tiles): the 3072-row bank repeated, so rows r and r + 3072 hold the same
+    hidden values and must give the same bits wherever they sit."""
+    hid, wl, wr = bank("prefill_r3072", 0)
+    big = np.ascontiguousarray(np.concatenate([hid, hid, hid[:2048]]))
+    rows = big.shape[0]
+    base = (0, 255, 1000, 2047, 3071)
+    ref = oracle_rows("prefill_r3072", 0, base)
+    with route.Plan(route.PREFILL, rows) as plan:
+        lat, lg, ids, w = run_step(plan, to_dev_bf16(big), to_dev_bf16(wl), to_dev_bf16(wr))
+    for off in (0, 3072, 6144):
+        sel = [b + off for b in base if b + off < rows]
+        k = len(sel)
+        check_latent(lat[sel], ref["latent"][:k], ref["y_lat"][:k], ref["abs_lat"][:k])
+        check_logits(lg[sel], ref["y_log"][:k], ref["abs_log"][:k])
+    for r in (0, 1000, 2047):
+        for off in (3072, 6144):
+            assert np.array_equal(lat[r], lat[r + off]) and np.array_equal(
+                lg[r].view(np.uint32), lg[r + off].view(np.uint32))
+    ids_o, w_o = oracle.topk(lg[:64])
+    check_topk_exact(ids[:64], w[:64], ids_o, w_o)
+
+
 # ------------------------------------------------------- host entry / errors
 
 def test_route_step_host_matches_device():
