@@ -27,7 +27,7 @@
 //   warp 1      TMEM owner (both CTAs); the leader's lane 0 issues the MMAs
 //               and re-arms each stage's barrier once it has consumed it
 //   warps 2..5  epilogue (both CTAs): TMEM -> registers -> global
-// Pairs walk the (column tile, row tile) grid with stride = number of pairs;
+// Pairs walk the (row tile, column tile) grid with stride = number of pairs;
 // two TMEM accumulators let one tile's epilogue overlap the next main loop.
 //
 // Programmatic dependent launch: weight boxes of the first stages are
@@ -90,9 +90,12 @@ __device__ __forceinline__ int tiles_of_pair(const ProjArgs &a, int pair, int np
     return pair < tiles ? (tiles - 1 - pair) / npairs + 1 : 0;
 }
 
+// Tiles in row-major order: the pairs at work at one time share a few
+// 256-row blocks of hidden and read every weight tile (measured 117 us
+// against 128 us at 3072 rows for column-major order).
 __device__ __forceinline__ Tile tile_get(const ProjArgs &a, int pair, int npairs, int i) {
     const int t = pair + i * npairs;
-    return Tile{t / a.row_tiles, t % a.row_tiles};
+    return Tile{t % kPairColTiles, t / kPairColTiles};
 }
 
 // Bounded wait for the completion of phase `parity` of `bar` (acquire at
