@@ -85,6 +85,10 @@ def test_calls_with_null_plan(lib):
     assert lib.topk16_select(null, x, x, x, None) == 3
     assert lib.route_step(null, x, x, x, x, x, x, x, None) == 3
     assert lib.route_step_host(null, x, x, x, x, x, x, x, None) == 3
+    assert lib.route_step_sumsq(null, x, x, x, x, x, x, x, x, None) == 3
+    assert lib.route_set_overlap(null, 1) == 3
+    assert lib.route_set_latent_ksplit(null, 1) == 3
+    assert lib.route_test_stall(null, 1, 0) == 3
     assert lib.route_device_status(null) == 3
     assert lib.route_destroy(null) == 0
     for f in ("route_plan_rows", "route_plan_mode", "route_plan_grid", "route_plan_segments"):
