@@ -151,8 +151,10 @@ route_status route_step_sumsq(const route_plan *plan, const void *hidden, const 
  * Weights stay device pointers (they are resident model parameters).  The
  * copies use the plan's device staging buffers (allocated by route_prepare)
  * and are enqueued on `stream`; the call returns after the stream has
- * finished (it synchronises `stream`).  Host pointers need no alignment;
- * page-locked host memory makes the copies faster.
+ * finished (it synchronises `stream`).  Host pointers need no alignment.
+ * Decode plans with every host buffer page-locked and 16-byte aligned skip the
+ * copies: a staging kernel reads `hidden_host` through its mapped address and
+ * the kernels write the results straight into the host buffers.
  */
 route_status route_step_host(const route_plan *plan, const void *hidden_host,
                              const void *W_latent, const void *W_router, void *latent_host,

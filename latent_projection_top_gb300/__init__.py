@@ -11,8 +11,11 @@ The route step of one MoE layer (see ``include/route.h``):
 * ``latent_router_forward`` -- latent down projection (BF16, one FP32 full-K
   sum rounded once) and FP32 router logits;
 * ``topk16_select`` -- standalone top-16 with sigmoid-renormalised weights;
-* ``route_step`` -- both, as one kernel for decode plans;
-* ``route_step_host`` -- ``route_step`` with host tensors (copies included).
+* ``route_step`` -- both (for decode plans, a weight-stream kernel and a kernel
+  that finishes the split-K sums and runs the top-16);
+* ``route_step_sumsq`` -- ``route_step`` plus each latent row's sum of squares;
+* ``route_step_host`` -- ``route_step`` with host tensors (transfers included);
+* ``route_set_overlap``, ``route_set_latent_ksplit`` -- plan options.
 """
 
 from __future__ import annotations
@@ -164,6 +167,13 @@ def _torch():
 
 
 def _dev_tensor(t, name, shape, dtypes, device):
+    # the common case in one expression (this runs on every call)
+    try:
+        if (t.is_cuda and t.get_device() == device and t.dtype in dtypes and t.shape == shape
+                and t.is_contiguous()):
+            return ctypes.c_void_p(t.data_ptr())
+    except AttributeError:
+        pass
     torch = _torch()
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
@@ -173,26 +183,33 @@ def _dev_tensor(t, name, shape, dtypes, device):
         raise TypeError(f"{name} has dtype {t.dtype}; expected one of {dtypes}")
     if tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} has shape {tuple(t.shape)}; expected {tuple(shape)}")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
-    return ctypes.c_void_p(t.data_ptr())
+    raise ValueError(f"{name} must be contiguous")
 
 
 def _host_tensor(t, name, shape, dtypes):
+    try:
+        if t.is_cpu and t.dtype in dtypes and t.shape == shape and t.is_contiguous():
+            return ctypes.c_void_p(t.data_ptr())
+    except AttributeError:
+        pass
     torch = _torch()
     if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
         raise TypeError(f"{name} must be a CPU torch.Tensor")
     if t.dtype not in dtypes:
         raise TypeError(f"{name} has dtype {t.dtype}; expected one of {dtypes}")
-    if tuple(t.shape) != tuple(shape) or not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous with shape {tuple(shape)}")
-    return ctypes.c_void_p(t.data_ptr())
+    raise ValueError(f"{name} must be contiguous with shape {tuple(shape)}")
+
+
+_BF16_TYPES = None
 
 
 def _bf16_types():
-    torch = _torch()
-    return (torch.bfloat16, torch.int16, torch.uint16) if hasattr(torch, "uint16") else \
-        (torch.bfloat16, torch.int16)
+    global _BF16_TYPES
+    if _BF16_TYPES is None:
+        torch = _torch()
+        _BF16_TYPES = (torch.bfloat16, torch.int16, torch.uint16) if hasattr(torch, "uint16") \
+            else (torch.bfloat16, torch.int16)
+    return _BF16_TYPES
 
 
 def _stream(stream, device):

@@ -18,8 +18,9 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libroute.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-SOURCES = ["decode_kernel.cu", "prefill_kernel.cu", "topk_kernel.cu", "route_api.cu"]
-HEADERS = ["common.cuh", "sm103_ptx.cuh", "topk16.cuh"]
+SOURCES = ["decode_kernel.cu", "prefill_kernel.cu", "topk_kernel.cu", "stage_kernel.cu",
+           "route_api.cu"]
+HEADERS = ["common.cuh", "sm103_ptx.cuh", "topk16.cuh", "twofloat.cuh"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

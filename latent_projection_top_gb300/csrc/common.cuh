@@ -99,6 +99,11 @@ cudaError_t decode_launch(int bn, const CUtensorMap &map_h, const CUtensorMap &m
                           const CUtensorMap &map_wr, const DecodeArgs &args, int do_topk,
                           cudaStream_t stream);
 
+// Copy `bytes` (a multiple of 16) from page-locked host memory, through its
+// device-mapped address, into device memory; PDL-chained like the route
+// kernels.
+cudaError_t stage_in_launch(const void *src_mapped, void *dst, size_t bytes, cudaStream_t stream);
+
 // The top-16 of each row; with `sumsq` non-null also the row's latent sum
 // of squares (read from `latent`, which the same predecessor wrote).
 cudaError_t topk_launch(const float *logits, int rows, int32_t *ids, float *weights,

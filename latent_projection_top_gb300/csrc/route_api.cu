@@ -29,6 +29,14 @@ struct route_plan {
     unsigned *words;          // device status word (+ spare)
     uint8_t *staging;         // device staging for route_step_host
     size_t staging_bytes;
+    // The last tensor map made for each operand (a map describes an address
+    // and a shape; the shapes are fixed per plan, so an equal address reuses
+    // it and skips the encode on the next call).
+    struct MapCache {
+        const void *ptr = nullptr;
+        CUtensorMap map;
+    };
+    mutable MapCache map_h, map_wl, map_wr;
 };
 
 namespace {
@@ -151,24 +159,40 @@ route_status check_plan(const route_plan *p) {
     return ROUTE_OK;
 }
 
+route_status cached_map(route_plan::MapCache &c, const void *ptr, uint64_t inner, uint64_t outer,
+                        uint32_t box_inner, uint32_t box_outer, const char *what, CUtensorMap *out) {
+    if (c.ptr != ptr) {
+        route_status st = encode_2d(&c.map, ptr, inner, outer, box_inner, box_outer, what);
+        if (st != ROUTE_OK) {
+            c.ptr = nullptr;
+            return st;
+        }
+        c.ptr = ptr;
+    }
+    *out = c.map;
+    return ROUTE_OK;
+}
+
 route_status encode_all(const route_plan *p, const void *hidden, const void *W_latent,
                         const void *W_router, CUtensorMap *mh, CUtensorMap *ml, CUtensorMap *mr) {
     route_status st;
     // decode: one box holds the step's rows; prefill: each CTA of a pair
     // loads half of a tile's token rows
     const uint32_t hbox = p->mode == ROUTE_DECODE ? (uint32_t)p->bn : (uint32_t)kPrefillHiddenBoxRows;
-    if ((st = encode_2d(mh, hidden, kHidden, (uint64_t)p->rows, kKBlock, hbox, "hidden")) !=
+    if ((st = cached_map(p->map_h, hidden, kHidden, (uint64_t)p->rows, kKBlock, hbox, "hidden",
+                         mh)) != ROUTE_OK)
+        return st;
+    if ((st = cached_map(p->map_wl, W_latent, kLatent, kHidden, 64, kKBlock, "W_latent", ml)) !=
         ROUTE_OK)
         return st;
-    if ((st = encode_2d(ml, W_latent, kLatent, kHidden, 64, kKBlock, "W_latent")) != ROUTE_OK)
-        return st;
-    return encode_2d(mr, W_router, kExperts, kHidden, 64, kKBlock, "W_router");
+    return cached_map(p->map_wr, W_router, kExperts, kHidden, 64, kKBlock, "W_router", mr);
 }
 
 // The projection (and, for decode with do_topk, the top-16) of one step.
 route_status launch_forward(const route_plan *p, const void *hidden, const void *W_latent,
                             const void *W_router, void *latent, float *logits, int32_t *ids,
-                            float *weights, int do_topk, float *sumsq, cudaStream_t stream) {
+                            float *weights, int do_topk, float *sumsq, cudaStream_t stream,
+                            bool no_overlap = false) {
     CUtensorMap mh, ml, mr;
     route_status st = encode_all(p, hidden, W_latent, W_router, &mh, &ml, &mr);
     if (st != ROUTE_OK) return st;
@@ -180,6 +204,7 @@ route_status launch_forward(const route_plan *p, const void *hidden, const void 
         a.ids = ids;
         a.weights = weights;
         a.sumsq = sumsq;
+        if (no_overlap) a.overlap = 0;
         e = decode_launch(p->bn, mh, ml, mr, a, do_topk, stream);
         if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
     } else {
@@ -491,6 +516,18 @@ route_status route_step_sumsq(const route_plan *plan, const void *hidden, const 
                     static_cast<cudaStream_t>(stream), latent_sumsq);
 }
 
+// Device-mapped address of page-locked host memory, or nullptr for memory the
+// GPU cannot reach directly (pageable memory takes the copy path).
+void *mapped_host(const void *p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();  // clear the sticky-free error of an unknown pointer
+        return nullptr;
+    }
+    if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr) return nullptr;
+    return a.devicePointer;
+}
+
 route_status route_step_host(const route_plan *plan, const void *hidden_host,
                              const void *W_latent, const void *W_router, void *latent_host,
                              float *logits_host, int32_t *ids_host, float *weights_host,
@@ -508,6 +545,27 @@ route_status route_step_host(const route_plan *plan, const void *hidden_host,
     const Staging d = staging_of(plan);
     const size_t r = (size_t)plan->rows;
     cudaError_t e;
+    if (plan->mode == ROUTE_DECODE) {
+        // Page-locked host buffers: a staging kernel reads the hidden rows
+        // through the mapped address and the finish kernel writes the results
+        // straight into the caller's buffers -- no copies to wait for.
+        void *h = mapped_host(hidden_host), *lat = mapped_host(latent_host),
+             *lg = mapped_host(logits_host), *ids = mapped_host(ids_host),
+             *w = mapped_host(weights_host);
+        if (h && lat && lg && ids && w && aligned16(h) && aligned16(lat) && aligned16(lg) &&
+            aligned16(ids) && aligned16(w)) {
+            if ((e = stage_in_launch(h, d.hidden, r * kHidden * 2, s)) != cudaSuccess)
+                return cuda_fail(e, "stage hidden rows");
+            // no overlap: the staging kernel releases its successor early
+            if ((st = launch_forward(plan, d.hidden, W_latent, W_router, lat,
+                                     static_cast<float *>(lg), static_cast<int32_t *>(ids),
+                                     static_cast<float *>(w), 1, nullptr, s, true)) != ROUTE_OK)
+                return st;
+            if ((e = cudaStreamSynchronize(s)) != cudaSuccess)
+                return cuda_fail(e, "cudaStreamSynchronize");
+            return ROUTE_OK;
+        }
+    }
     if ((e = cudaMemcpyAsync(d.hidden, hidden_host, r * kHidden * 2, cudaMemcpyHostToDevice, s)) !=
         cudaSuccess)
         return cuda_fail(e, "copy hidden to device");

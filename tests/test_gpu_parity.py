@@ -284,18 +284,25 @@ def test_prefill_8192_rows_sampled_and_position_independent():
 
 # ------------------------------------------------------- host entry / errors
 
-def test_route_step_host_matches_device():
-    hid, wl, wr = bank("decode_r8", 0)
-    rows = 8
+@pytest.mark.parametrize("mode,rows", [(route.DECODE, 8), (route.DECODE, 20), (route.PREFILL, 40)])
+@pytest.mark.parametrize("pinned", [True, False])
+def test_route_step_host_matches_device(mode, rows, pinned):
+    """Page-locked buffers take the direct path for decode (staging kernel in,
+    results written straight to host memory); pageable ones the copy path."""
+    hid, wl, wr = bank("decode_r8" if mode == route.DECODE else "prefill_r1024", 0)
+    hid = np.ascontiguousarray(np.resize(hid, (rows, hid.shape[1])))
     dwl, dwr = to_dev_bf16(wl), to_dev_bf16(wr)
-    with route.Plan(route.DECODE, rows) as plan:
-        dev = run_step(plan, to_dev_bf16(hid[:rows]), dwl, dwr)
-        h_host = torch.from_numpy(hid[:rows].view(np.int16).copy()).view(torch.bfloat16).pin_memory()
-        lat = torch.empty((rows, route.N_LATENT), dtype=torch.bfloat16).pin_memory()
-        lg = torch.empty((rows, route.N_EXPERTS), dtype=torch.float32).pin_memory()
-        ids = torch.empty((rows, route.TOPK), dtype=torch.int32).pin_memory()
-        w = torch.empty((rows, route.TOPK), dtype=torch.float32).pin_memory()
-        route.route_step_host(plan, h_host, dwl, dwr, lat, lg, ids, w)
+    pin = (lambda t: t.pin_memory()) if pinned else (lambda t: t)
+    with route.Plan(mode, rows) as plan:
+        dev = run_step(plan, to_dev_bf16(hid), dwl, dwr)
+        h_host = pin(torch.from_numpy(hid.view(np.int16).copy()).view(torch.bfloat16))
+        lat = pin(torch.full((rows, route.N_LATENT), float("nan"), dtype=torch.bfloat16))
+        lg = pin(torch.full((rows, route.N_EXPERTS), float("nan"), dtype=torch.float32))
+        ids = pin(torch.full((rows, route.TOPK), -1, dtype=torch.int32))
+        w = pin(torch.full((rows, route.TOPK), float("nan"), dtype=torch.float32))
+        for _ in range(2):  # twice: the staging buffer is reused
+            route.route_step_host(plan, h_host, dwl, dwr, lat, lg, ids, w)
+        route.route_device_status(plan)
     assert np.array_equal(lat.view(torch.int16).numpy().view(np.uint16), dev[0])
     assert np.array_equal(lg.numpy().view(np.uint32), dev[1].view(np.uint32))
     assert np.array_equal(ids.numpy(), dev[2])
