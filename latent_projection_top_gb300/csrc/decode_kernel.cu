@@ -17,18 +17,20 @@
 //   rows, zero-filled past `rows`) into a 4-stage shared-memory ring; one
 //   thread issues tcgen05 MMAs (128 weight columns on M, token rows on N) into
 //   a fresh TMEM accumulator per k-block; eight epilogue warps add each
-//   k-block's FP32 result into a two-float (TwoSum) running sum, so the only
-//   rounding left is the tensor core's inside one 64-long block.  A CTA's run
-//   covers at most two tiles; the first run's partial waits in shared memory
-//   and both are stored to their scratch slots when the CTA's stream ends.
+//   k-block's FP32 result into a two-float (TwoSum) running sum kept in TMEM
+//   next to the accumulators, so the only rounding left is the tensor core's
+//   inside one 64-long block.  A CTA's run covers at most two tiles; the
+//   first run's partial waits in shared memory and both are stored to their
+//   scratch slots when the CTA's stream ends.
 //
 // decode_finish_kernel -- at most one small CTA per SM, so that it fits next
 //   to a stream CTA: one CTA per row sums the row's 896 router logits and
-//   runs the top-16 on them from shared memory; the others sum the latent
-//   tiles, two (row, tile) items at a time.  Slots are summed in segment
-//   order as two-floats and rounded once, so results are bitwise reproducible
-//   and a row's bits do not depend on the row count (the partition depends
-//   only on the grid).
+//   runs the top-16 on them with all its threads; the others sum the latent
+//   tiles, two (row, tile) items at a time (and, when asked, each latent
+//   row's sum of squares, or the general path's K-split latent).  Slots are
+//   summed in segment order as two-floats and rounded once, so results are
+//   bitwise reproducible and a row's bits do not depend on the row count
+//   (the partition depends only on the grid).
 //
 // Programmatic dependent launch: both kernels let their successor launch at
 // once.  The stream kernel prefetches its first weight boxes (model

@@ -30,6 +30,11 @@
 // Pairs walk the (row tile, column tile) grid with stride = number of pairs;
 // two TMEM accumulators let one tile's epilogue overlap the next main loop.
 //
+// With the general path's K-split latent (args.ksplit), a latent tile runs as
+// eight jobs of 14 k-blocks into one accumulator; the epilogue rounds each
+// slice's partial to BF16 and adds it in FP32 to a running sum kept in the
+// other half of TMEM, rounding and storing after the eighth.
+//
 // Programmatic dependent launch: weight boxes of the first stages are
 // requested before `griddepcontrol.wait` (no predecessor writes the weights);
 // hidden rows are read and outputs written only after it.

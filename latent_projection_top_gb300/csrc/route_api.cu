@@ -521,7 +521,7 @@ route_status route_step_sumsq(const route_plan *plan, const void *hidden, const 
 void *mapped_host(const void *p) {
     cudaPointerAttributes a;
     if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
-        cudaGetLastError();  // clear the sticky-free error of an unknown pointer
+        cudaGetLastError();  // clear the (non-sticky) error this query left
         return nullptr;
     }
     if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr) return nullptr;
