@@ -248,6 +248,10 @@ __global__ void __maxnreg__(BN == 16 ? 72 : 80)
             uint32_t armed = 0u, armed_par = 0u;
             // Weight boxes of the first stages go out before the grid
             // dependency resolves (no predecessor writes the weights).
+            if (args.hold_ns != 0u) {  // see kPrefetchHoldNs
+                const uint64_t t0 = ptx::global_timer_ns();
+                while (ptx::global_timer_ns() - t0 < args.hold_ns) __nanosleep(64);
+            }
             for (int i = 0; i < n_pre; ++i) {
                 ptx::mbar_arrive_expect_tx(full_bar(i), C::kStageBytes);
                 weights_of(u0 + i, sbase + i * C::kStageBytes, full_bar(i));
@@ -377,17 +381,37 @@ __global__ void __maxnreg__(BN == 16 ? 72 : 80)
 constexpr int kFinishBatch = 10;
 constexpr int kSlotF4 = kDecodeMaxRows * kDTileCols / 2;  // float4 (two columns) per slot
 
+// Where the partials of one (row, column pair) sit: the first slot's float4
+// and the slot count.  Built from the launch parameters before the grid
+// dependency resolves, so that the sums start with the slot loads.
+struct SlotRun {
+    const float4 *p;
+    int n;
+};
+
+__device__ __forceinline__ SlotRun slot_run(const DecodeArgs &a, int r, int t, int cc) {
+    SlotRun s;
+    s.p = reinterpret_cast<const float4 *>(a.ws) +
+          ((size_t)a.seg_base[t] * kDecodeMaxRows + r) * (kDTileCols / 2) + cc / 2;
+    s.n = a.seg_count[t];
+    return s;
+}
+
+// Keeps `s` computed here: an empty volatile asm is not moved across the
+// volatile `griddepcontrol.wait` that follows it.
+__device__ __forceinline__ void pin(SlotRun &s) {
+    asm volatile("" : "+l"(s.p), "+r"(s.n));
+}
+
 template <int NP>
-__device__ __forceinline__ void sum_slot_pairs(const DecodeArgs &a, int r, const int (&t)[NP],
-                                               const int (&cc)[NP], float2 (&y)[NP]) {
+__device__ __forceinline__ void sum_slot_pairs(const SlotRun (&run)[NP], float2 (&y)[NP]) {
     const float4 *p[NP];
     int n[NP], nmax = 0;
     float h[2 * NP], l[2 * NP];
 #pragma unroll
     for (int q = 0; q < NP; ++q) {
-        p[q] = reinterpret_cast<const float4 *>(a.ws) +
-               ((size_t)a.seg_base[t[q]] * kDecodeMaxRows + r) * (kDTileCols / 2) + cc[q] / 2;
-        n[q] = a.seg_count[t[q]];
+        p[q] = run[q].p;
+        n[q] = run[q].n;
         nmax = n[q] > nmax ? n[q] : nmax;
         h[2 * q] = h[2 * q + 1] = l[2 * q] = l[2 * q + 1] = 0.f;
     }
@@ -423,10 +447,9 @@ __device__ __forceinline__ void sum_slot_pairs(const DecodeArgs &a, int r, const
 // (checked on the host), slot j of a latent tile is slice j: each slot's
 // two-float partial is rounded to FP32 and then to BF16, and the BF16 values
 // are added in FP32 in slice order; the caller rounds the sum to BF16.
-__device__ __forceinline__ float2 ksplit_slot_pair(const DecodeArgs &a, int r, int t, int cc) {
-    const float4 *p = reinterpret_cast<const float4 *>(a.ws) +
-                      ((size_t)a.seg_base[t] * kDecodeMaxRows + r) * (kDTileCols / 2) + cc / 2;
-    const int n = a.seg_count[t];
+__device__ __forceinline__ float2 ksplit_slot_pair(const SlotRun &run) {
+    const float4 *p = run.p;
+    const int n = run.n;
     float4 v[kFinishBatch];
 #pragma unroll
     for (int j = 0; j < kFinishBatch; ++j)
@@ -519,7 +542,6 @@ __global__ void __maxnreg__(112) decode_finish_kernel(const __grid_constant__ De
     __shared__ TopkBlockSmem s_topk;
     __shared__ float2 s_ss[2][2][kLatentThreads / 32];  // [iteration parity][half][warp]
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");  // the stream kernel's partials are complete
     const int rows = a.rows;
     const int tid = threadIdx.x;
     const int b = blockIdx.x;
@@ -527,10 +549,13 @@ __global__ void __maxnreg__(112) decode_finish_kernel(const __grid_constant__ De
         if (tid >= kRouterThreads) return;  // the named barriers below count only router threads
         const int r = b;
         const int c0 = 2 * tid, c1 = c0 + kExperts / 2;  // columns c0, c0+1 and c1, c1+1
-        const int t[2] = {kDLatTiles + c0 / kDTileCols, kDLatTiles + c1 / kDTileCols};
-        const int cc[2] = {c0 % kDTileCols, c1 % kDTileCols};
+        SlotRun run[2] = {slot_run(a, r, kDLatTiles + c0 / kDTileCols, c0 % kDTileCols),
+                          slot_run(a, r, kDLatTiles + c1 / kDTileCols, c1 % kDTileCols)};
+        pin(run[0]);
+        pin(run[1]);
+        asm volatile("griddepcontrol.wait;" ::: "memory");  // the stream kernel's partials are complete
         float2 y[2];
-        sum_slot_pairs<2>(a, r, t, cc, y);
+        sum_slot_pairs<2>(run, y);
         float *lrow = a.logits + (size_t)r * kExperts;
         *reinterpret_cast<float2 *>(lrow + c0) = y[0];
         *reinterpret_cast<float2 *>(lrow + c1) = y[1];
@@ -545,20 +570,25 @@ __global__ void __maxnreg__(112) decode_finish_kernel(const __grid_constant__ De
         const int n_items = kDLatTiles * rows;
         const int stride = 2 * ((int)gridDim.x - rows);
         const int half = tid / kLatentThreads;
-        int parity = 0;
-        for (int i = 2 * (b - rows) + half; i < n_items; i += stride, parity ^= 1) {
-            const int r = i / kDLatTiles;
-            const int t[1] = {i % kDLatTiles}, cc[1] = {2 * (tid % kLatentThreads)};
+        const int cc = 2 * (tid % kLatentThreads);
+        const int i0 = 2 * (b - rows) + half;
+        SlotRun run[1] = {i0 < n_items ? slot_run(a, i0 / kDLatTiles, i0 % kDLatTiles, cc)
+                                       : SlotRun{nullptr, 0}};
+        pin(run[0]);
+        asm volatile("griddepcontrol.wait;" ::: "memory");  // the stream kernel's partials are complete
+        for (int i = i0, parity = 0; i < n_items; i += stride, parity ^= 1) {
+            const int r = i / kDLatTiles, t = i % kDLatTiles;
+            if (i != i0) run[0] = slot_run(a, r, t, cc);
             float2 y[1];
             if (a.ksplit)
-                y[0] = ksplit_slot_pair(a, r, t[0], cc[0]);
+                y[0] = ksplit_slot_pair(run[0]);
             else
-                sum_slot_pairs<1>(a, r, t, cc, y);
+                sum_slot_pairs<1>(run, y);
             const uint16_t b0 = bf16_bits(y[0].x), b1 = bf16_bits(y[0].y);
-            *reinterpret_cast<uint32_t *>(a.latent + (size_t)r * kLatent + t[0] * kDTileCols + cc[0]) =
+            *reinterpret_cast<uint32_t *>(a.latent + (size_t)r * kLatent + t * kDTileCols + cc) =
                 (uint32_t)b0 | ((uint32_t)b1 << 16);
             if (a.sumsq != nullptr)
-                latent_sumsq_part(a, r, t[0], b0, b1, half, tid % kLatentThreads, s_ss[parity][half]);
+                latent_sumsq_part(a, r, t, b0, b1, half, tid % kLatentThreads, s_ss[parity][half]);
         }
     }
 }

@@ -192,7 +192,7 @@ route_status encode_all(const route_plan *p, const void *hidden, const void *W_l
 route_status launch_forward(const route_plan *p, const void *hidden, const void *W_latent,
                             const void *W_router, void *latent, float *logits, int32_t *ids,
                             float *weights, int do_topk, float *sumsq, cudaStream_t stream,
-                            bool no_overlap = false) {
+                            bool after_staging = false) {
     CUtensorMap mh, ml, mr;
     route_status st = encode_all(p, hidden, W_latent, W_router, &mh, &ml, &mr);
     if (st != ROUTE_OK) return st;
@@ -204,7 +204,8 @@ route_status launch_forward(const route_plan *p, const void *hidden, const void 
         a.ids = ids;
         a.weights = weights;
         a.sumsq = sumsq;
-        if (no_overlap) a.overlap = 0;
+        if (after_staging) a.overlap = 0;  // hidden is the staging kernel's output
+        a.hold_ns = a.overlap || after_staging ? 0u : kPrefetchHoldNs;
         e = decode_launch(p->bn, mh, ml, mr, a, do_topk, stream);
         if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
     } else {
@@ -352,6 +353,7 @@ route_status noalloc_setup(int device, NoAllocDevice **out) {
                     kNoAllocMaxSlots);
     d.scratch = static_cast<unsigned char *>(ptr);
     d.base.timeout_ns = kDefaultTimeoutNs;
+    d.base.hold_ns = kPrefetchHoldNs;  // no overlap here
     d.base.words = reinterpret_cast<unsigned *>(d.scratch);
     d.base.ws = reinterpret_cast<float2 *>(d.scratch + kNoAllocWordBytes);
     d.ready = true;
@@ -556,7 +558,7 @@ route_status route_step_host(const route_plan *plan, const void *hidden_host,
             aligned16(ids) && aligned16(w)) {
             if ((e = stage_in_launch(h, d.hidden, r * kHidden * 2, s)) != cudaSuccess)
                 return cuda_fail(e, "stage hidden rows");
-            // no overlap: the staging kernel releases its successor early
+            // after the staging kernel: no overlap, no hold
             if ((st = launch_forward(plan, d.hidden, W_latent, W_router, lat,
                                      static_cast<float *>(lg), static_cast<int32_t *>(ids),
                                      static_cast<float *>(w), 1, nullptr, s, true)) != ROUTE_OK)
