@@ -15,6 +15,7 @@ The route step of one MoE layer (see ``include/route.h``):
   that finishes the split-K sums and runs the top-16);
 * ``route_step_sumsq`` -- ``route_step`` plus each latent row's sum of squares;
 * ``route_step_host`` -- ``route_step`` with host tensors (transfers included);
+  ``HostStep`` -- the same on fixed buffers, checked once, for serving loops;
 * ``route_set_overlap``, ``route_set_latent_ksplit`` -- plan options.
 """
 
@@ -140,6 +141,9 @@ class Plan:
     def close(self) -> None:
         if self._h is not None and self._h.value:
             lib().route_destroy(self._h)
+            # a HostStep made on this plan shares the handle object: it now
+            # passes NULL and gets ROUTE_ERR_NULL instead of a freed plan
+            self._h.value = None
         self._h = None
 
     def __enter__(self):
@@ -269,19 +273,50 @@ def route_step_sumsq(plan: Plan, hidden, W_latent, W_router, latent, logits, ids
     _check(lib().route_step_sumsq(plan.handle, *p, i, w, ss, _stream(stream, plan.device)))
 
 
-def route_step_host(plan: Plan, hidden_host, W_latent, W_router, latent_host, logits_host,
-                    ids_host, weights_host, stream=None) -> None:
+def _host_step_args(plan, hidden_host, W_latent, W_router, latent_host, logits_host, ids_host,
+                    weights_host):
     torch = _torch()
     R, d = plan.rows, plan.device
     bf = _bf16_types()
-    args = (_host_tensor(hidden_host, "hidden_host", (R, K_HIDDEN), bf),
+    return (_host_tensor(hidden_host, "hidden_host", (R, K_HIDDEN), bf),
             _dev_tensor(W_latent, "W_latent", (K_HIDDEN, N_LATENT), bf, d),
             _dev_tensor(W_router, "W_router", (K_HIDDEN, N_EXPERTS), bf, d),
             _host_tensor(latent_host, "latent_host", (R, N_LATENT), bf),
             _host_tensor(logits_host, "logits_host", (R, N_EXPERTS), (torch.float32,)),
             _host_tensor(ids_host, "ids_host", (R, TOPK), (torch.int32,)),
             _host_tensor(weights_host, "weights_host", (R, TOPK), (torch.float32,)))
-    _check(lib().route_step_host(plan.handle, *args, _stream(stream, d)))
+
+
+def route_step_host(plan: Plan, hidden_host, W_latent, W_router, latent_host, logits_host,
+                    ids_host, weights_host, stream=None) -> None:
+    args = _host_step_args(plan, hidden_host, W_latent, W_router, latent_host, logits_host,
+                           ids_host, weights_host)
+    _check(lib().route_step_host(plan.handle, *args, _stream(stream, plan.device)))
+
+
+class HostStep:
+    """``route_step_host`` on fixed buffers, checked once.
+
+    For a serving loop that refills the same page-locked ``hidden_host`` and
+    reads the same result buffers every step: the tensors are validated and
+    their pointers marshalled here, so each call goes straight to the C entry
+    point (the checks cost about 5 us a call otherwise).  The object keeps
+    references to the tensors and the plan; the caller must not resize them.
+    """
+
+    def __init__(self, plan: Plan, hidden_host, W_latent, W_router, latent_host, logits_host,
+                 ids_host, weights_host, stream=None):
+        self._keep = (plan, hidden_host, W_latent, W_router, latent_host, logits_host, ids_host,
+                      weights_host, stream)
+        self._args = (plan.handle,) + _host_step_args(
+            plan, hidden_host, W_latent, W_router, latent_host, logits_host, ids_host,
+            weights_host) + (_stream(stream, plan.device),)
+        self._fn = lib().route_step_host
+
+    def __call__(self) -> None:
+        st = self._fn(*self._args)
+        if st != ROUTE_OK:
+            _check(st)
 
 
 def route_set_overlap(plan: Plan, enable: bool) -> None:

@@ -309,6 +309,35 @@ def test_route_step_host_matches_device(mode, rows, pinned):
     assert np.array_equal(w.numpy().view(np.uint32), dev[3].view(np.uint32))
 
 
+def test_host_step_reuses_buffers():
+    """HostStep: checked once, then each call runs route_step_host on the same
+    buffers -- new hidden rows written into hidden_host give that step's
+    results; once the plan is closed a call is refused, not run."""
+    rows = 8
+    _, wl, wr = bank("decode_r8", 0)
+    dwl, dwr = to_dev_bf16(wl), to_dev_bf16(wr)
+    h0 = bank("decode_r8", 0)[0][:rows]
+    h1 = bank("decode_r8", 1)[0][:rows]
+    with route.Plan(route.DECODE, rows) as plan:
+        want = [run_step(plan, to_dev_bf16(h), dwl, dwr) for h in (h0, h1)]
+        h_host = torch.empty((rows, route.K_HIDDEN), dtype=torch.bfloat16).pin_memory()
+        lat = torch.empty((rows, route.N_LATENT), dtype=torch.bfloat16).pin_memory()
+        lg = torch.empty((rows, route.N_EXPERTS), dtype=torch.float32).pin_memory()
+        ids = torch.empty((rows, route.TOPK), dtype=torch.int32).pin_memory()
+        w = torch.empty((rows, route.TOPK), dtype=torch.float32).pin_memory()
+        step = route.HostStep(plan, h_host, dwl, dwr, lat, lg, ids, w)
+        for h, dev in zip((h0, h1, h0), want + want[:1]):
+            h_host.copy_(torch.from_numpy(h.view(np.int16).copy()).view(torch.bfloat16))
+            step()
+            assert np.array_equal(lat.view(torch.int16).numpy().view(np.uint16), dev[0])
+            assert np.array_equal(lg.numpy().view(np.uint32), dev[1].view(np.uint32))
+            assert np.array_equal(ids.numpy(), dev[2])
+            assert np.array_equal(w.numpy().view(np.uint32), dev[3].view(np.uint32))
+        route.route_device_status(plan)
+    with pytest.raises(route.RouteError):
+        step()
+
+
 def test_gpu_argument_errors():
     lib = route.lib()
     import ctypes
