@@ -10,16 +10,20 @@
 // decode_stream_kernel -- one CTA per SM.  The weights are cut into 18
 //   column tiles of 256 columns (14 latent, 4 router; the last router tile
 //   has 128 real columns and TMA zero-fills the rest) and 112 k-blocks of 64;
-//   CTA g owns a contiguous run of (tile, k-block) units, the same number
-//   (+-1) for every CTA.  256-column tiles put 512 contiguous bytes per weight
+//   CTA g owns a contiguous run of (tile, k-block) units, the same even
+//   number for every CTA.  256-column tiles put 512 contiguous bytes per weight
 //   row in flight, which the HBM needs to run at full speed.  Per unit a TMA
 //   producer brings four 64x64 weight boxes and the hidden box (BN = 16 or 32
 //   rows, zero-filled past `rows`) into a 4-stage shared-memory ring; one
 //   thread issues tcgen05 MMAs (128 weight columns on M, token rows on N) into
-//   a fresh TMEM accumulator per k-block; eight epilogue warps add each
-//   k-block's FP32 result into a two-float (TwoSum) running sum kept in TMEM
-//   next to the accumulators, so the only rounding left is the tensor core's
-//   inside one 64-long block.  A CTA's run covers at most two tiles; the
+//   a fresh TMEM accumulator per pair of k-blocks (runs are even and tiles
+//   start at even units, so a pair never crosses a tile); eight epilogue
+//   warps add each pair's FP32 result into a two-float (TwoSum) running sum
+//   kept in TMEM next to the accumulators, so the only rounding left is the
+//   tensor core's inside one 128-long block.  Pairing halves the epilogue's
+//   TMEM traffic, two-float work and barrier hand-offs per streamed byte,
+//   which set the pace at 17..20 rows (measured 12.6 -> 11.3 us a layer at
+//   20 rows, 10.7 -> 10.4 at 8).  A CTA's run covers at most two tiles; the
 //   first run's partial waits in shared memory and both are stored to their
 //   scratch slots when the CTA's stream ends.
 //
@@ -287,13 +291,14 @@ __global__ void __maxnreg__(BN == 16 ? 72 : 80)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            // ---------------- MMA issuer: one fresh accumulator per k-block ----------------
+            // ---------------- MMA issuer: one fresh accumulator per k-block pair ----------------
             for (int i = 0; i < n_units; ++i) {
                 const int s = i % C::kStages;
                 const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
-                const int buf = i % C::kNumAcc;
-                const uint32_t use = (uint32_t)(i / C::kNumAcc);
-                if (!wait_phase(accempty_bar(buf), (use & 1u) ^ 1u, args, &s_abort)) break;
+                const int buf = (i >> 1) % C::kNumAcc;
+                const uint32_t use = (uint32_t)((i >> 1) / C::kNumAcc);
+                if (!(i & 1) && !wait_phase(accempty_bar(buf), (use & 1u) ^ 1u, args, &s_abort))
+                    break;
                 if (!wait_phase(full_bar(s), ph, args, &s_abort)) break;
                 ptx::tc_fence_after();
                 const uint32_t a = sbase + s * C::kStageBytes;
@@ -309,11 +314,11 @@ __global__ void __maxnreg__(BN == 16 ? 72 : 80)
                         const uint64_t da =
                             smem_desc(a + blk * 2 * kBoxBytes + kk * 2048u, kBoxBytes, 1024u);
                         const uint64_t db = smem_desc(b + kk * 32u, 16u, 1024u);
-                        ptx::mma_bf16(d_tmem, da, db, C::kIdesc, kk > 0 ? 1u : 0u);
+                        ptx::mma_bf16(d_tmem, da, db, C::kIdesc, kk > 0 || (i & 1) ? 1u : 0u);
                     }
                 }
                 ptx::mma_commit(empty_bar(s));
-                ptx::mma_commit(accfull_bar(buf));
+                if (i & 1) ptx::mma_commit(accfull_bar(buf));
             }
             ptx::mma_commit(drain_bar);  // every MMA retired before TMEM is freed
             wait_drain(drain_bar, 0u, args);
@@ -329,11 +334,11 @@ __global__ void __maxnreg__(BN == 16 ? 72 : 80)
         const uint32_t sum_lo = sum_hi + BN;
         int first_slot = -1;
         bool run_start = true;
-        for (int i = 0; i < n_units; ++i) {
+        for (int i = 1; i < n_units; i += 2) {  // the second k-block of each pair
             const int u = u0 + i;
             const int t = u / kKBlocks;
-            const int buf = i % C::kNumAcc;
-            const uint32_t use = (uint32_t)(i / C::kNumAcc);
+            const int buf = (i >> 1) % C::kNumAcc;
+            const uint32_t use = (uint32_t)((i >> 1) / C::kNumAcc);
             // Each warp waits on its own; an abort seen by one is seen by all.
             if (!wait_phase(accfull_bar(buf), use & 1u, args, &s_abort)) break;
             __syncwarp();  // the TMEM loads below are warp-wide (.sync.aligned)
@@ -353,7 +358,7 @@ __global__ void __maxnreg__(BN == 16 ? 72 : 80)
             if constexpr (BN == 32)
                 epi_chunk<kDecodeMaxRows - 16>(acc, sum_hi, sum_lo, 16, run_start, run_end, true,
                                                accempty_bar(buf), out, col, rows);
-            if (!run_end) ptx::tmem_st_wait();  // the next k-block reads these sums back
+            if (!run_end) ptx::tmem_st_wait();  // the next pair reads these sums back
             if (run_end && !last) first_slot = slot;
             if (last && first_slot >= 0) {
                 float2 *p0 = args.ws + (size_t)first_slot * kDecodeMaxRows * kDTileCols;

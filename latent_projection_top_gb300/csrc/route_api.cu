@@ -254,14 +254,16 @@ route_status run_step(const route_plan *p, const void *hidden, const void *W_lat
 }
 
 // Decode stream grid: the largest CTA count, at most one per SM and at most
-// `cap`, that divides the 18 * 112 (tile, k-block) units evenly, so that every
-// CTA streams the same number of bytes (144 CTAs of 14 units on 152 SMs).
-// Never below the tile count, which route_prepare requires of the device.
+// `cap`, that divides the 18 * 112 (tile, k-block) units into equal, even
+// runs: every CTA streams the same number of bytes, and its k-blocks pair up
+// on one accumulator without a pair crossing a tile (tiles start at even
+// units).  144 CTAs of 14 units on 152 SMs.  Never below the tile count,
+// which route_prepare requires of the device.
 int decode_grid(int sms, int cap) {
     const int U = kDTiles * kKBlocks;
     const int hi = sms < cap ? sms : cap;
     for (int g = hi; g > kDTiles; --g)
-        if (U % g == 0) return g;
+        if ((U / 2) % g == 0) return g;
     return kDTiles;
 }
 

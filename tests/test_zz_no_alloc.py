@@ -89,7 +89,7 @@ def test_noalloc_matches_route_step_on_two_calls(rows):
         sms = torch.cuda.get_device_properties(0).multi_processor_count
         # the stream grid: the largest count <= min(SMs, cap) dividing the
         # 18 * 112 units; the allocation-free entry point caps it at 160
-        noalloc_grid = next(g for g in range(min(sms, 160), 17, -1) if 2016 % g == 0)
+        noalloc_grid = next(g for g in range(min(sms, 160), 17, -1) if 1008 % g == 0)
         if plan_grid == noalloc_grid:
             # Same kernels and the same split-K partition: identical bits.
             for name, a, b in zip(("latent", "logits", "ids", "weights"), g, w):
