@@ -219,7 +219,8 @@ struct TopkBlockSmem {
 // take every thread's share at once.  The threshold is the one above: each
 // lane of warp 0 takes the maximum of seven threads' maxima (28 logits), and
 // T = the 16th largest of those 32.  Candidates >= T are compacted with a
-// shared counter (their order is not fixed; the ranking is).  Rows with more
+// shared counter, one atomic per warp (their order is not fixed; the
+// ranking is).  Rows with more
 // than kCandMax candidates fall back to topk16_warp over `row`, the same 896
 // logits in shared memory.  Every one of the 224 threads calls it; it uses
 // named barrier `bar`.
@@ -247,12 +248,27 @@ __device__ __forceinline__ void topk16_block(const float (&v)[4], const int (&id
     }
     asm volatile("barrier.sync %0, %1;" ::"r"(bar), "n"(kThreads) : "memory");
     const uint32_t T = sh.T;
+    // Compaction, one shared atomic per warp: a ballot per key slot gives
+    // each candidate its place within the warp's share.
+    const int lane = tid & 31;
+    const uint32_t below = (1u << lane) - 1u;
+    uint32_t ball[4], wcount = 0u;
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
+    for (int j = 0; j < 4; ++j) {
+        ball[j] = __ballot_sync(0xFFFFFFFFu, key[j] >= T);
+        wcount += __popc(ball[j]);
+    }
+    uint32_t base = 0u;
+    if (lane == 0 && wcount != 0u) base = atomicAdd(&sh.count, wcount);
+    base = __shfl_sync(0xFFFFFFFFu, base, 0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
         if (key[j] >= T) {
-            const uint32_t pos = atomicAdd(&sh.count, 1u);
+            const uint32_t pos = base + __popc(ball[j] & below);
             if (pos < (uint32_t)kCandMax) sh.cand[pos] = make_uint2(key[j], (uint32_t)id[j]);
         }
+        base += __popc(ball[j]);
+    }
     asm volatile("barrier.sync %0, %1;" ::"r"(bar), "n"(kThreads) : "memory");
     if (tid >= 32) return;
     const uint32_t total = sh.count;
