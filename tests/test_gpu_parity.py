@@ -282,6 +282,25 @@ def test_prefill_8192_rows_sampled_and_position_independent():
     check_topk_exact(ids[:64], w[:64], ids_o, w_o)
 
 
+@pytest.mark.parametrize("mode,rows", [(route.DECODE, 8), (route.DECODE, 20), (route.PREFILL, 40)])
+def test_router_column_permutation_permutes_ids(mode, rows):
+    """Pin P7 on the GPU: with W_router's columns permuted, logit column e is
+    bit for bit the plain run's column perm[e] (every output is summed over
+    the same K slices in the same order wherever its column sits), so
+    perm[ids] are the plain run's ids and the weights are the same bits."""
+    hid, wl, wr = bank("decode_r8" if mode == route.DECODE else "prefill_r1024", 0)
+    hid = np.ascontiguousarray(np.resize(hid, (rows, hid.shape[1])))
+    perm = np.random.default_rng(7).permutation(route.N_EXPERTS)
+    dh, dwl = to_dev_bf16(hid), to_dev_bf16(wl)
+    with route.Plan(mode, rows) as plan:
+        lat_a, lg_a, ids_a, w_a = run_step(plan, dh, dwl, to_dev_bf16(wr))
+        lat_b, lg_b, ids_b, w_b = run_step(plan, dh, dwl, to_dev_bf16(wr[:, perm]))
+    assert np.array_equal(lat_a, lat_b)  # the latent does not see the router's columns
+    assert np.array_equal(lg_b.view(np.uint32), lg_a[:, perm].view(np.uint32))
+    assert np.array_equal(perm[ids_b], ids_a)
+    assert np.array_equal(w_b.view(np.uint32), w_a.view(np.uint32))
+
+
 # ------------------------------------------------------- host entry / errors
 
 @pytest.mark.parametrize("mode,rows", [(route.DECODE, 8), (route.DECODE, 20), (route.PREFILL, 40)])
