@@ -30,8 +30,9 @@
 // decode_finish_kernel -- at most one small CTA per SM, so that it fits next
 //   to a stream CTA: one CTA per row sums the row's 896 router logits and
 //   runs the top-16 on them with all its threads; the others sum the latent
-//   tiles, two (row, tile) items at a time (and, when asked, each latent
-//   row's sum of squares, or the general path's K-split latent).  Slots are
+//   tiles, two or four (row, tile) items per memory round trip (and, when
+//   asked, each latent row's sum of squares, or the general path's K-split
+//   latent).  Slots are
 //   summed in segment order as two-floats and rounded once, so results are
 //   bitwise reproducible and a row's bits do not depend on the row count
 //   (the partition depends only on the grid).
@@ -408,7 +409,7 @@ __device__ __forceinline__ void pin(SlotRun &s) {
     asm volatile("" : "+l"(s.p), "+r"(s.n));
 }
 
-template <int NP>
+template <int NP, int B = kFinishBatch>
 __device__ __forceinline__ void sum_slot_pairs(const SlotRun (&run)[NP], float2 (&y)[NP]) {
     const float4 *p[NP];
     int n[NP], nmax = 0;
@@ -420,15 +421,15 @@ __device__ __forceinline__ void sum_slot_pairs(const SlotRun (&run)[NP], float2 
         nmax = n[q] > nmax ? n[q] : nmax;
         h[2 * q] = h[2 * q + 1] = l[2 * q] = l[2 * q + 1] = 0.f;
     }
-    for (int s0 = 0; s0 < nmax; s0 += kFinishBatch) {
-        float4 v[NP][kFinishBatch];
+    for (int s0 = 0; s0 < nmax; s0 += B) {
+        float4 v[NP][B];
 #pragma unroll
-        for (int j = 0; j < kFinishBatch; ++j)
+        for (int j = 0; j < B; ++j)
 #pragma unroll
             for (int q = 0; q < NP; ++q)
                 if (s0 + j < n[q]) v[q][j] = __ldcg(p[q] + j * kSlotF4);
 #pragma unroll
-        for (int j = 0; j < kFinishBatch; ++j)
+        for (int j = 0; j < B; ++j)
 #pragma unroll
             for (int q = 0; q < NP; ++q)
                 if (s0 + j < n[q]) {
@@ -438,7 +439,7 @@ __device__ __forceinline__ void sum_slot_pairs(const SlotRun (&run)[NP], float2 
                     l[2 * q + 1] += v[q][j].w;
                 }
 #pragma unroll
-        for (int q = 0; q < NP; ++q) p[q] += kFinishBatch * kSlotF4;
+        for (int q = 0; q < NP; ++q) p[q] += B * kSlotF4;
     }
 #pragma unroll
     for (int q = 0; q < NP; ++q) y[q] = make_float2(two_float_value(h[2 * q], l[2 * q]),
@@ -452,21 +453,26 @@ __device__ __forceinline__ void sum_slot_pairs(const SlotRun (&run)[NP], float2 
 // (checked on the host), slot j of a latent tile is slice j: each slot's
 // two-float partial is rounded to FP32 and then to BF16, and the BF16 values
 // are added in FP32 in slice order; the caller rounds the sum to BF16.
-__device__ __forceinline__ float2 ksplit_slot_pair(const SlotRun &run) {
-    const float4 *p = run.p;
-    const int n = run.n;
-    float4 v[kFinishBatch];
+// NP column pairs at a time, all their slots loaded before any is added.
+template <int NP>
+__device__ __forceinline__ void ksplit_slot_pairs(const SlotRun (&run)[NP], float2 (&y)[NP]) {
+    float4 v[NP][kKSplitSlices];
 #pragma unroll
-    for (int j = 0; j < kFinishBatch; ++j)
-        if (j < n) v[j] = __ldcg(p + j * kSlotF4);
-    float s0 = 0.f, s1 = 0.f;
+    for (int j = 0; j < kKSplitSlices; ++j)
 #pragma unroll
-    for (int j = 0; j < kFinishBatch; ++j)
-        if (j < n) {
-            s0 += __uint_as_float((uint32_t)bf16_bits(two_float_value(v[j].x, v[j].y)) << 16);
-            s1 += __uint_as_float((uint32_t)bf16_bits(two_float_value(v[j].z, v[j].w)) << 16);
-        }
-    return make_float2(s0, s1);
+        for (int q = 0; q < NP; ++q)
+            if (j < run[q].n) v[q][j] = __ldcg(run[q].p + j * kSlotF4);
+#pragma unroll
+    for (int q = 0; q < NP; ++q) {
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < kKSplitSlices; ++j)
+            if (j < run[q].n) {
+                s0 += __uint_as_float((uint32_t)bf16_bits(two_float_value(v[q][j].x, v[q][j].y)) << 16);
+                s1 += __uint_as_float((uint32_t)bf16_bits(two_float_value(v[q][j].z, v[q][j].w)) << 16);
+            }
+        y[q] = make_float2(s0, s1);
+    }
 }
 
 // Small CTAs that fit on an SM next to a stream CTA: with overlap, the finish
@@ -475,18 +481,29 @@ __device__ __forceinline__ float2 ksplit_slot_pair(const SlotRun &run) {
 // round trip to memory takes microseconds, so a CTA makes as few as it can.
 // The grid is at most one CTA per SM: CTA r < rows sums row r's 896 router
 // logits (224 threads, two column pairs each) and runs the row's top-16 from
-// shared memory; the other CTAs sum latent items (row, 256-column tile), two
-// at a time (128 threads, one column pair each).
+// shared memory; the other CTAs sum latent items (row, 256-column tile) in
+// two halves of 128 threads, one column pair per thread, each half taking
+// `per_half` (1 or 2) consecutive items per memory round trip.
 static_assert(kExpertsTopk == kExperts, "top-16 row width");
 constexpr int kRouterThreads = kExperts / 4;    // 224
 constexpr int kLatentThreads = kDTileCols / 2;  // 128 per latent item
 constexpr int kFinishThreads = 2 * kLatentThreads;
 
+// Latent items per CTA half and round trip: 2 above 16 rows, or when one
+// pass over the 14 * rows items at 1 would need more than one CTA per SM;
+// else 1.  (Measured: at 20 rows the CTAs that needed two passes made it
+// 0.2 us a layer slower; at 17..18 rows 2 is 0.1..0.2 us faster, at 1..16
+// rows 1 is as fast or faster.)
+int finish_per_half(const DecodeArgs &a) {
+    return a.rows > 16 || a.rows + (kDLatTiles * a.rows + 1) / 2 > a.grid ? 2 : 1;
+}
+
 // rows router CTAs + enough latent CTAs for one pass over the 14 * rows
 // latent items, capped at the stream grid (one CTA per SM), with at least one
 // latent CTA.
 int finish_grid(const DecodeArgs &a) {
-    int g = a.rows + (kDLatTiles * a.rows + 1) / 2;
+    const int per_cta = 2 * finish_per_half(a);
+    int g = a.rows + (kDLatTiles * a.rows + per_cta - 1) / per_cta;
     if (g > a.grid) g = a.grid;
     if (g < a.rows + 1) g = a.rows + 1;
     return g;
@@ -542,10 +559,60 @@ __device__ __forceinline__ void latent_sumsq_part(const DecodeArgs &a, int r, in
     a.words[kWordSsCount + r] = 0u;
 }
 
+// The latent CTAs of the finish kernel (KSPLIT: the general path's K-split
+// arithmetic).  Pass p: each half sums items i0 .. i0 + per_half - 1, i0 =
+// per_half * (2 (p * latent CTAs + CTA) + half), with one memory round trip.
+template <bool KSPLIT>
+__device__ __forceinline__ void finish_latent(const DecodeArgs &a, int per_half,
+                                              float2 (&s_ss)[2][2][kLatentThreads / 32]) {
+    const int rows = a.rows;
+    const int tid = threadIdx.x;
+    const int b = blockIdx.x;
+    const int n_items = kDLatTiles * rows;
+    const int half = tid / kLatentThreads;
+    const int cc = 2 * (tid % kLatentThreads);
+    const int first = per_half * (2 * (b - rows) + half);
+    const int stride = per_half * 2 * ((int)gridDim.x - rows);
+    SlotRun run[2];
+    auto runs_at = [&](int i0) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int i = i0 + q;
+            run[q] = q < per_half && i < n_items ? slot_run(a, i / kDLatTiles, i % kDLatTiles, cc)
+                                                 : SlotRun{nullptr, 0};
+        }
+    };
+    runs_at(first);
+    pin(run[0]);
+    pin(run[1]);
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the stream kernel's partials are complete
+    int calls = 0;  // sum-of-squares scratch alternates between calls
+    for (int i0 = first; i0 < n_items; i0 += stride) {
+        if (i0 != first) runs_at(i0);
+        float2 y[2];
+        if constexpr (KSPLIT)
+            ksplit_slot_pairs<2>(run, y);
+        else
+            sum_slot_pairs<2, 8>(run, y);  // batches of 8 slots: the registers of two items
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int i = i0 + q;
+            if (q >= per_half || i >= n_items) break;  // the same for the whole half
+            const int r = i / kDLatTiles, t = i % kDLatTiles;
+            const uint16_t b0 = bf16_bits(y[q].x), b1 = bf16_bits(y[q].y);
+            *reinterpret_cast<uint32_t *>(a.latent + (size_t)r * kLatent + t * kDTileCols + cc) =
+                (uint32_t)b0 | ((uint32_t)b1 << 16);
+            if (a.sumsq != nullptr)
+                latent_sumsq_part(a, r, t, b0, b1, half, tid % kLatentThreads,
+                                  s_ss[calls++ & 1][half]);
+        }
+    }
+}
+
 __global__ void __maxnreg__(112) decode_finish_kernel(const __grid_constant__ DecodeArgs a,
-                                                      int do_topk) {
+                                                      int do_topk, int per_half) {
     __shared__ TopkBlockSmem s_topk;
-    __shared__ float2 s_ss[2][2][kLatentThreads / 32];  // [iteration parity][half][warp]
+    __shared__ float2 s_ss[2][2][kLatentThreads / 32];  // [call parity][half][warp]
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int rows = a.rows;
     const int tid = threadIdx.x;
@@ -571,30 +638,10 @@ __global__ void __maxnreg__(112) decode_finish_kernel(const __grid_constant__ De
         const int id[4] = {c0, c0 + 1, c1, c1 + 1};
         topk16_block(v, id, lrow, tid, 1, s_topk, a.ids + (size_t)r * kTopK,
                      a.weights + (size_t)r * kTopK);
+    } else if (a.ksplit) {
+        finish_latent<true>(a, per_half, s_ss);
     } else {
-        const int n_items = kDLatTiles * rows;
-        const int stride = 2 * ((int)gridDim.x - rows);
-        const int half = tid / kLatentThreads;
-        const int cc = 2 * (tid % kLatentThreads);
-        const int i0 = 2 * (b - rows) + half;
-        SlotRun run[1] = {i0 < n_items ? slot_run(a, i0 / kDLatTiles, i0 % kDLatTiles, cc)
-                                       : SlotRun{nullptr, 0}};
-        pin(run[0]);
-        asm volatile("griddepcontrol.wait;" ::: "memory");  // the stream kernel's partials are complete
-        for (int i = i0, parity = 0; i < n_items; i += stride, parity ^= 1) {
-            const int r = i / kDLatTiles, t = i % kDLatTiles;
-            if (i != i0) run[0] = slot_run(a, r, t, cc);
-            float2 y[1];
-            if (a.ksplit)
-                y[0] = ksplit_slot_pair(run[0]);
-            else
-                sum_slot_pairs<1>(run, y);
-            const uint16_t b0 = bf16_bits(y[0].x), b1 = bf16_bits(y[0].y);
-            *reinterpret_cast<uint32_t *>(a.latent + (size_t)r * kLatent + t * kDTileCols + cc) =
-                (uint32_t)b0 | ((uint32_t)b1 << 16);
-            if (a.sumsq != nullptr)
-                latent_sumsq_part(a, r, t, b0, b1, half, tid % kLatentThreads, s_ss[parity][half]);
-        }
+        finish_latent<false>(a, per_half, s_ss);
     }
 }
 
@@ -649,7 +696,7 @@ cudaError_t decode_launch(int bn, const CUtensorMap &map_h, const CUtensorMap &m
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t c =
         pdl_config(dim3(finish_grid(args)), dim3(kFinishThreads), 0, stream, attr);
-    return cudaLaunchKernelEx(&c, decode_finish_kernel, args, do_topk);
+    return cudaLaunchKernelEx(&c, decode_finish_kernel, args, do_topk, finish_per_half(args));
 }
 
 }  // namespace route
