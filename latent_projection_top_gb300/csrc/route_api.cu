@@ -192,7 +192,7 @@ route_status encode_all(const route_plan *p, const void *hidden, const void *W_l
 route_status launch_forward(const route_plan *p, const void *hidden, const void *W_latent,
                             const void *W_router, void *latent, float *logits, int32_t *ids,
                             float *weights, int do_topk, float *sumsq, cudaStream_t stream,
-                            bool after_staging = false) {
+                            bool after_copy_in = false) {
     CUtensorMap mh, ml, mr;
     route_status st = encode_all(p, hidden, W_latent, W_router, &mh, &ml, &mr);
     if (st != ROUTE_OK) return st;
@@ -204,8 +204,10 @@ route_status launch_forward(const route_plan *p, const void *hidden, const void 
         a.ids = ids;
         a.weights = weights;
         a.sumsq = sumsq;
-        if (after_staging) a.overlap = 0;  // hidden is the staging kernel's output
-        a.hold_ns = a.overlap || after_staging ? 0u : kPrefetchHoldNs;
+        // After the host path's copy in (a staging kernel or a copy), hidden
+        // is the predecessor's output, and no finish kernel precedes.
+        if (after_copy_in) a.overlap = 0;
+        a.hold_ns = a.overlap || after_copy_in ? 0u : kPrefetchHoldNs;
         e = decode_launch(p->bn, mh, ml, mr, a, do_topk, stream);
         if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
     } else {
@@ -573,8 +575,8 @@ route_status route_step_host(const route_plan *plan, const void *hidden_host,
     if ((e = cudaMemcpyAsync(d.hidden, hidden_host, r * kHidden * 2, cudaMemcpyHostToDevice, s)) !=
         cudaSuccess)
         return cuda_fail(e, "copy hidden to device");
-    if ((st = run_step(plan, d.hidden, W_latent, W_router, d.latent, d.logits, d.ids, d.weights,
-                       s)) != ROUTE_OK)
+    if ((st = launch_forward(plan, d.hidden, W_latent, W_router, d.latent, d.logits, d.ids,
+                             d.weights, 1, nullptr, s, true)) != ROUTE_OK)
         return st;
     if ((e = cudaMemcpyAsync(latent_host, d.latent, r * kLatent * 2, cudaMemcpyDeviceToHost, s)) !=
             cudaSuccess ||
