@@ -162,6 +162,31 @@ route_status route_step_host(const route_plan *plan, const void *hidden_host,
                              void *stream);
 
 /*
+ * route_host_step: route_step_host on fixed buffers, prepared once, for a
+ * serving loop that refills the same page-locked `hidden_host` every step and
+ * reads the results in place.
+ *
+ * route_host_step_create takes the arguments of route_step_host.  Decode
+ * plans with every host buffer page-locked and 16-byte aligned only (the
+ * path that copies nothing); otherwise ROUTE_ERR_PLAN, and the caller uses
+ * route_step_host.  The staging, stream and finish kernels are captured once
+ * into a CUDA graph (on a stream of the step's own), so that
+ * route_host_step_run is one graph launch on `stream` and a synchronise of
+ * `stream`; it returns after the results are in the host buffers.  The step
+ * belongs to the plan: route_destroy releases its graph, after which
+ * route_host_step_run returns ROUTE_ERR_NULL.  route_host_step_destroy frees
+ * the step (NULL: no-op).  Steps and their plan are not thread-safe.
+ */
+typedef struct route_host_step route_host_step;
+
+route_status route_host_step_create(route_plan *plan, const void *hidden_host,
+                                    const void *W_latent, const void *W_router,
+                                    void *latent_host, float *logits_host, int32_t *ids_host,
+                                    float *weights_host, void *stream, route_host_step **out);
+route_status route_host_step_run(route_host_step *step);
+route_status route_host_step_destroy(route_host_step *step);
+
+/*
  * route_device_status: synchronise the plan's device, then report (and clear)
  * the device-side error word that kernels set instead of hanging: ROUTE_OK
  * or ROUTE_ERR_DEVICE_TIMEOUT (a bounded wait expired; outputs of that launch

@@ -15,7 +15,8 @@ The route step of one MoE layer (see ``include/route.h``):
   that finishes the split-K sums and runs the top-16);
 * ``route_step_sumsq`` -- ``route_step`` plus each latent row's sum of squares;
 * ``route_step_host`` -- ``route_step`` with host tensors (transfers included);
-  ``HostStep`` -- the same on fixed buffers, checked once, for serving loops;
+  ``HostStep`` -- the same on fixed buffers, checked once and (decode,
+  page-locked buffers) captured as a CUDA graph, for serving loops;
 * ``route_set_overlap``, ``route_set_latent_ksplit`` -- plan options.
 """
 
@@ -40,6 +41,7 @@ STATUS_NAMES = {
     4: "ROUTE_ERR_ALIGN", 5: "ROUTE_ERR_CUDA", 6: "ROUTE_ERR_DEVICE_TIMEOUT",
     7: "ROUTE_ERR_PLAN", 8: "ROUTE_ERR_DEVICE",
 }
+STATUS_CODES = {name: code for code, name in STATUS_NAMES.items()}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libroute.so")
@@ -50,7 +52,8 @@ EXPORTS = (
     "route_step_host", "route_device_status", "route_plan_rows", "route_plan_mode",
     "route_plan_grid", "route_plan_segments", "route_last_error", "route_test_stall",
     "route_set_overlap", "route_step_decode_noalloc", "route_step_sumsq",
-    "route_set_latent_ksplit",
+    "route_set_latent_ksplit", "route_host_step_create", "route_host_step_run",
+    "route_host_step_destroy",
 )
 
 
@@ -93,6 +96,11 @@ def lib() -> ctypes.CDLL:
         L.route_set_latent_ksplit.restype = i32
         L.route_test_stall.argtypes = [vp, i32, ctypes.c_uint64]
         L.route_test_stall.restype = i32
+        L.route_host_step_create.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(vp)]
+        L.route_host_step_run.argtypes = [vp]
+        L.route_host_step_destroy.argtypes = [vp]
+        for f in ("route_host_step_create", "route_host_step_run", "route_host_step_destroy"):
+            getattr(L, f).restype = i32
         for f in ("route_plan_rows", "route_plan_mode", "route_plan_grid", "route_plan_segments"):
             getattr(L, f).argtypes = [vp]
             getattr(L, f).restype = i32
@@ -299,9 +307,13 @@ class HostStep:
 
     For a serving loop that refills the same page-locked ``hidden_host`` and
     reads the same result buffers every step: the tensors are validated and
-    their pointers marshalled here, so each call goes straight to the C entry
-    point (the checks cost about 5 us a call otherwise).  The object keeps
-    references to the tensors and the plan; the caller must not resize them.
+    their pointers marshalled here, and for a decode plan with page-locked
+    buffers the step is prepared once as a captured graph
+    (``route_host_step_create``), so each call is one graph launch and a wait
+    (``route_host_step_run``).  Otherwise each call goes straight to
+    ``route_step_host``.  The object keeps references to the tensors and the
+    plan; the caller must not resize them.  ``close()`` (or the plan's)
+    releases the graph.
     """
 
     def __init__(self, plan: Plan, hidden_host, W_latent, W_router, latent_host, logits_host,
@@ -311,12 +323,41 @@ class HostStep:
         self._args = (plan.handle,) + _host_step_args(
             plan, hidden_host, W_latent, W_router, latent_host, logits_host, ids_host,
             weights_host) + (_stream(stream, plan.device),)
-        self._fn = lib().route_step_host
+        L = lib()
+        self._step = None
+        h = ctypes.c_void_p()
+        st = L.route_host_step_create(*self._args, ctypes.byref(h))
+        if st == ROUTE_OK:
+            self._step = h
+            self._fn, self._call_args = L.route_host_step_run, (h,)
+        elif st == STATUS_CODES["ROUTE_ERR_PLAN"]:  # not the copy-free decode path
+            self._fn, self._call_args = L.route_step_host, self._args
+        else:
+            _check(st)
+
+    @property
+    def graph(self) -> bool:
+        """True when calls launch the captured graph."""
+        return self._step is not None
 
     def __call__(self) -> None:
-        st = self._fn(*self._args)
+        if self._fn is None:
+            raise RouteError(STATUS_CODES["ROUTE_ERR_NULL"], "host step is closed")
+        st = self._fn(*self._call_args)
         if st != ROUTE_OK:
             _check(st)
+
+    def close(self) -> None:
+        if self._step is not None:
+            lib().route_host_step_destroy(self._step)
+            self._step = None
+        self._fn = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def route_set_overlap(plan: Plan, enable: bool) -> None:

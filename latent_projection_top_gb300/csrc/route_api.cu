@@ -37,6 +37,17 @@ struct route_plan {
         CUtensorMap map;
     };
     mutable MapCache map_h, map_wl, map_wr;
+    route_host_step *steps = nullptr;  // prepared host steps, released with the plan
+};
+
+// A captured route_step_host (decode, page-locked buffers): staging kernel,
+// stream kernel, finish kernel.
+struct route_host_step {
+    route_plan *plan;         // NULL once the plan is gone
+    route_host_step *next;    // the plan's list
+    cudaGraph_t graph;
+    cudaGraphExec_t exec;
+    cudaStream_t stream;      // the caller's stream: launches and waits there
 };
 
 namespace {
@@ -115,8 +126,19 @@ struct DeviceGuard {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+void release_step_graph(route_host_step *h) {
+    if (h->exec) cudaGraphExecDestroy(h->exec);
+    if (h->graph) cudaGraphDestroy(h->graph);
+    h->exec = nullptr;
+    h->graph = nullptr;
+}
+
 void free_plan(route_plan *p) {
     if (!p) return;
+    for (route_host_step *h = p->steps; h; h = h->next) {  // the steps outlive it, inert
+        release_step_graph(h);
+        h->plan = nullptr;
+    }
     if (p->ws) cudaFree(p->ws);
     if (p->words) cudaFree(p->words);
     if (p->staging) cudaFree(p->staging);
@@ -534,6 +556,22 @@ void *mapped_host(const void *p) {
     return a.devicePointer;
 }
 
+// The host path without copies: the staging kernel reads the hidden rows
+// through their mapped address (h), the finish kernel writes the results to
+// the mapped host buffers.  Enqueued on s; nothing waits.
+static route_status enqueue_mapped_step(const route_plan *plan, const void *h,
+                                        const void *W_latent, const void *W_router, void *lat,
+                                        void *lg, void *ids, void *w, cudaStream_t s) {
+    const Staging d = staging_of(plan);
+    cudaError_t e;
+    if ((e = stage_in_launch(h, d.hidden, (size_t)plan->rows * kHidden * 2, s)) != cudaSuccess)
+        return cuda_fail(e, "stage hidden rows");
+    // after the staging kernel: no overlap, no hold
+    return launch_forward(plan, d.hidden, W_latent, W_router, lat, static_cast<float *>(lg),
+                          static_cast<int32_t *>(ids), static_cast<float *>(w), 1, nullptr, s,
+                          true);
+}
+
 route_status route_step_host(const route_plan *plan, const void *hidden_host,
                              const void *W_latent, const void *W_router, void *latent_host,
                              float *logits_host, int32_t *ids_host, float *weights_host,
@@ -560,12 +598,8 @@ route_status route_step_host(const route_plan *plan, const void *hidden_host,
              *w = mapped_host(weights_host);
         if (h && lat && lg && ids && w && aligned16(h) && aligned16(lat) && aligned16(lg) &&
             aligned16(ids) && aligned16(w)) {
-            if ((e = stage_in_launch(h, d.hidden, r * kHidden * 2, s)) != cudaSuccess)
-                return cuda_fail(e, "stage hidden rows");
-            // after the staging kernel: no overlap, no hold
-            if ((st = launch_forward(plan, d.hidden, W_latent, W_router, lat,
-                                     static_cast<float *>(lg), static_cast<int32_t *>(ids),
-                                     static_cast<float *>(w), 1, nullptr, s, true)) != ROUTE_OK)
+            if ((st = enqueue_mapped_step(plan, h, W_latent, W_router, lat, lg, ids, w, s)) !=
+                ROUTE_OK)
                 return st;
             if ((e = cudaStreamSynchronize(s)) != cudaSuccess)
                 return cuda_fail(e, "cudaStreamSynchronize");
@@ -607,6 +641,86 @@ route_status route_device_status(const route_plan *plan) {
     cudaDeviceSynchronize();
     return fail(ROUTE_ERR_DEVICE_TIMEOUT,
                 "a kernel gave up waiting (status 0x%x); that launch's outputs are invalid", status);
+}
+
+route_status route_host_step_create(route_plan *plan, const void *hidden_host,
+                                    const void *W_latent, const void *W_router,
+                                    void *latent_host, float *logits_host, int32_t *ids_host,
+                                    float *weights_host, void *stream, route_host_step **out) {
+    route_status st = check_plan(plan);
+    if (st != ROUTE_OK) return st;
+    if (!out) return fail(ROUTE_ERR_NULL, "out must be non-NULL");
+    *out = nullptr;
+    if (!hidden_host || !W_latent || !W_router || !latent_host || !logits_host || !ids_host ||
+        !weights_host)
+        return fail(ROUTE_ERR_NULL, "every pointer must be non-NULL");
+    if (!aligned16(W_latent) || !aligned16(W_router))
+        return fail(ROUTE_ERR_ALIGN, "weight pointers must be 16-byte aligned");
+    if (plan->mode != ROUTE_DECODE)
+        return fail(ROUTE_ERR_PLAN, "host steps are prepared for decode plans only");
+    DeviceGuard guard(plan->device);
+    if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+    void *h = mapped_host(hidden_host), *lat = mapped_host(latent_host),
+         *lg = mapped_host(logits_host), *ids = mapped_host(ids_host),
+         *w = mapped_host(weights_host);
+    if (!(h && lat && lg && ids && w && aligned16(h) && aligned16(lat) && aligned16(lg) &&
+          aligned16(ids) && aligned16(w)))
+        return fail(ROUTE_ERR_PLAN,
+                    "host steps need every host buffer page-locked and 16-byte aligned");
+    route_host_step *step = new (std::nothrow) route_host_step{};
+    if (!step) return fail(ROUTE_ERR_CUDA, "out of host memory");
+    step->stream = static_cast<cudaStream_t>(stream);
+    // Capture on a stream of our own: the caller's may be the legacy
+    // default stream, which cannot be captured.
+    cudaStream_t cs = nullptr;
+    cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+    if (e == cudaSuccess) {
+        st = enqueue_mapped_step(plan, h, W_latent, W_router, lat, lg, ids, w, cs);
+        const cudaError_t e2 = cudaStreamEndCapture(cs, &step->graph);
+        if (st == ROUTE_OK && e2 != cudaSuccess) e = e2;
+    }
+    if (st == ROUTE_OK && e == cudaSuccess)
+        e = cudaGraphInstantiate(&step->exec, step->graph, 0);
+    if (cs) cudaStreamDestroy(cs);
+    if (st != ROUTE_OK || e != cudaSuccess) {
+        release_step_graph(step);
+        delete step;
+        return st != ROUTE_OK ? st : cuda_fail(e, "capture the host step");
+    }
+    step->plan = plan;
+    step->next = plan->steps;
+    plan->steps = step;
+    *out = step;
+    return ROUTE_OK;
+}
+
+route_status route_host_step_run(route_host_step *step) {
+    g_err[0] = '\0';
+    if (!step || !step->plan || !step->exec)
+        return fail(ROUTE_ERR_NULL, "host step is NULL or its plan has been destroyed");
+    DeviceGuard guard(step->plan->device);
+    if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+    cudaError_t e = cudaGraphLaunch(step->exec, step->stream);
+    if (e != cudaSuccess) return cuda_fail(e, "launch the host step");
+    if ((e = cudaStreamSynchronize(step->stream)) != cudaSuccess)
+        return cuda_fail(e, "cudaStreamSynchronize");
+    return ROUTE_OK;
+}
+
+route_status route_host_step_destroy(route_host_step *step) {
+    if (!step) return ROUTE_OK;
+    if (route_plan *p = step->plan) {
+        for (route_host_step **q = &p->steps; *q; q = &(*q)->next)
+            if (*q == step) {
+                *q = step->next;
+                break;
+            }
+        DeviceGuard guard(p->device);
+        release_step_graph(step);
+    }
+    delete step;
+    return ROUTE_OK;
 }
 
 route_status route_set_overlap(route_plan *plan, int enable) {

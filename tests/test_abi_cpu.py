@@ -90,6 +90,10 @@ def test_calls_with_null_plan(lib):
     assert lib.route_set_latent_ksplit(null, 1) == 3
     assert lib.route_test_stall(null, 1, 0) == 3
     assert lib.route_device_status(null) == 3
+    out = ctypes.c_void_p(0x1000)
+    assert lib.route_host_step_create(null, x, x, x, x, x, x, x, None, ctypes.byref(out)) == 3
+    assert lib.route_host_step_run(null) == 3
+    assert lib.route_host_step_destroy(null) == 0
     assert lib.route_destroy(null) == 0
     for f in ("route_plan_rows", "route_plan_mode", "route_plan_grid", "route_plan_segments"):
         assert getattr(lib, f)(null) == -1

@@ -345,6 +345,7 @@ def test_host_step_reuses_buffers():
         ids = torch.empty((rows, route.TOPK), dtype=torch.int32).pin_memory()
         w = torch.empty((rows, route.TOPK), dtype=torch.float32).pin_memory()
         step = route.HostStep(plan, h_host, dwl, dwr, lat, lg, ids, w)
+        assert step.graph  # decode, page-locked: the captured graph
         for h, dev in zip((h0, h1, h0), want + want[:1]):
             h_host.copy_(torch.from_numpy(h.view(np.int16).copy()).view(torch.bfloat16))
             step()
@@ -354,7 +355,34 @@ def test_host_step_reuses_buffers():
             assert np.array_equal(w.numpy().view(np.uint32), dev[3].view(np.uint32))
         route.route_device_status(plan)
     with pytest.raises(route.RouteError):
+        step()  # the plan released the step's graph
+    step.close()
+    with pytest.raises(route.RouteError):
         step()
+
+
+@pytest.mark.parametrize("mode,rows,pinned", [(route.DECODE, 8, False), (route.PREFILL, 40, True)])
+def test_host_step_without_graph_runs_route_step_host(mode, rows, pinned):
+    """Pageable buffers, or a prefill plan: HostStep calls route_step_host."""
+    hid, wl, wr = bank("decode_r8" if mode == route.DECODE else "prefill_r1024", 0)
+    hid = np.ascontiguousarray(np.resize(hid, (rows, hid.shape[1])))
+    dwl, dwr = to_dev_bf16(wl), to_dev_bf16(wr)
+    pin = (lambda t: t.pin_memory()) if pinned else (lambda t: t)
+    with route.Plan(mode, rows) as plan:
+        dev = run_step(plan, to_dev_bf16(hid), dwl, dwr)
+        h_host = pin(torch.from_numpy(hid.view(np.int16).copy()).view(torch.bfloat16))
+        lat = pin(torch.empty((rows, route.N_LATENT), dtype=torch.bfloat16))
+        lg = pin(torch.empty((rows, route.N_EXPERTS), dtype=torch.float32))
+        ids = pin(torch.empty((rows, route.TOPK), dtype=torch.int32))
+        w = pin(torch.empty((rows, route.TOPK), dtype=torch.float32))
+        step = route.HostStep(plan, h_host, dwl, dwr, lat, lg, ids, w)
+        assert not step.graph
+        step()
+        route.route_device_status(plan)
+    assert np.array_equal(lat.view(torch.int16).numpy().view(np.uint16), dev[0])
+    assert np.array_equal(lg.numpy().view(np.uint32), dev[1].view(np.uint32))
+    assert np.array_equal(ids.numpy(), dev[2])
+    assert np.array_equal(w.numpy().view(np.uint32), dev[3].view(np.uint32))
 
 
 def test_gpu_argument_errors():
