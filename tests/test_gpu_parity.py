@@ -328,15 +328,16 @@ def test_route_step_host_matches_device(mode, rows, pinned):
     assert np.array_equal(w.numpy().view(np.uint32), dev[3].view(np.uint32))
 
 
-def test_host_step_reuses_buffers():
-    """HostStep: checked once, then each call runs route_step_host on the same
-    buffers -- new hidden rows written into hidden_host give that step's
-    results; once the plan is closed a call is refused, not run."""
-    rows = 8
+@pytest.mark.parametrize("rows", [1, 8, 20])
+def test_host_step_reuses_buffers(rows):
+    """HostStep: checked once and captured as a graph, then each call runs the
+    copy-free host path on the same buffers -- new hidden rows written into
+    hidden_host give that step's results; once the plan is closed a call is
+    refused, not run."""
     _, wl, wr = bank("decode_r8", 0)
     dwl, dwr = to_dev_bf16(wl), to_dev_bf16(wr)
-    h0 = bank("decode_r8", 0)[0][:rows]
-    h1 = bank("decode_r8", 1)[0][:rows]
+    h0 = np.ascontiguousarray(np.resize(bank("decode_r8", 0)[0], (rows, route.K_HIDDEN)))
+    h1 = np.ascontiguousarray(np.resize(bank("decode_r8", 1)[0], (rows, route.K_HIDDEN)))
     with route.Plan(route.DECODE, rows) as plan:
         want = [run_step(plan, to_dev_bf16(h), dwl, dwr) for h in (h0, h1)]
         h_host = torch.empty((rows, route.K_HIDDEN), dtype=torch.bfloat16).pin_memory()
