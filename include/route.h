@@ -172,9 +172,10 @@ route_status route_step_host(const route_plan *plan, const void *hidden_host,
  * route_step_host.  The staging, stream and finish kernels are captured once
  * into a CUDA graph (on a stream of the step's own), so that
  * route_host_step_run is one graph launch on `stream` and a synchronise of
- * `stream`; it returns after the results are in the host buffers.  The step
- * belongs to the plan: route_destroy releases its graph, after which
- * route_host_step_run returns ROUTE_ERR_NULL.  route_host_step_destroy frees
+ * `stream`; it returns after the results are in the host buffers.  The
+ * graph keeps the plan's settings (route_set_latent_ksplit) as they were at
+ * creation.  The step belongs to the plan: route_destroy releases its
+ * graph, after which route_host_step_run returns ROUTE_ERR_NULL.  route_host_step_destroy frees
  * the step (NULL: no-op).  Steps and their plan are not thread-safe.
  */
 typedef struct route_host_step route_host_step;
