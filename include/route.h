@@ -175,8 +175,9 @@ route_status route_step_host(const route_plan *plan, const void *hidden_host,
  * `stream`; it returns after the results are in the host buffers.  The
  * graph keeps the plan's settings (route_set_latent_ksplit) as they were at
  * creation.  The step belongs to the plan: route_destroy releases its
- * graph, after which route_host_step_run returns ROUTE_ERR_NULL.  route_host_step_destroy frees
- * the step (NULL: no-op).  Steps and their plan are not thread-safe.
+ * graph, after which route_host_step_run returns ROUTE_ERR_NULL.
+ * route_host_step_destroy frees the step (NULL: no-op).  Steps and their
+ * plan are not thread-safe.
  */
 typedef struct route_host_step route_host_step;
 
