@@ -75,7 +75,7 @@ def parse_args():
     p.add_argument("--prefill-banks", type=int, default=92,
                    help="distinct weight banks of a prefill chunk (one per layer)")
     p.add_argument("--no-overlap", action="store_true",
-                   help="decode: keep each step's weight stream behind the previous step's tail")
+                   help="read each step's hidden rows only after the previous step has finished")
     return p.parse_args()
 
 
@@ -493,7 +493,7 @@ def main_ours(args):
                          wk == "decode_sweep" else 1024 if wk == "prefill_r1024" else 3072)
     decode = wk.startswith("decode")
     nbanks = 8 if decode else args.prefill_banks
-    overlap = decode and not args.no_overlap
+    overlap = not args.no_overlap
     plan, steps, launches = rb.make_steps(wk, rows, nbanks, overlap=overlap)
     ms, clocks = rb.run(steps, args.steps, args.warmup, dist, sampler_index=dev)
     rb.route.route_device_status(plan)  # raises if any launch hit a bounded-wait timeout
@@ -518,7 +518,7 @@ def main_ours(args):
                 "algorithmic_bytes_per_launch": algo,
                 "traffic": recorded_traffic("decode_stream_kernel", wk)}
     else:
-        p2, gsteps, _ = rb.make_steps(wk, rows, nbanks, gemm_only=True)
+        p2, gsteps, _ = rb.make_steps(wk, rows, nbanks, gemm_only=True, overlap=overlap)
         gms, _ = rb.run(gsteps, 92, 3 * 92, dist)
         kern_s = dist.max(gms) / 1e3 / 92
         flop = FLOP_PER_ROW * rows
@@ -544,15 +544,17 @@ def main_ours(args):
                       "parallelism": f"replicas x{dist.world} (no sharding, no collectives)"},
            "roofline": roof, "clocks": clocks, "gpu_launches": launches * args.steps}
 
-    if decode and overlap:
+    if overlap:
         # the same workload with each step held behind the previous one's tail
         p3, s3, _ = rb.make_steps(wk, rows, nbanks, overlap=False)
-        ms3, _ = rb.run(s3, min(args.steps, 64 * 256), args.warmup, dist)
-        t3 = dist.max(ms3) / 1e3 / min(args.steps, 64 * 256)
-        algo = WEIGHT_BYTES + rows * ROW_BYTES
+        n3 = min(args.steps, 64 * 256)
+        ms3, _ = rb.run(s3, n3, args.warmup, dist, **({} if decode else {"graph_len": 92}))
+        t3 = dist.max(ms3) / 1e3 / n3
         out["without_overlap"] = {"us_per_layer": round(t3 * 1e6, 3),
-                                  "rows_per_s": round(dist.world * rows / t3, 1),
-                                  "hbm_frac": round(algo / t3 / 1e9 / peaks["hbm_gbs"], 4)}
+                                  "rows_per_s": round(dist.world * rows / t3, 1)}
+        if decode:
+            algo = WEIGHT_BYTES + rows * ROW_BYTES
+            out["without_overlap"]["hbm_frac"] = round(algo / t3 / 1e9 / peaks["hbm_gbs"], 4)
         p3.close()
     if not args.no_e2e:
         out["e2e"] = rb.e2e(wk, rows, min(args.steps, 4096), dist)
@@ -586,27 +588,28 @@ def sweep(rb, dist, peaks, args):
         res.append(entry)
     for wk, rows in [("prefill_r1024", 1024), ("prefill_r3072", 3072)]:
         nb = args.prefill_banks
-        plan, steps, _ = rb.make_steps(wk, rows, nb)
-        ms, _ = rb.run(steps, 92 * 5, 92 * 2, dist, graph_len=92)
-        ms = dist.max(ms)
-        t = ms / 1e3 / (92 * 5)
-        p2, gsteps, _ = rb.make_steps(wk, rows, nb, gemm_only=True)
-        gms, _ = rb.run(gsteps, 92 * 5, 92 * 2, dist, graph_len=92)
-        rb.route.route_device_status(plan)
-        rb.route.route_device_status(p2)
-        tg = dist.max(gms) / 1e3 / (92 * 5)
         flop = FLOP_PER_ROW * rows
-        e = {"workload": wk, "rows": rows, "us_per_layer": round(t * 1e6, 3),
-             "chunk_ms_92_layers": round(t * 92 * 1e3, 3),
-             "rows_per_s": round(rows / t, 1), "gemm_us": round(tg * 1e6, 3),
-             "bound": "tensor", "gemm_tflops": round(flop / tg / 1e12, 1),
-             "frac": round(flop / tg / 1e12 / peaks["bf16_tflops"], 4),
-             "weight_banks": nb}
-        if rows == 3072:
-            e["per_layer_us"] = rb.per_layer_us(steps[:92], dist)
+        e = {"workload": wk, "rows": rows, "bound": "tensor", "weight_banks": nb}
+        for ov in (True, False):
+            plan, steps, _ = rb.make_steps(wk, rows, nb, overlap=ov)
+            ms, _ = rb.run(steps, 92 * 5, 92 * 2, dist, graph_len=92)
+            t = dist.max(ms) / 1e3 / (92 * 5)
+            p2, gsteps, _ = rb.make_steps(wk, rows, nb, gemm_only=True, overlap=ov)
+            gms, _ = rb.run(gsteps, 92 * 5, 92 * 2, dist, graph_len=92)
+            rb.route.route_device_status(plan)
+            rb.route.route_device_status(p2)
+            tg = dist.max(gms) / 1e3 / (92 * 5)
+            sfx = "" if ov else "_without_overlap"
+            e.update({"us_per_layer" + sfx: round(t * 1e6, 3),
+                      "chunk_ms_92_layers" + sfx: round(t * 92 * 1e3, 3),
+                      "rows_per_s" + sfx: round(rows / t, 1), "gemm_us" + sfx: round(tg * 1e6, 3),
+                      "gemm_tflops" + sfx: round(flop / tg / 1e12, 1),
+                      "frac" + sfx: round(flop / tg / 1e12 / peaks["bf16_tflops"], 4)})
+            if rows == 3072 and ov:
+                e["per_layer_us"] = rb.per_layer_us(steps[:92], dist)
+            plan.close()
+            p2.close()
         res.append(e)
-        plan.close()
-        p2.close()
     # the route step that also returns each latent row's sum of squares
     for wk, rows, ov in [("decode_r8", 8, True), ("decode_sweep", 20, True),
                          ("prefill_r3072", 3072, False)]:

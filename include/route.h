@@ -197,16 +197,18 @@ route_status route_host_step_destroy(route_host_step *step);
 route_status route_device_status(const route_plan *plan);
 
 /*
- * route_set_overlap: let a decode plan's weight stream start before the
+ * route_set_overlap: let a plan's projection read `hidden` before the
  * preceding work on the stream has finished.  Every route kernel lets its
- * successor launch early; by default the decode kernel still waits for its
- * predecessor before it reads `hidden`.  With enable != 0 it reads `hidden`
- * at once and waits only before it first writes its scratch, so a step's
- * weight stream runs under the previous step's final reduction and top-16.
- * Enable ONLY when `hidden` is never written by the route call issued
- * immediately before on the same stream (it is safe whenever any other
- * kernel or copy produces `hidden`: those do not release their successors
- * early).  Prefill plans ignore the setting.  Default: disabled.
+ * successor launch early; by default the projection kernels still wait for
+ * their predecessor before they read `hidden`.  With enable != 0 they read
+ * it at once and wait only before they first write (decode: its scratch;
+ * prefill: its outputs), so a decode step's weight stream runs under the
+ * previous step's final reduction and top-16, and a prefill GEMM's main loop
+ * under the previous step's top-16.  Enable ONLY when `hidden` is never
+ * written by the route call issued immediately before on the same stream
+ * (it is safe whenever any other kernel or copy produces `hidden`: those do
+ * not release their successors early).  route_step_host ignores it.
+ * Default: disabled.
  */
 route_status route_set_overlap(route_plan *plan, int enable);
 

@@ -44,6 +44,7 @@ struct ProjArgs {
     int grid;            // persistent CTAs launched (pairs of CTAs: even)
     int test_stall;      // test hook: skip each CTA's last copy so a wait must time out
     int ksplit;          // latent with the general path's K-split arithmetic
+    int overlap;         // read hidden before the grid dependency resolves
     unsigned long long timeout_ns;  // bound on every wait inside the kernel
     unsigned *status;          // device status word
     uint16_t *latent;          // [rows, 3584] BF16 bits

@@ -37,7 +37,9 @@
 //
 // Programmatic dependent launch: weight boxes of the first stages are
 // requested before `griddepcontrol.wait` (no predecessor writes the weights);
-// hidden rows are read and outputs written only after it.
+// outputs are written only after it, and hidden rows are read only after it
+// too unless `overlap` is set (then the main loop runs under the previous
+// step's top-16).
 //
 // Every wait is bounded: after args.timeout_ns a waiting thread sets the
 // device status word and the CTA's abort flag, in-flight copies and MMAs are
@@ -225,7 +227,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
                 weights_of(it, sbase + it * kStageBytes, ptx::map_to_rank(full_bar(it), 0u));
                 armed |= 1u << it;
             }
-            asm volatile("griddepcontrol.wait;" ::: "memory");
+            if (!args.overlap) asm volatile("griddepcontrol.wait;" ::: "memory");
             for (int it = 0; it < n_pre; ++it) {
                 if (args.test_stall && leader && it == total - 1) continue;  // test hook
                 hidden_of(it, sbase + it * kStageBytes, ptx::map_to_rank(full_bar(it), 0u));

@@ -236,6 +236,7 @@ route_status launch_forward(const route_plan *p, const void *hidden, const void 
         ProjArgs a = p->pre;
         a.latent = static_cast<uint16_t *>(latent);
         a.logits = logits;
+        if (after_copy_in) a.overlap = 0;
         e = prefill_launch(mh, ml, mr, a, stream);
         if (e != cudaSuccess) return cuda_fail(e, "prefill kernel launch");
         if (do_topk) {
@@ -726,7 +727,7 @@ route_status route_host_step_destroy(route_host_step *step) {
 route_status route_set_overlap(route_plan *plan, int enable) {
     route_status st = check_plan(plan);
     if (st != ROUTE_OK) return st;
-    plan->dec.overlap = enable ? 1 : 0;
+    plan->dec.overlap = plan->pre.overlap = enable ? 1 : 0;
     return ROUTE_OK;
 }
 

@@ -163,14 +163,17 @@ def test_decode_batch_invariance_and_determinism():
                                   np.asarray(b)[:rows].view(np.uint8)), f"rows={rows}"
 
 
+@pytest.mark.parametrize("mode,rows,workload", [(route.DECODE, 8, "decode_r8"),
+                                                (route.PREFILL, 300, "prefill_r1024")])
 @pytest.mark.parametrize("overlap", [False, True])
-def test_decode_bank_cycling_under_graph_replay(overlap):
+def test_bank_cycling_under_graph_replay(mode, rows, workload, overlap):
     """Banks cycled inside one captured CUDA graph give the eager bits, also
-    when consecutive steps overlap (hidden is not written by route calls)."""
-    rows = 8
-    banks = [bank("decode_r8", b) for b in range(3)]
+    when consecutive steps overlap (hidden is not written by route calls):
+    decode, and prefill (whose GEMM then reads hidden under the previous
+    step's top-16 and writes only after it)."""
+    banks = [bank(workload, b) for b in range(3)]
     dev = [(to_dev_bf16(h[:rows]), to_dev_bf16(wl), to_dev_bf16(wr)) for h, wl, wr in banks]
-    with route.Plan(route.DECODE, rows) as plan:
+    with route.Plan(mode, rows) as plan:
         eager = [run_step(plan, *d) for d in dev]
         route.route_set_overlap(plan, overlap)
         outs = [outputs(rows) for _ in dev]
