@@ -110,7 +110,9 @@ route_status latent_router_forward(const route_plan *plan, const void *hidden,
  *                                       (-0 == +0) go to the lower expert id;
  *                                       NaN ranks below every number
  *   weights [rows, 16] FP32  (written)  s_i / sum_j s_j, s = sigmoid(logit),
- *                                       evaluated in double, rounded to FP32
+ *                                       in FP32 with compensated (two-float)
+ *                                       steps and one final rounding: within
+ *                                       5 FP32 ULP of the value in double
  * ("Kimi K3.1 recipe ...", commit message: "the standalone top-16 selects
  * their experts"; the routing-weight formula is this library's convention.)
  */
@@ -121,8 +123,8 @@ route_status topk16_select(const route_plan *plan, const float *logits, int32_t 
  * route_step: the whole route step (a1..a4) for the plan's rows, same
  * arguments and results as latent_router_forward followed by topk16_select.
  * Decode plans run it as two kernels: the weight stream, then one that
- * finishes the split-K sums and runs the top-16 on the router logits while
- * they are still in shared memory.
+ * finishes the split-K sums and runs the top-16 on the router logits it has
+ * just summed, without reading them back.
  */
 route_status route_step(const route_plan *plan, const void *hidden, const void *W_latent,
                         const void *W_router, void *latent, float *logits, int32_t *ids,
@@ -230,8 +232,8 @@ route_status route_set_latent_ksplit(route_plan *plan, int enable);
 
 /*
  * route_test_stall: TEST HOOK for the bounded-wait path, not for production.
- * With enable != 0, each CTA of the plan's projection kernel skips its last
- * weight copy, so its MMA warp waits for data that never arrives; after
+ * With enable != 0, each CTA of the plan's projection kernel skips a copy of
+ * its last k-block, so its MMA warp waits for data that never arrives; after
  * timeout_ns the wait gives up, the kernel sets the device status word, drains
  * its in-flight work, frees its tensor memory and returns, and
  * route_device_status() then reports ROUTE_ERR_DEVICE_TIMEOUT.  enable == 0
