@@ -59,3 +59,22 @@ def test_reference_arm_runs_on_rank_zero_only():
                        timeout=120)
     assert p.returncode == 0, p.stderr[-2000:]
     assert p.stdout.strip() == ""
+
+
+def test_recorded_traffic_only_for_the_profiled_sources(tmp_path, monkeypatch):
+    """roofline.traffic comes from the committed ncu summary only while the
+    kernel's sources hash to the value recorded with it; otherwise null."""
+    sys.path.insert(0, ROOT)
+    import bench
+    sha = bench.kernel_source_sha("decode_stream_kernel")
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_sha", lambda k: sha)
+    rec = {"decode_stream_kernel:decode_r8": {"dram_bytes_per_launch": 123, "source_sha": sha}}
+    (prof / "traffic.json").write_text(json.dumps(rec))
+    assert bench.recorded_traffic("decode_stream_kernel", "decode_r8") == 123.0
+    assert bench.recorded_traffic("decode_stream_kernel", "decode_r1") is None
+    rec["decode_stream_kernel:decode_r8"]["source_sha"] = "0" * 16
+    (prof / "traffic.json").write_text(json.dumps(rec))
+    assert bench.recorded_traffic("decode_stream_kernel", "decode_r8") is None
