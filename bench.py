@@ -54,7 +54,7 @@ _CSRC = "latent_projection_top_gb300/csrc/"
 # figure stands only while these files are unchanged
 KERNEL_SOURCES = {
     "decode_stream_kernel": [_CSRC + f for f in ("decode_kernel.cu", "topk16.cuh", "sm103_ptx.cuh",
-                                                 "common.cuh")],
+                                                 "common.cuh", "twofloat.cuh")],
     "prefill_pair_kernel": [_CSRC + f for f in ("prefill_kernel.cu", "sm103_ptx.cuh", "common.cuh")],
 }
 
