@@ -104,3 +104,32 @@ def test_binding_refuses_to_run_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(route, "_lib", None)
     with pytest.raises(route.RouteError):
         route.lib()
+
+
+def test_binding_checks_tensors_before_any_call():
+    """The binding's marshalling: wrong device, dtype, shape or layout raise
+    before any C entry point runs (a stand-in plan object is enough)."""
+    import torch
+
+    class FakePlan:
+        rows, device, mode = 4, 0, route.DECODE
+        handle = None
+
+    p = FakePlan()
+    cpu = torch.zeros((4, route.K_HIDDEN), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="must be on cuda:0"):
+        route._proj_ptrs(p, cpu, cpu, cpu, cpu, cpu)
+    with pytest.raises(TypeError, match="must be a torch.Tensor"):
+        route._dev_tensor([1, 2], "hidden", (4, route.K_HIDDEN), route._bf16_types(), 0)
+    # host tensors: dtype, shape and contiguity
+    h = torch.zeros((4, route.K_HIDDEN), dtype=torch.bfloat16)
+    assert route._host_tensor(h, "hidden_host", (4, route.K_HIDDEN), route._bf16_types()).value
+    with pytest.raises(TypeError, match="dtype"):
+        route._host_tensor(h.float(), "hidden_host", (4, route.K_HIDDEN), route._bf16_types())
+    with pytest.raises(ValueError, match="contiguous with shape"):
+        route._host_tensor(h[:2], "hidden_host", (4, route.K_HIDDEN), route._bf16_types())
+    with pytest.raises(ValueError, match="contiguous with shape"):
+        route._host_tensor(torch.zeros((route.K_HIDDEN, 4), dtype=torch.bfloat16).t(),
+                           "hidden_host", (4, route.K_HIDDEN), route._bf16_types())
+    with pytest.raises(TypeError, match="CPU torch.Tensor"):
+        route._host_tensor(None, "hidden_host", (4, route.K_HIDDEN), route._bf16_types())
