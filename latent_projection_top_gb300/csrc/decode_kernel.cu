@@ -69,7 +69,7 @@ struct DecCfg {
     static constexpr uint32_t kStageBytes = kDAStageBytes + kBStageBytes;
     static constexpr int kStages = 4;  // measured: 4 (and 3) beat 5 and 6 under back-to-back steps
     static constexpr uint32_t kAccCols = 2 * BN;       // two 128-column blocks per accumulator
-    // TMEM columns: kNumAcc accumulators (k-blocks in flight), then the
+    // TMEM columns: kNumAcc accumulators (k-block pairs in flight), then the
     // running sums, per column block BN hi columns and BN lo columns.
     static constexpr int kNumAcc = BN == 16 ? 8 : 6;
     static constexpr uint32_t kStateCol = kNumAcc * kAccCols;
@@ -102,8 +102,8 @@ __device__ __forceinline__ uint16_t bf16_bits(float x) {
 }
 
 // One chunk of W rows (TMEM columns r0 .. r0+W-1) of the epilogue: add the
-// k-block result at `acc` into the running two-float sums at s_hi / s_lo
-// (or start them, on the first k-block of a run); at the end of a run store
+// k-block pair's result at `acc` into the running two-float sums at s_hi /
+// s_lo (or start them, on the first pair of a run); at the end of a run store
 // the sums for rows < `rows` to `out` instead.  `release` frees the
 // accumulator once its columns are in registers.
 template <int W>
@@ -117,7 +117,7 @@ __device__ __forceinline__ void epi_chunk(uint32_t acc, uint32_t s_hi, uint32_t 
         ptx::tmem_ld(s_lo + r0, l);
     }
     ptx::tmem_ld_wait();
-    if (release) {  // the accumulator is free for the next k-block
+    if (release) {  // the accumulator is free for the next pair
         ptx::tc_fence_before();
         ptx::mbar_arrive(accempty);
     }
@@ -325,7 +325,7 @@ __global__ void __maxnreg__(BN == 16 ? 72 : 80)
             wait_drain(drain_bar, 0u, args);
         }
     } else {
-        // ---------------- epilogue: two-float sums of the k-block results ----------------
+        // ---------------- epilogue: two-float sums of the k-block pairs' results ----------------
         const int quarter = warp & 3;        // TMEM lanes 32*quarter .. +31
         const int blk = (warp - 2) >> 2;     // column block 0 or 1 of the tile
         const int col = blk * 128 + 32 * quarter + lane;
