@@ -71,8 +71,8 @@ static_assert(kWordSsCount + kDecodeMaxRows <= kWords, "word area");
 // (measured: the finish kernel's partial sums took 2.8 us instead of 0.8),
 // and the dependency resolves that much later.  So without overlap the
 // first weight boxes go out this long after the CTA starts (measured best
-// among 0.5 .. 4 us at 1, 8 and 20 rows).  Not after the staging kernel of
-// the host-buffer path, which ends sooner than that.
+// among 0.5 .. 4 us at 1, 8 and 20 rows).  Not after the host-buffer path's
+// copy in (its staging kernel ends sooner than that).
 constexpr unsigned kPrefetchHoldNs = 1000;
 
 struct DecodeArgs {
