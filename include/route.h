@@ -243,6 +243,15 @@ route_status route_set_latent_ksplit(route_plan *plan, int enable);
 route_status route_test_stall(route_plan *plan, int enable, uint64_t timeout_ns);
 
 /*
+ * route_test_poison_scratch: TEST HOOK.  Fill the plan's split-K scratch (the
+ * partials and the sum-of-squares parts, not the arrival counters) with 0xFF
+ * bytes on `stream`, so that a test can show that no launch reads a partial
+ * it did not write first.  Prefill plans keep no partials: a no-op.
+ * Capturable in a CUDA graph.
+ */
+route_status route_test_poison_scratch(const route_plan *plan, void *stream);
+
+/*
  * route_step_decode_noalloc: the decode route step (route_step for 1..20
  * rows) without a plan and without allocating any memory.  The pages have no
  * counterpart; this exists for callers that cannot allocate device memory:

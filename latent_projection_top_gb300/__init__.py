@@ -53,7 +53,7 @@ EXPORTS = (
     "route_plan_grid", "route_plan_segments", "route_last_error", "route_test_stall",
     "route_set_overlap", "route_step_decode_noalloc", "route_step_sumsq",
     "route_set_latent_ksplit", "route_host_step_create", "route_host_step_run",
-    "route_host_step_destroy",
+    "route_host_step_destroy", "route_test_poison_scratch",
 )
 
 
@@ -99,7 +99,9 @@ def lib() -> ctypes.CDLL:
         L.route_host_step_create.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(vp)]
         L.route_host_step_run.argtypes = [vp]
         L.route_host_step_destroy.argtypes = [vp]
-        for f in ("route_host_step_create", "route_host_step_run", "route_host_step_destroy"):
+        L.route_test_poison_scratch.argtypes = [vp, vp]
+        for f in ("route_host_step_create", "route_host_step_run", "route_host_step_destroy",
+                  "route_test_poison_scratch"):
             getattr(L, f).restype = i32
         for f in ("route_plan_rows", "route_plan_mode", "route_plan_grid", "route_plan_segments"):
             getattr(L, f).argtypes = [vp]
@@ -376,6 +378,11 @@ def route_test_stall(plan: Plan, enable: bool, timeout_ns: int = 1_000_000) -> N
     """Test hook: make the plan's projection kernel wait for a copy that never
     comes, so that its bounded wait expires (see include/route.h)."""
     _check(lib().route_test_stall(plan.handle, int(bool(enable)), int(timeout_ns)))
+
+
+def route_test_poison_scratch(plan: Plan, stream=None) -> None:
+    """Test hook: fill the plan's split-K scratch with 0xFF bytes (include/route.h)."""
+    _check(lib().route_test_poison_scratch(plan.handle, _stream(stream, plan.device)))
 
 
 def route_device_status(plan: Plan) -> None:

@@ -26,6 +26,7 @@ struct route_plan {
     ProjArgs pre;             // prefill launch arguments (per-call pointers added at launch)
     DecodeArgs dec;           // decode launch arguments, incl. the split-K partition
     float2 *ws;               // decode split-K partials, then the sum-of-squares parts
+    size_t ws_bytes;          // both
     unsigned *words;          // device status word (+ spare)
     uint8_t *staging;         // device staging for route_step_host
     size_t staging_bytes;
@@ -454,6 +455,7 @@ route_status route_prepare(int mode, int rows, int device, route_plan **out) {
         decode_partition(a, decode_grid(sms, kMaxGrid), &p->segments);
         const size_t ws_bytes = (size_t)p->segments * kDecodeMaxRows * kDTileCols * sizeof(float2);
         const size_t ss_bytes = (size_t)kDecodeMaxRows * kDLatTiles * sizeof(float2);
+        p->ws_bytes = ws_bytes + ss_bytes;
         if ((e = cudaMalloc(&p->ws, ws_bytes + ss_bytes)) != cudaSuccess) {
             free_plan(p);
             return cuda_fail(e, "cudaMalloc(split-K scratch)");
@@ -763,6 +765,17 @@ route_status route_test_stall(route_plan *plan, int enable, uint64_t timeout_ns)
     plan->pre.test_stall = plan->dec.test_stall = enable ? 1 : 0;
     plan->pre.timeout_ns = plan->dec.timeout_ns = t;
     return ROUTE_OK;
+}
+
+route_status route_test_poison_scratch(const route_plan *plan, void *stream) {
+    route_status st = check_plan(plan);
+    if (st != ROUTE_OK) return st;
+    if (!plan->ws) return ROUTE_OK;  // prefill plans keep no partials
+    DeviceGuard guard(plan->device);
+    if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+    const cudaError_t e =
+        cudaMemsetAsync(plan->ws, 0xFF, plan->ws_bytes, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ROUTE_OK : cuda_fail(e, "poison the scratch");
 }
 
 route_status route_step_decode_noalloc(int rows, const void *hidden, const void *W_latent,

@@ -94,6 +94,7 @@ def test_calls_with_null_plan(lib):
     assert lib.route_host_step_create(null, x, x, x, x, x, x, x, None, ctypes.byref(out)) == 3
     assert lib.route_host_step_run(null) == 3
     assert lib.route_host_step_destroy(null) == 0
+    assert lib.route_test_poison_scratch(null, None) == 3
     assert lib.route_destroy(null) == 0
     for f in ("route_plan_rows", "route_plan_mode", "route_plan_grid", "route_plan_segments"):
         assert getattr(lib, f)(null) == -1

@@ -199,6 +199,62 @@ def test_bank_cycling_under_graph_replay(mode, rows, workload, overlap):
             assert np.array_equal(o[3].cpu().numpy().view(np.uint32), e[3].view(np.uint32))
 
 
+def _guarded(shape, dtype, guard=4096):
+    """An output tensor inside a byte buffer with `guard` canary bytes (0xA5)
+    on each side; returns (tensor, buffer, nbytes)."""
+    n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+    buf = torch.full((guard + n + guard,), 0xA5, dtype=torch.uint8, device=DEV)
+    return buf[guard:guard + n].view(dtype).view(shape), buf, n
+
+
+@pytest.mark.parametrize("rows", [8, 20])
+def test_decode_replays_poisoned_scratch_and_canaries(rows):
+    """Robustness under replay: every step's split-K scratch is filled with
+    0xFF bytes before it runs (inside the captured graph), outputs are
+    poisoned before every replay, the bank changes every step, and each of
+    200 replays must give the eager bits (compared on the device) without
+    touching 4 KB of canary bytes on either side of every output."""
+    banks = [bank("decode_sweep", b) for b in range(3)]
+    dev = [(to_dev_bf16(np.resize(h, (rows, h.shape[1]))), to_dev_bf16(wl), to_dev_bf16(wr))
+           for h, wl, wr in banks]
+    with route.Plan(route.DECODE, rows) as plan:
+        want = []
+        for d in dev:
+            lat, lg, ids, w = outputs(rows)
+            ss = torch.empty((rows,), dtype=torch.float32, device=DEV)
+            route.route_step_sumsq(plan, *d, lat, lg, ids, w, ss)
+            want.append((lat, lg, ids, w, ss))
+        torch.cuda.synchronize()
+        shapes = [((rows, route.N_LATENT), torch.bfloat16), ((rows, route.N_EXPERTS), torch.float32),
+                  ((rows, route.TOPK), torch.int32), ((rows, route.TOPK), torch.float32),
+                  ((rows,), torch.float32)]
+        outs = [[_guarded(sh, dt) for sh, dt in shapes] for _ in dev]
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for d, o in zip(dev, outs):
+                    route.route_test_poison_scratch(plan, stream=s)
+                    route.route_step_sumsq(plan, *d, *[t for t, _, _ in o], stream=s)
+        torch.cuda.synchronize()
+        bad = 0
+        for _ in range(200):
+            for o in outs:
+                for t, _, _ in o:
+                    t.view(torch.uint8).fill_(0xFF)  # NaN / -1 everywhere
+            g.replay()
+            for o, ref in zip(outs, want):
+                for (t, _, _), r in zip(o, ref):
+                    bad += int(not torch.equal(t.view(torch.uint8), r.view(torch.uint8)))
+        torch.cuda.synchronize()
+        route.route_device_status(plan)
+        assert bad == 0, f"{bad} output tensors differed from the eager bits"
+        for o in outs:
+            for _, buf, n in o:
+                assert bool((buf[:4096] == 0xA5).all()) and bool((buf[4096 + n:] == 0xA5).all())
+
+
 # ------------------------------------------------------------------- prefill
 
 @pytest.mark.parametrize("rows,sample", [(1, None), (40, None), (256, (0, 100, 255)),
