@@ -364,3 +364,25 @@ def test_sumsq_against_exact_rationals(N):
     for r in range(4):
         exact = sum(Fraction(float(x)) ** 2 for x in v[r].view(np.float32))
         assert got[r] == _f32_nearest_even(exact), r
+
+
+def test_ksplit_hand_computed_slice_boundary():
+    """K-split latent on a hand-computed row: slice 0 (k < 896) holds the
+    partial 1 + 2^-8 + 2^-10, slice 1 (896 <= k < 1792) the partial -2^-9.
+    General path: bf16(1 + 2^-8 + 2^-10) = 1 + 2^-7, plus -2^-9 gives
+    1 + 2^-8 + 2^-9, which rounds to 1 + 2^-7.  Full K: the exact sum
+    1 + 2^-8 - 2^-10 rounds to 1.  Slices of another width, or partials not
+    rounded to BF16, give 1."""
+    K, N = 7168, 2
+    h = np.zeros((1, K), np.float32)
+    h[0, [893, 894, 895, 896]] = 1.0
+    W = np.zeros((K, N), np.float32)
+    W[893, 0], W[894, 0], W[895, 0], W[896, 0] = 1.0, 2.0 ** -8, 2.0 ** -10, -(2.0 ** -9)
+    W[895, 1] = 3.0  # column 1: one product, same in both paths
+    hb, Wb = torch_bf16_bits(h), torch_bf16_bits(W)
+    split = oracle.bf16_to_f64(oracle.latent_ksplit(hb, Wb, 8))
+    full, _, _, _ = oracle.latent_router(hb, Wb, np.zeros((K, 896), np.uint16))
+    full = oracle.bf16_to_f64(full)
+    assert split[0, 0] == 1.0 + 2.0 ** -7
+    assert full[0, 0] == 1.0
+    assert split[0, 1] == full[0, 1] == 3.0
