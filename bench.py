@@ -179,6 +179,75 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": n_in}
 
 
+class NvmlClocks:
+    """In-process, read-only NVML queries of the SM clock and the active
+    clock-event reasons, polled every millisecond: nvidia-smi samples every
+    100 ms at best, which can miss a timed region of a fraction of a
+    millisecond altogether.  Nothing is set; unavailable NVML reads as None."""
+
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap"}
+
+    def __init__(self, index: int):
+        import ctypes
+        self.ok = False
+        self.samples = []
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h)) != 0:
+                return
+            self.lib, self.h, self.ct = lib, h, ctypes
+            fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.reasons_fn = fn
+            self.max_mhz = self._clock(lib.nvmlDeviceGetMaxClockInfo)
+            self.ok = True
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def _clock(self, fn):
+        v = self.ct.c_uint()
+        return v.value if fn(self.h, self.ct.c_uint(1), self.ct.byref(v)) == 0 else None  # 1 = SM
+
+    def read(self):
+        if not self.ok:
+            return None
+        r = self.ct.c_ulonglong()
+        reasons = r.value if self.reasons_fn(self.h, self.ct.byref(r)) == 0 else 0
+        return (self._clock(self.lib.nvmlDeviceGetClockInfo), reasons)
+
+    def start(self):
+        self.stop_flag = False
+        if self.ok:
+            self.samples.append(self.read())
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+        return self
+
+    def _poll(self):
+        while not self.stop_flag:
+            self.samples.append(self.read())
+            time.sleep(0.001)
+
+    def stop(self):
+        self.stop_flag = True
+        if not self.ok:
+            return None
+        self.thread.join(timeout=1)
+        self.samples.append(self.read())
+        sm = [s[0] for s in self.samples if s and s[0]]
+        bits = 0
+        for s in self.samples:
+            if s:
+                bits |= s[1]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(n for b, n in self.REASONS.items() if bits & b),
+                "samples": len(self.samples), "source": "NVML (in process, read only), 1 ms poll"}
+
+
 # ----------------------------------------------------------- distributed
 
 class Dist:
@@ -304,8 +373,16 @@ class RouteBench:
                 torch.empty((rows, route.TOPK), dtype=torch.float32, device=self.dev))
 
     def make_steps(self, workload: str, rows: int, nbanks: int, gemm_only: bool = False,
-                   overlap: bool = False, sumsq: bool = False, ksplit: bool = False):
-        """Closures, one per bank, each enqueuing one layer's route step."""
+                   overlap: bool = False, sumsq: bool = False, ksplit: bool = False,
+                   producer: str | None = None):
+        """Closures, one per bank, each enqueuing one layer's route step.
+
+        producer="before": each step is preceded on the stream by a plain
+        copy kernel (torch's) that writes the step's hidden rows from a
+        source buffer -- a stand-in for the norm that precedes routing in a
+        model; it triggers no programmatic launch, so the route step starts
+        only once it has finished.  producer="alone": the copies only (their
+        time is subtracted from the pair's)."""
         route = self.route
         mode = route.DECODE if workload.startswith("decode") else route.PREFILL
         plan = route.Plan(mode, rows, self.device)
@@ -318,7 +395,16 @@ class RouteBench:
         outs = [self.outputs(rows) for _ in range(nbanks)]
         steps = []
         for (wl, wr), h, o in zip(banks, hs, outs):
-            if gemm_only:
+            if producer is not None:
+                dst = self.torch.empty_like(h)
+                if producer == "alone":
+                    steps.append(lambda s, h=h, dst=dst: dst.copy_(h))
+                else:
+                    def step(s, h=h, dst=dst, wl=wl, wr=wr, o=o):
+                        dst.copy_(h)
+                        route.route_step(plan, dst, wl, wr, *o, stream=s)
+                    steps.append(step)
+            elif gemm_only:
                 steps.append(lambda s, h=h, wl=wl, wr=wr, o=o:
                              route.latent_router_forward(plan, h, wl, wr, o[0], o[1], stream=s))
             elif sumsq:
@@ -330,6 +416,40 @@ class RouteBench:
                              route.route_step(plan, h, wl, wr, *o, stream=s))
         launches = 1 if (mode == route.PREFILL and gemm_only) else 2
         return plan, steps, launches
+
+    def spread(self, steps, runs: int = 5, replays: int = 200, graph_len: int = GRAPH_LEN,
+               warm_replays: int = 20, dist=None):
+        """The timing method of the decode page ("Kimi K3.1 recipe ...",
+        commit message): `runs` runs of `replays` replays of a graph of
+        `graph_len` layer steps.  Returns the per-step time of each run (us)."""
+        with guarded(f"spread {runs}x{replays}"):
+            torch = self.torch
+            s = torch.cuda.Stream(device=self.dev)
+            s.wait_stream(torch.cuda.current_stream(self.dev))
+            g = self.graph(steps, graph_len, 0, s)
+            torch.cuda.synchronize(self.dev)
+            with torch.cuda.stream(s):
+                for _ in range(warm_replays):
+                    g.replay()
+            torch.cuda.synchronize(self.dev)
+            out = []
+            for _ in range(runs):
+                if dist is not None:
+                    dist.barrier()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(s):
+                    e0.record(s)
+                    for _ in range(replays):
+                        g.replay()
+                    e1.record(s)
+                e1.synchronize()
+                ms = e0.elapsed_time(e1)
+                if dist is not None:
+                    ms = dist.max(ms)
+                out.append(ms * 1e3 / (replays * graph_len))
+            del g
+            return out
 
     def per_layer_us(self, steps, dist):
         """One chunk launched eagerly with an event between consecutive layers:
@@ -380,6 +500,7 @@ class RouteBench:
         g_wrem = self.graph(steps, w_rem, 0, s) if w_rem else None
         torch.cuda.synchronize(self.dev)
         sampler = ClockSampler(sampler_index).start() if sampler_index is not None else None
+        nvml = NvmlClocks(sampler_index) if sampler_index is not None else None
         with torch.cuda.stream(s):
             for _ in range(w_full):
                 g_full.replay()
@@ -391,6 +512,8 @@ class RouteBench:
         torch.cuda.synchronize(self.dev)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
+        if nvml is not None:
+            nvml.start()
         t0 = time.time()
         with torch.cuda.stream(s):
             e0.record(s)
@@ -402,9 +525,15 @@ class RouteBench:
         e1.synchronize()
         torch.cuda.synchronize(self.dev)
         t1 = time.time()
+        nv = nvml.stop() if nvml is not None else None
         if dist is not None:
             dist.barrier()
         clocks = sampler.stop(t0, t1) if sampler is not None else None
+        if clocks is not None and not clocks.get("samples") and nv is not None:
+            # a timed region shorter than nvidia-smi's sampling interval
+            nv["note"] = (f"timed region {1e3 * (t1 - t0):.2f} ms is shorter than nvidia-smi's "
+                          "100 ms sampling interval; clocks from in-process NVML reads")
+            clocks = nv
         return e0.elapsed_time(e1), clocks
 
     def e2e(self, workload: str, rows: int, k: int, dist):
@@ -481,6 +610,39 @@ def oracle_rows_per_s(workload: str, rows: int, budget_s: float = 10.0):
                       f"{t:.1f} s, single-threaded float64 C"}
 
 
+def oracle_rows_per_s_all_cores(workload: str, rows: int, budget_s: float = 10.0):
+    """A second CPU figure, labelled apart from `cpu_baseline`: the same
+    single-threaded oracle run as independent whole layer steps on every host
+    core at once (one thread per core; each ctypes call releases the
+    interpreter lock), rows of all threads over the wall time."""
+    import oracle
+    import synth
+    from concurrent.futures import ThreadPoolExecutor
+    wk = synth.WORKLOADS[workload]
+    hid = wk.hidden(0, rows)
+    wl, wr = synth.weight_bank(wk.seed, 0)
+    oracle.build()
+    cores = os.cpu_count() or 1
+    t0 = time.perf_counter()
+
+    def worker(_):
+        n = 0
+        while True:
+            _, lg, _, _ = oracle.latent_router(hid, wl, wr)
+            oracle.topk(lg)
+            n += 1
+            if time.perf_counter() - t0 >= budget_s:
+                return n
+
+    with ThreadPoolExecutor(cores) as ex:
+        steps = sum(ex.map(worker, range(cores)))
+    t = time.perf_counter() - t0
+    return {"value": round(steps * rows / t, 3), "unit": "rows/s", "cores": cores,
+            "kind": "oracle, all cores",
+            "sample": f"{steps} full layer steps of {rows} rows of {workload} (bank 0) on "
+                      f"{cores} threads, {t:.1f} s wall"}
+
+
 def main_ours(args):
     import torch
     dist = Dist()
@@ -544,13 +706,17 @@ def main_ours(args):
                       "parallelism": f"replicas x{dist.world} (no sharding, no collectives)"},
            "roofline": roof, "clocks": clocks, "gpu_launches": launches * args.steps}
 
+    # the same configuration timed the decode page's way: median (min, max)
+    # over 5 runs of many graph replays (steady state, no pipeline fill)
+    sp = DECODE_SPREAD if decode else PREFILL_SPREAD
+    out["spread"] = dict(summarise(rb.spread(steps, dist=dist, **sp)), method=SPREAD_METHOD)
     if overlap:
         # the same workload with each step held behind the previous one's tail
         p3, s3, _ = rb.make_steps(wk, rows, nbanks, overlap=False)
-        n3 = min(args.steps, 64 * 256)
-        ms3, _ = rb.run(s3, n3, args.warmup, dist, **({} if decode else {"graph_len": 92}))
-        t3 = dist.max(ms3) / 1e3 / n3
-        out["without_overlap"] = {"us_per_layer": round(t3 * 1e6, 3),
+        sm = summarise(rb.spread(s3, dist=dist, **sp))
+        rb.route.route_device_status(p3)
+        t3 = sm["median"] / 1e6
+        out["without_overlap"] = {"us_per_layer": sm["median"], "us_spread": sm,
                                   "rows_per_s": round(dist.world * rows / t3, 1)}
         if decode:
             algo = WEIGHT_BYTES + rows * ROW_BYTES
@@ -559,13 +725,31 @@ def main_ours(args):
     if not args.no_e2e:
         out["e2e"] = rb.e2e(wk, rows, min(args.steps, 4096), dist)
     if not args.no_sweep:
+        smp = ClockSampler(dev).start()
+        t0 = time.time()
         out["sweep"] = sweep(rb, dist, peaks, args)
+        out["sweep_clocks"] = smp.stop(t0, time.time())
+        out["sweep_method"] = SPREAD_METHOD
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu:
         out["cpu_baseline"] = oracle_rows_per_s(wk, rows)
+        out["cpu_all_cores"] = oracle_rows_per_s_all_cores(wk, rows)
     plan.close()
     if dist.rank == 0:
         print(json.dumps(out), flush=True)
     dist.close()
+
+
+def summarise(us):
+    """median / min / max of per-run per-layer times (us)."""
+    srt = sorted(us)
+    return {"median": round(statistics.median(srt), 3), "min": round(srt[0], 3),
+            "max": round(srt[-1], 3), "runs": len(srt)}
+
+
+DECODE_SPREAD = dict(runs=5, replays=200, graph_len=GRAPH_LEN)
+PREFILL_SPREAD = dict(runs=5, replays=10, graph_len=92)
+SPREAD_METHOD = ("per-layer us: median (min, max) over 5 runs; decode: 200 replays of a "
+                 "64-layer graph per run, prefill: 10 replays of a 92-layer graph per run")
 
 
 def sweep(rb, dist, peaks, args):
@@ -576,33 +760,53 @@ def sweep(rb, dist, peaks, args):
         entry = {"workload": wk, "rows": rows, "bound": "hbm"}
         for ov in (True, False):
             plan, steps, _ = rb.make_steps(wk, rows, 8, overlap=ov)
-            ms, _ = rb.run(steps, 64 * 64, 64 * 8, dist)
+            sm = summarise(rb.spread(steps, dist=dist, **DECODE_SPREAD))
             rb.route.route_device_status(plan)
-            t = dist.max(ms) / 1e3 / (64 * 64)
             plan.close()
+            t = sm["median"] / 1e6
             sfx = "" if ov else "_without_overlap"
-            entry.update({"us_per_layer" + sfx: round(t * 1e6, 3),
+            entry.update({"us_per_layer" + sfx: sm["median"], "us_spread" + sfx: sm,
                           "rows_per_s" + sfx: round(rows / t, 1),
                           "achieved_gbs" + sfx: round(algo / t / 1e9, 1),
                           "frac" + sfx: round(algo / t / 1e9 / peaks["hbm_gbs"], 4)})
         res.append(entry)
+    # the regime of a model: each route step follows a kernel that writes its
+    # hidden rows and does not trigger a programmatic launch (overlap off)
+    for wk, rows in [("decode_r1", 1), ("decode_r8", 8), ("decode_sweep", 12),
+                     ("decode_sweep", 16), ("decode_sweep", 20)]:
+        algo = WEIGHT_BYTES + rows * ROW_BYTES
+        plan, pair, _ = rb.make_steps(wk, rows, 8, producer="before")
+        us_pair = summarise(rb.spread(pair, dist=dist, **DECODE_SPREAD))
+        rb.route.route_device_status(plan)
+        plan.close()
+        p2, alone, _ = rb.make_steps(wk, rows, 8, producer="alone")
+        us_prod = summarise(rb.spread(alone, dist=dist, **DECODE_SPREAD))
+        p2.close()
+        t = (us_pair["median"] - us_prod["median"]) / 1e6
+        res.append({"workload": wk, "rows": rows, "bound": "hbm",
+                    "regime": "after a producer kernel (copy of the hidden rows, no programmatic "
+                              "launch trigger), overlap off",
+                    "us_per_layer": round(t * 1e6, 3), "rows_per_s": round(rows / t, 1),
+                    "frac": round(algo / t / 1e9 / peaks["hbm_gbs"], 4),
+                    "us_producer_and_step": us_pair, "us_producer_alone": us_prod,
+                    "note": "us_per_layer = median(producer + step) - median(producer alone)"})
     for wk, rows in [("prefill_r1024", 1024), ("prefill_r3072", 3072)]:
         nb = args.prefill_banks
         flop = FLOP_PER_ROW * rows
         e = {"workload": wk, "rows": rows, "bound": "tensor", "weight_banks": nb}
         for ov in (True, False):
             plan, steps, _ = rb.make_steps(wk, rows, nb, overlap=ov)
-            ms, _ = rb.run(steps, 92 * 5, 92 * 2, dist, graph_len=92)
-            t = dist.max(ms) / 1e3 / (92 * 5)
+            st = summarise(rb.spread(steps, dist=dist, **PREFILL_SPREAD))
             p2, gsteps, _ = rb.make_steps(wk, rows, nb, gemm_only=True, overlap=ov)
-            gms, _ = rb.run(gsteps, 92 * 5, 92 * 2, dist, graph_len=92)
+            gm = summarise(rb.spread(gsteps, dist=dist, **PREFILL_SPREAD))
             rb.route.route_device_status(plan)
             rb.route.route_device_status(p2)
-            tg = dist.max(gms) / 1e3 / (92 * 5)
+            t, tg = st["median"] / 1e6, gm["median"] / 1e6
             sfx = "" if ov else "_without_overlap"
-            e.update({"us_per_layer" + sfx: round(t * 1e6, 3),
+            e.update({"us_per_layer" + sfx: st["median"], "us_spread" + sfx: st,
                       "chunk_ms_92_layers" + sfx: round(t * 92 * 1e3, 3),
-                      "rows_per_s" + sfx: round(rows / t, 1), "gemm_us" + sfx: round(tg * 1e6, 3),
+                      "rows_per_s" + sfx: round(rows / t, 1), "gemm_us" + sfx: gm["median"],
+                      "gemm_us_spread" + sfx: gm,
                       "gemm_tflops" + sfx: round(flop / tg / 1e12, 1),
                       "frac" + sfx: round(flop / tg / 1e12 / peaks["bf16_tflops"], 4)})
             if rows == 3072 and ov:
@@ -610,39 +814,29 @@ def sweep(rb, dist, peaks, args):
             plan.close()
             p2.close()
         res.append(e)
-    # the route step that also returns each latent row's sum of squares
-    for wk, rows, ov in [("decode_r8", 8, True), ("decode_sweep", 20, True),
-                         ("prefill_r3072", 3072, False)]:
-        decode = wk.startswith("decode")
-        nb = 8 if decode else args.prefill_banks
-        plan, steps, _ = rb.make_steps(wk, rows, nb, overlap=ov, sumsq=True)
-        n, w, gl = (64 * 64, 64 * 8, 64) if decode else (92 * 5, 92 * 2, 92)
-        ms, _ = rb.run(steps, n, w, dist, graph_len=gl)
-        rb.route.route_device_status(plan)
-        t = dist.max(ms) / 1e3 / n
-        plan.close()
-        e = {"workload": wk, "rows": rows, "call": "route_step_sumsq", "overlap": ov,
-             "us_per_layer": round(t * 1e6, 3), "rows_per_s": round(rows / t, 1)}
-        if decode:
-            algo = WEIGHT_BYTES + rows * (ROW_BYTES + 4)
-            e.update({"bound": "hbm", "frac": round(algo / t / 1e9 / peaks["hbm_gbs"], 4)})
-        res.append(e)
+    # the route step that also returns each latent row's sum of squares, and
     # the step with the general path's K-split latent arithmetic
-    for wk, rows in [("decode_r8", 8), ("decode_sweep", 20), ("prefill_r3072", 3072)]:
-        decode = wk.startswith("decode")
-        nb = 8 if decode else args.prefill_banks
-        plan, steps, _ = rb.make_steps(wk, rows, nb, overlap=decode, ksplit=True)
-        n, w, gl = (64 * 64, 64 * 8, 64) if decode else (92 * 5, 92 * 2, 92)
-        ms, _ = rb.run(steps, n, w, dist, graph_len=gl)
-        rb.route.route_device_status(plan)
-        t = dist.max(ms) / 1e3 / n
-        plan.close()
-        e = {"workload": wk, "rows": rows, "latent": "k-split (8 BF16 partials)",
-             "overlap": decode, "us_per_layer": round(t * 1e6, 3), "rows_per_s": round(rows / t, 1)}
-        if decode:
-            algo = WEIGHT_BYTES + rows * ROW_BYTES
-            e.update({"bound": "hbm", "frac": round(algo / t / 1e9 / peaks["hbm_gbs"], 4)})
-        res.append(e)
+    variants = [dict(sumsq=True), dict(ksplit=True)]
+    for var in variants:
+        for wk, rows in [("decode_r8", 8), ("decode_sweep", 20), ("prefill_r3072", 3072)]:
+            decode = wk.startswith("decode")
+            nb = 8 if decode else args.prefill_banks
+            ov = decode
+            plan, steps, _ = rb.make_steps(wk, rows, nb, overlap=ov, **var)
+            sm = summarise(rb.spread(steps, dist=dist, **(DECODE_SPREAD if decode else PREFILL_SPREAD)))
+            rb.route.route_device_status(plan)
+            plan.close()
+            t = sm["median"] / 1e6
+            e = {"workload": wk, "rows": rows, "overlap": ov, "us_per_layer": sm["median"],
+                 "us_spread": sm, "rows_per_s": round(rows / t, 1)}
+            if var.get("sumsq"):
+                e["call"] = "route_step_sumsq"
+            else:
+                e["latent"] = "k-split (8 BF16 partials)"
+            if decode:
+                algo = WEIGHT_BYTES + rows * (ROW_BYTES + (4 if var.get("sumsq") else 0))
+                e.update({"bound": "hbm", "frac": round(algo / t / 1e9 / peaks["hbm_gbs"], 4)})
+            res.append(e)
     return res
 
 

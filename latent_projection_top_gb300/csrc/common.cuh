@@ -29,26 +29,44 @@ static_assert(kKBlocks % kKSplitSlices == 0, "K slices of whole k-blocks");
 // columns.
 constexpr int kPrefillBN = 256;
 constexpr int kPrefillColTiles = 18;
-constexpr int kPrefillHiddenBoxRows = 128;
-constexpr int kProjThreads = 192;                           // 6 warps
+constexpr int kPrefillLatTiles = 14;
+constexpr int kPrefillHiddenBoxRows = 64;
+constexpr int kProjThreads = 320;                           // 10 warps
 
 enum Mode : int { kDecode = 0, kPrefill = 1 };
 
 // Device status bits (the kernels set them instead of hanging).
 constexpr unsigned kStatusTimeout = 1u;
 
+// Prefill work is a list of tiles per CTA pair, built on the host.  A tile
+// is 256 weight columns (one column tile c: 0..13 latent, 14..17 router) by
+// the token rows from row0 on:
+//   full -- 256 rows, one FP32 accumulation over the whole K;
+//   K-split half -- 128 rows of a latent column tile, eight 896-deep K slices
+//     whose results are rounded to BF16 and added in FP32 (the general
+//     path's latent).
+// Packed into one int: row0 (a multiple of 128) + 32 * kind + c.
+enum PrefillTileKind : int { kTileFull = 0, kTileKsplitHalf = 2 };
+__host__ __device__ constexpr int pack_tile(int c, int kind, int row0) { return row0 + 32 * kind + c; }
+__host__ __device__ constexpr int tile_col(int t) { return t & 31; }
+__host__ __device__ constexpr int tile_kind(int t) { return (t >> 5) & 3; }
+__host__ __device__ constexpr int tile_row0(int t) { return t & ~127; }
+
+// Per-row latent sum-of-squares parts written by the prefill epilogue: one
+// per (latent column tile, CTA of the pair, 32-column warp group).
+constexpr int kSsParts = kPrefillLatTiles * 2 * 4;          // 112
+
 // Everything the prefill projection kernel needs besides its tensor maps.
 struct ProjArgs {
     int rows;            // token rows in this call
-    int row_tiles;       // ceil(rows / kPrefillBN)
     int grid;            // persistent CTAs launched (pairs of CTAs: even)
     int test_stall;      // test hook: skip each CTA's last copy so a wait must time out
-    int ksplit;          // latent with the general path's K-split arithmetic
     int overlap;         // read hidden before the grid dependency resolves
     unsigned long long timeout_ns;  // bound on every wait inside the kernel
     unsigned *status;          // device status word
-    uint16_t *latent;          // [rows, 3584] BF16 bits
-    float *logits;             // [rows, 896]
+    const int *sched;          // packed tiles of every pair, pair after pair
+    const int *sched_off;      // pair p's tiles: sched[sched_off[p] .. sched_off[p + 1])
+    float2 *ss_part;           // optional [rows][kSsParts] latent sum-of-squares parts (hi, lo)
 };
 
 // Decode split-K: 18 column tiles of 256 columns (14 latent, 4 router -- the
@@ -102,8 +120,11 @@ struct DecodeArgs {
 // programmatic dependent launch (see the kernels for what each waits on).
 int prefill_smem_bytes();
 cudaError_t prefill_configure();
+// map_lat / map_lg: store maps of the latent [rows, 3584] BF16 and the logits
+// [rows, 896] FP32 with 32-column x 16-row boxes.
 cudaError_t prefill_launch(const CUtensorMap &map_h, const CUtensorMap &map_wl,
-                           const CUtensorMap &map_wr, const ProjArgs &args, cudaStream_t stream);
+                           const CUtensorMap &map_wr, const CUtensorMap &map_lat,
+                           const CUtensorMap &map_lg, const ProjArgs &args, cudaStream_t stream);
 
 int decode_bn_for(int rows);
 int decode_smem_bytes(int bn);
@@ -118,8 +139,9 @@ cudaError_t decode_launch(int bn, const CUtensorMap &map_h, const CUtensorMap &m
 cudaError_t stage_in_launch(const void *src_mapped, void *dst, size_t bytes, cudaStream_t stream);
 
 // The top-16 of each row; with `sumsq` non-null also the row's latent sum
-// of squares (read from `latent`, which the same predecessor wrote).
+// of squares (the sum of its kSsParts parts in `ss_part`, which the same
+// predecessor wrote).
 cudaError_t topk_launch(const float *logits, int rows, int32_t *ids, float *weights,
-                        const uint16_t *latent, float *sumsq, cudaStream_t stream);
+                        const float2 *ss_part, float *sumsq, cudaStream_t stream);
 
 }  // namespace route

@@ -4,42 +4,46 @@
 //   latent[r, n] = bf16( sum_k hidden[r, k] * W_latent[k, n] )   n < 3584
 //   logits[r, e] =       sum_k hidden[r, k] * W_router[k, e]    e < 896
 //
-// Each output is one FP32-accumulated dot product over the full K = 7168,
-// rounded once ("Optionally gather the Kimi3 prefill latent instead of
+// Each latent value is one FP32-accumulated dot product over the full K =
+// 7168, rounded once ("Optionally gather the Kimi3 prefill latent instead of
 // reducing it", Description, Numerics and Compile bullets: at prefill the
 // projection is a dense M = rows, K = 7168 GEMM); the two projections share
 // the hidden operand and run as one N = 3584 + 896 problem.
 //
 // The weights are [K, N] with N contiguous, so their tensor-core operand is
-// MN-major.  A tile is 256 weight columns (the MMA's M) by 256 token rows
-// (its N), computed by a cluster of two CTAs with tcgen05.mma.cta_group::2:
-// each CTA stages its half of the weight columns (A, 128 x 64 per k-block)
-// and its half of the token rows (B, 128 x 64), and holds its 128 weight
-// columns x 256 token rows of the FP32 accumulator in its own TMEM.  Against
-// one CTA per 128 x 256 tile this moves a third fewer bytes from L2 per
-// flop and leaves room for a 6-stage ring.
+// MN-major.  A tile is 256 weight columns (the MMA's M) by 256 or 128 token
+// rows (its N), computed by a cluster of two CTAs with
+// tcgen05.mma.cta_group::2: each CTA stages its 128 weight columns (A) and
+// its half of the token rows (B) per 64-deep k-block, and holds its 128
+// weight columns x N token rows of the FP32 accumulator in its own TMEM.
 //
-// Warp roles (192 threads, persistent, one CTA per SM, pairs = clusters):
-//   warp 0      TMA producer (both CTAs): its halves into a 6-stage ring;
-//               completion is counted on the leader CTA's barrier, which the
-//               leader arms for both CTAs' bytes before either may fill the
-//               stage (so its transaction count never goes below zero)
+// Tile kinds (the host builds each pair's list; see common.cuh):
+//   full (256 rows): one accumulation over the whole K; the epilogue stores
+//     the latent (rounded to BF16, with per-row sum-of-squares parts when
+//     asked) or the FP32 router logits.
+//   K-split half (latent, 128 rows): the general path's eight 896-deep K
+//     slices (same page, Numerics bullet and commit body), each rounded to
+//     BF16 and added in FP32 in slice order.
+// Every job accumulates into an aligned pair of TMEM quarters (a full tile's
+// 256 columns, or two slices of a K-split tile in 128 columns each), and the
+// pairs {0,1} and {2,3} alternate, so one job is drained while the next is
+// computed.  A K-split tile's running sums stay in registers.
+//
+// Warp roles (320 threads, persistent, one CTA per SM, pairs = clusters):
+//   warp 0      TMA producer (both CTAs); completion is counted on the leader
+//               CTA's barrier, which the leader arms for both CTAs' bytes
+//               before either may fill the stage
 //   warp 1      TMEM owner (both CTAs); the leader's lane 0 issues the MMAs
 //               and re-arms each stage's barrier once it has consumed it
-//   warps 2..5  epilogue (both CTAs): TMEM -> registers -> global
-// Pairs walk the (row tile, column tile) grid with stride = number of pairs;
-// two TMEM accumulators let one tile's epilogue overlap the next main loop.
-//
-// With the general path's K-split latent (args.ksplit), a latent tile runs as
-// eight jobs of 14 k-blocks into one accumulator; the epilogue rounds each
-// slice's partial to BF16 and adds it in FP32 to a running sum kept in the
-// other half of TMEM, rounding and storing after the eighth.
+//   warps 2..9  epilogue (both CTAs): warp w reads TMEM lanes 32 (w % 4) ..
+//               +31 and half of the tile's token rows; results go through a
+//               small shared-memory buffer per warp and out with TMA stores
+//               (32 columns x 16 rows per store).
 //
 // Programmatic dependent launch: weight boxes of the first stages are
 // requested before `griddepcontrol.wait` (no predecessor writes the weights);
 // outputs are written only after it, and hidden rows are read only after it
-// too unless `overlap` is set (then the main loop runs under the previous
-// step's top-16).
+// too unless `overlap` is set.
 //
 // Every wait is bounded: after args.timeout_ns a waiting thread sets the
 // device status word and the CTA's abort flag, in-flight copies and MMAs are
@@ -50,31 +54,38 @@
 
 #include "common.cuh"
 #include "sm103_ptx.cuh"
+#include "twofloat.cuh"
 
 namespace route {
 namespace {
 
-constexpr uint32_t kABoxBytes = 64 * 64 * 2;               // 64 columns x 64 k, BF16
-constexpr int kHalf = 128;                                 // each CTA's share of M and of N
-constexpr int kPairCols = 2 * kHalf;                       // weight columns per tile (M)
-constexpr int kPairRows = kPrefillBN;                      // token rows per tile (N)
-constexpr uint32_t kBHalfBytes = kHalf * 128;              // 128 token rows x 64 k
-constexpr uint32_t kAHalfBytes = 2 * kABoxBytes;           // 128 weight columns x 64 k
-constexpr uint32_t kStageBytes = kBHalfBytes + kAHalfBytes;  // B half first, then A half
+constexpr uint32_t kBoxBytes = 64 * 64 * 2;                // 64 x 64 BF16 box
+constexpr int kHalf = 128;                                 // each CTA's weight columns
+constexpr uint32_t kBBytes = 2 * kBoxBytes;                // up to 128 token rows x 64 k
+constexpr uint32_t kABytes = 2 * kBoxBytes;                // 128 weight columns x 64 k
+constexpr uint32_t kStageBytes = kBBytes + kABytes;        // B first, then A
 constexpr int kStages = 6;
-constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + 256;
-constexpr uint32_t kTmemCols = 512;                        // two accumulators of 256 columns
-constexpr int kLatPairTiles = kLatent / kPairCols;         // 14
-constexpr int kPairColTiles = kLatPairTiles + (kExperts + kPairCols - 1) / kPairCols;  // 18
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr uint32_t kStoreBufBytes = 16 * 32 * 4;           // 16 rows x 32 columns, up to FP32
+constexpr uint32_t kStoreBytes = kEpiWarps * 2 * kStoreBufBytes;
+constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + kStoreBytes + 256;
+constexpr uint32_t kTmemCols = 512;                        // four quarters of 128 columns
+constexpr int kKsplitJobs = kKSplitSlices / 2;                    // 4 jobs of two slices
+
 // tcgen05 instruction descriptor, kind::f16: FP32 accumulator, BF16 A and B,
-// A MN-major (transposed), B K-major, N = 256, M = 256 (over the pair).
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) |
-                            ((uint32_t)(kPairRows >> 3) << 17) | ((uint32_t)(kPairCols >> 4) << 24);
-static_assert(kPairColTiles == kPrefillColTiles, "column tiles");
-static_assert(kHalf == kPrefillHiddenBoxRows, "hidden box");
+// A MN-major (transposed), B K-major, M = 256 (over the pair), N = n.
+constexpr uint32_t idesc_for(int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(2 * kHalf >> 4) << 24);
+}
+constexpr uint32_t kIdescFull = idesc_for(kPrefillBN);
+constexpr uint32_t kIdescHalf = idesc_for(kPrefillBN / 2);
+static_assert(kProjThreads == 64 + kEpiThreads, "warp roles");
+static_assert(kHalf == 2 * kPrefillHiddenBoxRows, "two hidden boxes per CTA and full tile");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
-static_assert(8 * (2 * kStages + 5) <= 256, "barrier area");
-static_assert(kLatent % kPairCols == 0, "latent tiles");
+static_assert(8 * (2 * kStages + 9) <= 256, "barrier area");
+static_assert(kLatent == kPrefillLatTiles * 2 * kHalf, "latent tiles");
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand tile.
 // lbo / sbo are the leading / stride byte offsets of the canonical layout.
@@ -87,22 +98,11 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
     return d;
 }
 
-struct Tile {
-    int c;   // column tile: 0..13 latent, 14..17 router (the last has 128 real columns)
-    int rt;  // row tile
-};
+__device__ __forceinline__ int tile_jobs(int kind) { return kind == kTileFull ? 1 : kKsplitJobs; }
 
-__device__ __forceinline__ int tiles_of_pair(const ProjArgs &a, int pair, int npairs) {
-    const int tiles = kPairColTiles * a.row_tiles;
-    return pair < tiles ? (tiles - 1 - pair) / npairs + 1 : 0;
-}
-
-// Tiles in row-major order: the pairs at work at one time share a few
-// 256-row blocks of hidden and read every weight tile (measured 117 us
-// against 128 us at 3072 rows for column-major order).
-__device__ __forceinline__ Tile tile_get(const ProjArgs &a, int pair, int npairs, int i) {
-    const int t = pair + i * npairs;
-    return Tile{t % kPairColTiles, t / kPairColTiles};
+// Transaction bytes of one stage of a tile of this kind, both CTAs.
+__device__ __forceinline__ uint32_t stage_tx(int kind) {
+    return 2u * (kABytes + (kind == kTileFull ? kBBytes : kBoxBytes));
 }
 
 // Bounded wait for the completion of phase `parity` of `bar` (acquire at
@@ -139,10 +139,16 @@ __device__ __forceinline__ uint16_t bf16_bits(float x) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
 
+__device__ __forceinline__ float bf16_round(float x) {
+    return __uint_as_float((uint32_t)bf16_bits(x) << 16);
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap map_h,
                         const __grid_constant__ CUtensorMap map_wl,
                         const __grid_constant__ CUtensorMap map_wr,
+                        const __grid_constant__ CUtensorMap map_lat,
+                        const __grid_constant__ CUtensorMap map_lg,
                         const __grid_constant__ ProjArgs args) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t s_tmem_base;
@@ -152,20 +158,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
     // one names the same operand or barrier in the other.
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
-    const uint32_t bars = sbase + kStages * kStageBytes;
+    const uint32_t store_base = sbase + kStages * kStageBytes;
+    const uint32_t bars = store_base + kStoreBytes;
     auto full_bar = [&](int s) { return bars + 8u * s; };                 // leader's are used
     auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
-    auto accfull_bar = [&](int b) { return bars + 8u * (2 * kStages + b); };
-    auto accempty_bar = [&](int b) { return bars + 8u * (2 * kStages + 2 + b); };  // leader's
-    const uint32_t drain_bar = bars + 8u * (2 * kStages + 4);
+    auto qfull_bar = [&](int q) { return bars + 8u * (2 * kStages + q); };
+    auto qempty_bar = [&](int q) { return bars + 8u * (2 * kStages + 4 + q); };  // leader's
+    const uint32_t drain_bar = bars + 8u * (2 * kStages + 8);
 
     const uint32_t rank = ptx::cluster_ctarank();
     const bool leader = rank == 0u;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int pair = blockIdx.x >> 1;
-    const int npairs = gridDim.x >> 1;
-    const int nseg = tiles_of_pair(args, pair, npairs);
+    const int* const sched = args.sched + args.sched_off[pair];
+    const int ntiles = args.sched_off[pair + 1] - args.sched_off[pair];
+    const int total = ntiles * kKBlocks;
 
     if (threadIdx.x == 0) {
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -174,19 +182,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
             ptx::mbar_init(full_bar(s), 1);
             ptx::mbar_init(empty_bar(s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            ptx::mbar_init(accfull_bar(b), 1);
-            ptx::mbar_init(accempty_bar(b), 2);  // one arrival from each CTA's epilogue
+        for (int q = 0; q < 4; ++q) {
+            ptx::mbar_init(qfull_bar(q), 1);
+            ptx::mbar_init(qempty_bar(q), 2 * kEpiWarps);  // each epilogue warp of both CTAs
         }
         ptx::mbar_init(drain_bar, 1);
         // the leader arms the first round of every stage that will be filled
-        const int first = nseg * kKBlocks < kStages ? nseg * kKBlocks : kStages;
-        if (leader)
-            for (int s = 0; s < first; ++s) ptx::mbar_arrive_expect_tx(full_bar(s), 2 * kStageBytes);
+        // (all of them belong to the pair's first tile)
+        const int first = total < kStages ? total : kStages;
+        if (leader && ntiles > 0)
+            for (int s = 0; s < first; ++s)
+                ptx::mbar_arrive_expect_tx(full_bar(s), stage_tx(tile_kind(sched[0])));
         ptx::fence_barrier_init();
         ptx::prefetch_tensormap(&map_h);
         ptx::prefetch_tensormap(&map_wl);
         ptx::prefetch_tensormap(&map_wr);
+        ptx::prefetch_tensormap(&map_lat);
+        ptx::prefetch_tensormap(&map_lg);
     }
     if (warp == 1) {
         ptx::tmem_alloc_pair(ptx::smem_addr(&s_tmem_base), kTmemCols);
@@ -203,23 +215,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
             const uint64_t pol_w = ptx::policy_evict_normal();
             const uint64_t pol_h = ptx::policy_evict_last();
             uint32_t armed = 0u, armed_par = 0u;  // leader: stages armed / their phase parity
-            const int total = nseg * kKBlocks;
             const int n_pre = total < kStages ? total : kStages;
             auto weights_of = [&](int it, uint32_t st, uint32_t bar) {
-                const Tile tl = tile_get(args, pair, npairs, it / kKBlocks);
+                const int t = sched[it / kKBlocks];
                 const int kb = it % kKBlocks;
-                const bool lat = tl.c < kLatPairTiles;
+                const int c = tile_col(t);
+                const bool lat = c < kPrefillLatTiles;
                 const CUtensorMap *wmap = lat ? &map_wl : &map_wr;
                 // this CTA's 128 columns; past column 896 of W_router TMA fills zeros
-                const int x0 = (lat ? tl.c : tl.c - kLatPairTiles) * kPairCols + (int)rank * kHalf;
-                ptx::tma_load_2d_pair(st + kBHalfBytes, wmap, bar, x0, kb * kKBlock, pol_w);
-                ptx::tma_load_2d_pair(st + kBHalfBytes + kABoxBytes, wmap, bar, x0 + 64,
-                                      kb * kKBlock, pol_w);
+                const int x0 = (lat ? c : c - kPrefillLatTiles) * 2 * kHalf + (int)rank * kHalf;
+                ptx::tma_load_2d_pair(st + kBBytes, wmap, bar, x0, kb * kKBlock, pol_w);
+                ptx::tma_load_2d_pair(st + kBBytes + kBoxBytes, wmap, bar, x0 + 64, kb * kKBlock,
+                                      pol_w);
             };
             auto hidden_of = [&](int it, uint32_t st, uint32_t bar) {
-                const Tile tl = tile_get(args, pair, npairs, it / kKBlocks);
-                ptx::tma_load_2d_pair(st, &map_h, bar, (it % kKBlocks) * kKBlock,
-                                      tl.rt * kPairRows + (int)rank * kHalf, pol_h);
+                const int t = sched[it / kKBlocks];
+                const int k0 = (it % kKBlocks) * kKBlock;
+                if (tile_kind(t) == kTileFull) {  // this CTA's 128 of the tile's 256 rows
+                    const int y0 = tile_row0(t) + (int)rank * kHalf;
+                    ptx::tma_load_2d_pair(st, &map_h, bar, k0, y0, pol_h);
+                    ptx::tma_load_2d_pair(st + kBoxBytes, &map_h, bar, k0, y0 + 64, pol_h);
+                } else {                          // this CTA's 64 of the tile's 128 rows
+                    ptx::tma_load_2d_pair(st, &map_h, bar, k0, tile_row0(t) + (int)rank * 64, pol_h);
+                }
             };
             // Weight boxes of the first stages go out before the grid
             // dependency resolves (no predecessor writes the weights).
@@ -258,31 +276,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             // ---------------- MMA issuer (leader CTA) ----------------
-            uint32_t it = 0, job = 0;
+            uint32_t occ = 0u;  // bit q: parity of the occupations of TMEM quarter q so far
+            auto acquire = [&](int q) {
+                const bool r = wait_phase(qempty_bar(q), ((occ >> q) & 1u) ^ 1u, args, &s_abort);
+                occ ^= 1u << q;
+                return r;
+            };
+            int it = 0, job = 0;
             bool ok = true;
-            for (int i = 0; i < nseg && ok; ++i) {
-                const Tile tl = tile_get(args, pair, npairs, i);
-                const int njobs = (args.ksplit && tl.c < kLatPairTiles) ? kKSplitSlices : 1;
-                const int kb_per_job = kKBlocks / njobs;
+            for (int i = 0; i < ntiles && ok; ++i) {
+                const int kind = tile_kind(sched[i]);
+                const bool full = kind == kTileFull;
+                const int njobs = tile_jobs(kind);
+                const int kbpj = kKBlocks / njobs;        // k-blocks of one job
+                const int kbpa = full ? kbpj : kbpj / 2;  // k-blocks of one accumulator
                 for (int j = 0; j < njobs && ok; ++j, ++job) {
-                    const int buf = args.ksplit ? 0 : (int)(job & 1u);
-                    const uint32_t use = args.ksplit ? job : (job >> 1);
-                    if (!wait_phase(accempty_bar(buf), (use & 1u) ^ 1u, args, &s_abort)) {
+                    const int q = 2 * (job & 1);
+                    if (!(acquire(q) && acquire(q + 1))) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kPairRows);
-                    for (int kb = 0; kb < kb_per_job; ++kb, ++it) {
-                        const int s = (int)(it % kStages);
-                        const uint32_t ph = (it / kStages) & 1u;
+                    const uint32_t idesc = full ? kIdescFull : kIdescHalf;
+                    for (int kb = 0; kb < kbpj; ++kb, ++it) {
+                        const int s = it % kStages;
+                        const uint32_t ph = (uint32_t)(it / kStages) & 1u;
                         if (!wait_phase(full_bar(s), ph, args, &s_abort)) {
                             ok = false;
                             break;
                         }
                         ptx::tc_fence_after();
+                        // a half tile's second accumulator starts half-way through the job
+                        const uint32_t d_tmem = tmem_base + (uint32_t)(128 * q + (kb >= kbpa ? 128 : 0));
+                        const int kba = kb % kbpa;  // k-block within this accumulator
                         const uint32_t b = sbase + s * kStageBytes;
-                        const uint32_t a = b + kBHalfBytes;
+                        const uint32_t a = b + kBBytes;
 #pragma unroll
                         for (int kk = 0; kk < kKBlock / 16; ++kk) {
                             // A: k advances 16 rows = two 8-row swizzle atoms (2048 B);
@@ -290,109 +318,171 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
                             //    8-row k groups 1024 B apart (SBO).
                             // B: k advances 32 B inside the 128-byte swizzled row;
                             //    8-row groups of token rows are 1024 B apart (SBO).
-                            const uint64_t da = smem_desc(a + kk * 2048u, kABoxBytes, 1024u);
+                            const uint64_t da = smem_desc(a + kk * 2048u, kBoxBytes, 1024u);
                             const uint64_t db = smem_desc(b + kk * 32u, 16u, 1024u);
-                            ptx::mma_bf16_pair(d_tmem, da, db, kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                            ptx::mma_bf16_pair(d_tmem, da, db, idesc, (kba > 0 || kk > 0) ? 1u : 0u);
                         }
                         // re-arm stage s for its next round before it is freed:
                         // the copies that fill it can only start after the commit
-                        if (it + kStages < (uint32_t)(nseg * kKBlocks))
-                            ptx::mbar_arrive_expect_tx(full_bar(s), 2 * kStageBytes);
+                        if (it + kStages < total)
+                            ptx::mbar_arrive_expect_tx(
+                                full_bar(s), stage_tx(tile_kind(sched[(it + kStages) / kKBlocks])));
                         ptx::mma_commit_pair(empty_bar(s), 0x3);  // frees stage s in both CTAs
                     }
-                    if (ok) ptx::mma_commit_pair(accfull_bar(buf), 0x3);
+                    if (ok) ptx::mma_commit_pair(qfull_bar(q), 0x3);
                 }
             }
             ptx::mma_commit_pair(drain_bar, 0x3);  // every MMA retired before TMEM is freed
             wait_drain(drain_bar, 0u, args);
         }
     } else {
-        // ---------------- epilogue (warps 2..5, both CTAs) ----------------
-        const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
-        const int col = 32 * quarter + lane;
+        // ---------------- epilogue (warps 2..9, both CTAs) ----------------
+        const int lq = warp & 3;            // TMEM lanes 32*lq .. +31 = this CTA's weight columns
+        const int cs = (warp - 2) >> 2;     // which half of the tile's token rows
         const int rows = args.rows;
+        const uint32_t lanes = tmem_base + ((uint32_t)(32 * lq) << 16);
+        uint8_t *const store_gen = smem_raw + (store_base - raw) + (warp - 2) * 2 * kStoreBufBytes;
+        const uint32_t store_sh = store_base + (warp - 2) * 2 * kStoreBufBytes;
+        int sb = 0;
+        uint32_t qc = 0u;  // bit q: parity of the completions of quarter q consumed
+        int job = 0;       // jobs so far: job j accumulates in quarters 2 (j & 1) and 2 (j & 1) + 1
         asm volatile("griddepcontrol.wait;" ::: "memory");  // outputs may still be read by the predecessor
-        uint32_t job = 0;
+
+        // Stage 16 rows of this warp's 32 columns and send them out with one
+        // TMA store (rows past `rows` and columns past the map are not written).
+        auto store_chunk = [&](const uint32_t (&v)[16], bool fp32, const CUtensorMap *map, int x,
+                               int y, bool valid) {
+            if (lane == 0) ptx::bulk_wait_group_read<1>();  // this buffer's last store has read it
+            __syncwarp();
+            uint8_t *buf = store_gen + sb * kStoreBufBytes;
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+                if (fp32)
+                    reinterpret_cast<uint32_t *>(buf)[jj * 32 + lane] = v[jj];
+                else
+                    reinterpret_cast<uint16_t *>(buf)[jj * 32 + lane] = (uint16_t)v[jj];
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                if (valid && y < rows) ptx::tma_store_2d(map, store_sh + sb * kStoreBufBytes, x, y);
+                // one group per chunk, empty when nothing is stored, so that
+                // "at most one group pending" always means this buffer is free
+                ptx::bulk_commit_group();
+            }
+            sb ^= 1;
+        };
+        // Per-row sum of squares of the 32 BF16 values of this warp (exact
+        // squares, a fixed warp tree of two-floats): one part per row.
+        auto sumsq_parts = [&](const uint32_t (&b)[16], int part, int y) {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+                const float f = __uint_as_float(b[jj] << 16);
+                float hi = f * f, lo = 0.f;
+                warp_two_sum(hi, lo);
+                if (lane == 0 && y + jj < rows)
+                    args.ss_part[(size_t)(y + jj) * kSsParts + part] = make_float2(hi, lo);
+            }
+        };
+        // This warp is done reading quarter q (one of the 16 arrivals the
+        // leader's barrier counts: every epilogue warp of both CTAs).
+        auto release = [&](int q) {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader)
+                    ptx::mbar_arrive(qempty_bar(q));
+                else
+                    ptx::mbar_arrive_remote(ptx::map_to_rank(qempty_bar(q), 0u));
+            }
+        };
+        auto wait_full = [&](int q) {
+            const bool ok = wait_phase(qfull_bar(q), (qc >> q) & 1u, args, &s_abort);
+            qc ^= 1u << q;
+            __syncwarp();  // the TMEM loads that follow are warp-wide (.sync.aligned)
+            ptx::tc_fence_after();
+            return ok;
+        };
         bool go = true;
-        for (int i = 0; i < nseg && go; ++i) {
-            const Tile tl = tile_get(args, pair, npairs, i);
-            const bool lat = tl.c < kLatPairTiles;
-            const int njobs = (args.ksplit && lat) ? kKSplitSlices : 1;
-            const int ncol = (lat ? tl.c : tl.c - kLatPairTiles) * kPairCols + (int)rank * kHalf + col;
-            const bool valid = lat || ncol < kExperts;
-            for (int j = 0; j < njobs; ++j, ++job) {
-                const int buf = args.ksplit ? 0 : (int)(job & 1u);
-                const uint32_t use = args.ksplit ? job : (job >> 1);
-                const bool ok = wait_phase(accfull_bar(buf), use & 1u, args, &s_abort);
-                if (!ptx::named_bar_and(1, 128, ok)) {
+        for (int i = 0; i < ntiles && go; ++i) {
+            const int t = sched[i];
+            const int c = tile_col(t), kind = tile_kind(t), row0 = tile_row0(t);
+            const bool lat = c < kPrefillLatTiles;
+            // global column of lane 0 of this warp
+            const int xw = (lat ? c : c - kPrefillLatTiles) * 2 * kHalf + (int)rank * kHalf + 32 * lq;
+            const bool valid = lat || xw < kExperts;
+            const int part = c * 8 + (int)rank * 4 + lq;
+            if (kind == kTileFull) {
+                const int q = 2 * (job++ & 1);
+                if (!wait_full(q)) {
                     go = false;
                     break;
                 }
-                __syncwarp();  // the TMEM loads below are warp-wide (.sync.aligned)
-                ptx::tc_fence_after();
-                const uint32_t lanes = tmem_base + ((uint32_t)(32 * quarter) << 16);
-                const uint32_t taddr = lanes + (uint32_t)(buf * kPairRows);
-                if (njobs == 1) {
+                const uint32_t acc = lanes + (uint32_t)(128 * q + 128 * cs);  // token rows 128 cs ..
 #pragma unroll 1
-                    for (int ch = 0; ch < kPairRows / 16; ++ch) {
-                        uint32_t u[16];
-                        ptx::tmem_ld_x16(taddr + ch * 16, u);
-                        ptx::tmem_ld_wait();
-                        const int r0 = tl.rt * kPairRows + ch * 16;
-#pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) {
-                            const int r = r0 + jj;
-                            if (valid && r < rows) {
-                                const float x = __uint_as_float(u[jj]);
-                                if (lat)
-                                    args.latent[(size_t)r * kLatent + ncol] = bf16_bits(x);
-                                else
-                                    args.logits[(size_t)r * kExperts + ncol] = x;
-                            }
-                        }
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint32_t u[16];
+                    ptx::tmem_ld_x16(acc + 16 * ch, u);
+                    ptx::tmem_ld_wait();
+                    if (ch == 7) {  // every column of the accumulator is in registers
+                        release(q);
+                        release(q + 1);
                     }
-                } else {
-                    // K-split latent: slice j's partial, rounded to BF16, is
-                    // added in FP32 to the running sum kept in the other half
-                    // of TMEM; the last slice rounds the sum to BF16 and stores.
-                    const uint32_t tsum = lanes + (uint32_t)kPairRows;
-                    const bool last = j == njobs - 1;
-#pragma unroll 1
-                    for (int ch = 0; ch < kPairRows / 16; ++ch) {
-                        uint32_t u[16], acc[16];
-                        ptx::tmem_ld_x16(taddr + ch * 16, u);
-                        if (j > 0) ptx::tmem_ld_x16(tsum + ch * 16, acc);
-                        ptx::tmem_ld_wait();
+                    const int y = row0 + 128 * cs + 16 * ch;
+                    if (lat) {
 #pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) {
-                            const float part = __uint_as_float((uint32_t)bf16_bits(__uint_as_float(u[jj])) << 16);
-                            acc[jj] = __float_as_uint(j > 0 ? __uint_as_float(acc[jj]) + part : part);
-                        }
-                        if (!last) {
-                            ptx::tmem_st_x16(tsum + ch * 16, acc);
-                        } else {
-                            const int r0 = tl.rt * kPairRows + ch * 16;
-#pragma unroll
-                            for (int jj = 0; jj < 16; ++jj)
-                                if (r0 + jj < rows)
-                                    args.latent[(size_t)(r0 + jj) * kLatent + ncol] =
-                                        bf16_bits(__uint_as_float(acc[jj]));
-                        }
+                        for (int jj = 0; jj < 16; ++jj) u[jj] = bf16_bits(__uint_as_float(u[jj]));
+                        store_chunk(u, false, &map_lat, xw, y, true);
+                        if (args.ss_part != nullptr) sumsq_parts(u, part, y);
+                    } else {
+                        store_chunk(u, true, &map_lg, xw, y, valid);
                     }
-                    if (!last) ptx::tmem_st_wait();  // the next slice reads these sums back
                 }
-                // all 128 epilogue threads are done with this accumulator: one
-                // arrival from this CTA on the leader's barrier
-                ptx::tc_fence_before();
-                ptx::named_bar_sync(2, 128);
-                if (threadIdx.x == 64) {
-                    if (leader)
-                        ptx::mbar_arrive(accempty_bar(buf));
-                    else
-                        ptx::mbar_arrive_remote(ptx::map_to_rank(accempty_bar(buf), 0u));
+            } else {
+                // The K-split sums of this warp's 64 token rows, in registers:
+                // the BF16-rounded slice partials added in FP32 in slice order.
+                float sum[64];
+#pragma unroll 1
+                for (int j = 0; j < kKsplitJobs; ++j) {
+                    const int q = 2 * (job++ & 1);
+                    if (!wait_full(q)) {
+                        go = false;
+                        break;
+                    }
+                    const uint32_t acc = lanes + (uint32_t)(128 * q + 64 * cs);  // token rows 64 cs ..
+#pragma unroll
+                    for (int hh = 0; hh < 4; ++hh) {  // slices 2j and 2j + 1, 16 rows at a time
+                        uint32_t u[16], v[16];
+                        ptx::tmem_ld_x16(acc + 16 * hh, u);
+                        ptx::tmem_ld_x16(acc + 128 + 16 * hh, v);
+                        ptx::tmem_ld_wait();
+                        if (hh == 3) {
+                            release(q);
+                            release(q + 1);
+                        }
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int x = 16 * hh + e;
+                            const float p0 = bf16_round(__uint_as_float(u[e]));
+                            const float p1 = bf16_round(__uint_as_float(v[e]));
+                            sum[x] = (j == 0 ? p0 : sum[x] + p0) + p1;
+                        }
+                    }
+                }
+                if (!go) break;
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t v[16];
+                    const int y = row0 + 64 * cs + 16 * ch;
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) v[jj] = bf16_bits(sum[16 * ch + jj]);
+                    store_chunk(v, false, &map_lat, xw, y, true);
+                    if (args.ss_part != nullptr) sumsq_parts(v, part, y);
                 }
             }
         }
+        if (lane == 0) ptx::bulk_wait_group_all();  // every store has left shared memory
+        __syncwarp();
     }
 
     ptx::tc_fence_before();
@@ -417,7 +507,8 @@ cudaError_t prefill_configure() {
 }
 
 cudaError_t prefill_launch(const CUtensorMap &map_h, const CUtensorMap &map_wl,
-                           const CUtensorMap &map_wr, const ProjArgs &args, cudaStream_t stream) {
+                           const CUtensorMap &map_wr, const CUtensorMap &map_lat,
+                           const CUtensorMap &map_lg, const ProjArgs &args, cudaStream_t stream) {
     if (args.grid <= 0 || args.grid % 2 != 0) return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t c = {};
     cudaLaunchAttribute attr[1];
@@ -429,7 +520,7 @@ cudaError_t prefill_launch(const CUtensorMap &map_h, const CUtensorMap &map_wl,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     c.attrs = attr;
     c.numAttrs = 1;
-    return cudaLaunchKernelEx(&c, prefill_pair_kernel, map_h, map_wl, map_wr, args);
+    return cudaLaunchKernelEx(&c, prefill_pair_kernel, map_h, map_wl, map_wr, map_lat, map_lg, args);
 }
 
 }  // namespace route

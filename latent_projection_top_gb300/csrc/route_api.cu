@@ -10,6 +10,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <vector>
 
 #include "common.cuh"
 #include "route.h"
@@ -25,8 +26,13 @@ struct route_plan {
     int segments;
     ProjArgs pre;             // prefill launch arguments (per-call pointers added at launch)
     DecodeArgs dec;           // decode launch arguments, incl. the split-K partition
-    float2 *ws;               // decode split-K partials, then the sum-of-squares parts
+    float2 *ws;               // decode: split-K partials, then the sum-of-squares parts;
+                              // prefill: the per-row latent sum-of-squares parts
     size_t ws_bytes;          // both
+    int *sched;               // prefill: the pairs' tile lists (device), plain and K-split
+    const int *sched_tiles[2], *sched_off[2];  // [0] plain, [1] K-split latent
+    int sched_pairs[2];
+    int pre_ksplit;           // prefill: latent with the general path's K-split arithmetic
     unsigned *words;          // device status word (+ spare)
     uint8_t *staging;         // device staging for route_step_host
     size_t staging_bytes;
@@ -37,7 +43,7 @@ struct route_plan {
         const void *ptr = nullptr;
         CUtensorMap map;
     };
-    mutable MapCache map_h, map_wl, map_wr;
+    mutable MapCache map_h, map_wl, map_wr, map_lat, map_lg;
     route_host_step *steps = nullptr;  // prepared host steps, released with the plan
 };
 
@@ -92,18 +98,23 @@ route_status get_encode(EncodeTiledFn *out) {
     return ROUTE_OK;
 }
 
-// 2-D BF16 tensor map, 128-byte swizzle, zero fill out of bounds.
+// 2-D row-major tensor map (zero fill out of bounds): BF16 operands with
+// 128-byte swizzle for the MMA loads; for the prefill stores, BF16 or FP32
+// without swizzle.
 route_status encode_2d(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer,
-                       uint32_t box_inner, uint32_t box_outer, const char *what) {
+                       uint32_t box_inner, uint32_t box_outer, const char *what,
+                       bool fp32 = false, bool swizzle = true) {
     EncodeTiledFn enc;
     route_status st = get_encode(&enc);
     if (st != ROUTE_OK) return st;
+    const uint64_t esize = fp32 ? 4 : 2;
     cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {inner * 2};
+    cuuint64_t strides[1] = {inner * esize};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    CUresult r = enc(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                     const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(ROUTE_ERR_CUDA, "tensor map for %s rejected (CUresult %d)", what, (int)r);
     return ROUTE_OK;
@@ -141,6 +152,7 @@ void free_plan(route_plan *p) {
         h->plan = nullptr;
     }
     if (p->ws) cudaFree(p->ws);
+    if (p->sched) cudaFree(p->sched);
     if (p->words) cudaFree(p->words);
     if (p->staging) cudaFree(p->staging);
     delete p;
@@ -183,9 +195,11 @@ route_status check_plan(const route_plan *p) {
 }
 
 route_status cached_map(route_plan::MapCache &c, const void *ptr, uint64_t inner, uint64_t outer,
-                        uint32_t box_inner, uint32_t box_outer, const char *what, CUtensorMap *out) {
+                        uint32_t box_inner, uint32_t box_outer, const char *what, CUtensorMap *out,
+                        bool fp32 = false, bool swizzle = true) {
     if (c.ptr != ptr) {
-        route_status st = encode_2d(&c.map, ptr, inner, outer, box_inner, box_outer, what);
+        route_status st = encode_2d(&c.map, ptr, inner, outer, box_inner, box_outer, what, fp32,
+                                    swizzle);
         if (st != ROUTE_OK) {
             c.ptr = nullptr;
             return st;
@@ -234,15 +248,24 @@ route_status launch_forward(const route_plan *p, const void *hidden, const void 
         e = decode_launch(p->bn, mh, ml, mr, a, do_topk, stream);
         if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
     } else {
+        // the epilogue's TMA stores: 32 columns x 16 rows per box
+        CUtensorMap mlat, mlg;
+        if ((st = cached_map(p->map_lat, latent, kLatent, (uint64_t)p->rows, 32, 16, "latent", &mlat,
+                             false, false)) != ROUTE_OK ||
+            (st = cached_map(p->map_lg, logits, kExperts, (uint64_t)p->rows, 32, 16, "logits", &mlg,
+                             true, false)) != ROUTE_OK)
+            return st;
         ProjArgs a = p->pre;
-        a.latent = static_cast<uint16_t *>(latent);
-        a.logits = logits;
+        const int ks = p->pre_ksplit ? 1 : 0;
+        a.sched = p->sched_tiles[ks];
+        a.sched_off = p->sched_off[ks];
+        a.grid = 2 * p->sched_pairs[ks];
+        a.ss_part = sumsq != nullptr ? p->ws : nullptr;
         if (after_copy_in) a.overlap = 0;
-        e = prefill_launch(mh, ml, mr, a, stream);
+        e = prefill_launch(mh, ml, mr, mlat, mlg, a, stream);
         if (e != cudaSuccess) return cuda_fail(e, "prefill kernel launch");
         if (do_topk) {
-            e = topk_launch(logits, p->rows, ids, weights, static_cast<const uint16_t *>(latent),
-                            sumsq, stream);
+            e = topk_launch(logits, p->rows, ids, weights, p->ws, sumsq, stream);
             if (e != cudaSuccess) return cuda_fail(e, "top-16 kernel launch");
         }
     }
@@ -277,6 +300,52 @@ route_status run_step(const route_plan *p, const void *hidden, const void *W_lat
                       float *weights, cudaStream_t stream, float *sumsq = nullptr) {
     return launch_forward(p, hidden, W_latent, W_router, latent, logits, ids, weights, 1, sumsq,
                           stream);
+}
+
+// Prefill work lists.  The tiles of a call, in column bands: a band of B
+// column tiles over every 256-row block, then the next band, with B = the
+// pair count over the row blocks (at least 1, at most all 18), so that the
+// pairs at work at one time read few weight tiles and every hidden row block.
+// Column tiles are full tiles (256 rows); with the K-split latent, latent
+// column tiles are two half tiles of 128 rows instead (one when the second
+// would start past the last row).  Each tile goes, in that order, to the
+// pair with the least work so far (a half tile counts 11/20 of a full one:
+// half the MMAs plus its slower feed).
+void build_schedule(int rows, bool ksplit, int max_pairs, std::vector<int> &off,
+                    std::vector<int> &tiles, int *pairs) {
+    const int row_blocks = (rows + kPrefillBN - 1) / kPrefillBN;
+    int band = max_pairs / row_blocks;
+    band = band < 1 ? 1 : band > kPrefillColTiles ? kPrefillColTiles : band;
+    std::vector<int> order;
+    for (int c0 = 0; c0 < kPrefillColTiles; c0 += band)
+        for (int r = 0; r < row_blocks; ++r)
+            for (int c = c0; c < c0 + band && c < kPrefillColTiles; ++c) {
+                const int row0 = r * kPrefillBN;
+                if (c >= kPrefillLatTiles || !ksplit) {
+                    order.push_back(pack_tile(c, kTileFull, row0));
+                } else {
+                    order.push_back(pack_tile(c, kTileKsplitHalf, row0));
+                    if (row0 + kPrefillBN / 2 < rows)
+                        order.push_back(pack_tile(c, kTileKsplitHalf, row0 + kPrefillBN / 2));
+                }
+            }
+    const int np = max_pairs < (int)order.size() ? max_pairs : (int)order.size();
+    std::vector<std::vector<int>> lists(np);
+    std::vector<int> load(np, 0);
+    for (int t : order) {
+        int best = 0;
+        for (int q = 1; q < np; ++q)
+            if (load[q] < load[best]) best = q;
+        lists[best].push_back(t);
+        load[best] += tile_kind(t) == kTileFull ? 20 : 11;
+    }
+    off.assign(1, 0);
+    tiles.clear();
+    for (auto &l : lists) {
+        tiles.insert(tiles.end(), l.begin(), l.end());
+        off.push_back((int)tiles.size());
+    }
+    *pairs = np;
 }
 
 // Decode stream grid: the largest CTA count, at most one per SM and at most
@@ -468,12 +537,40 @@ route_status route_prepare(int mode, int rows, int device, route_plan **out) {
         ProjArgs &a = p->pre;
         a.rows = rows;
         a.timeout_ns = kDefaultTimeoutNs;
-        a.row_tiles = (rows + p->bn - 1) / p->bn;
-        const int tiles = kPrefillColTiles * a.row_tiles;  // tiles of a CTA pair
-        a.grid = 2 * (sms / 2 < tiles ? sms / 2 : tiles);
         a.status = p->words + kWordStatus;
-        p->segments = tiles;
-        p->grid = a.grid;
+        std::vector<int> off[2], tiles[2];
+        for (int ks = 0; ks < 2; ++ks)
+            build_schedule(rows, ks == 1, sms / 2, off[ks], tiles[ks], &p->sched_pairs[ks]);
+        size_t n = 0;
+        for (int ks = 0; ks < 2; ++ks) n += off[ks].size() + tiles[ks].size();
+        if ((e = cudaMalloc(&p->sched, n * sizeof(int))) != cudaSuccess) {
+            free_plan(p);
+            return cuda_fail(e, "cudaMalloc(prefill schedule)");
+        }
+        size_t at = 0;
+        for (int ks = 0; ks < 2 && e == cudaSuccess; ++ks) {
+            p->sched_off[ks] = p->sched + at;
+            e = cudaMemcpy(p->sched + at, off[ks].data(), off[ks].size() * sizeof(int),
+                           cudaMemcpyHostToDevice);
+            at += off[ks].size();
+            p->sched_tiles[ks] = p->sched + at;
+            if (e == cudaSuccess)
+                e = cudaMemcpy(p->sched + at, tiles[ks].data(), tiles[ks].size() * sizeof(int),
+                               cudaMemcpyHostToDevice);
+            at += tiles[ks].size();
+        }
+        if (e != cudaSuccess) {
+            free_plan(p);
+            return cuda_fail(e, "copy the prefill schedule");
+        }
+        // per-row latent sum-of-squares parts (route_step_sumsq)
+        p->ws_bytes = (size_t)rows * kSsParts * sizeof(float2);
+        if ((e = cudaMalloc(&p->ws, p->ws_bytes)) != cudaSuccess) {
+            free_plan(p);
+            return cuda_fail(e, "cudaMalloc(sum-of-squares parts)");
+        }
+        p->segments = (int)tiles[0].size();
+        p->grid = 2 * p->sched_pairs[0];
     }
     p->staging_bytes = staging_size(rows);
     if ((e = cudaMalloc(&p->staging, p->staging_bytes)) != cudaSuccess) {
@@ -737,7 +834,7 @@ route_status route_set_latent_ksplit(route_plan *plan, int enable) {
     route_status st = check_plan(plan);
     if (st != ROUTE_OK) return st;
     if (plan->mode == ROUTE_PREFILL) {  // K slices of 14 k-blocks split every prefill tile evenly
-        plan->pre.ksplit = enable ? 1 : 0;
+        plan->pre_ksplit = enable ? 1 : 0;
         return ROUTE_OK;
     }
     if (enable) {
@@ -770,7 +867,7 @@ route_status route_test_stall(route_plan *plan, int enable, uint64_t timeout_ns)
 route_status route_test_poison_scratch(const route_plan *plan, void *stream) {
     route_status st = check_plan(plan);
     if (st != ROUTE_OK) return st;
-    if (!plan->ws) return ROUTE_OK;  // prefill plans keep no partials
+    if (!plan->ws) return ROUTE_OK;
     DeviceGuard guard(plan->device);
     if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
     const cudaError_t e =

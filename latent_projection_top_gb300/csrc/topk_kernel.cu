@@ -3,11 +3,12 @@
 // decode finish kernel).  Launched with programmatic dependent launch: it
 // waits for the logits' producer before reading them.
 //
-// Optionally the same warp also reduces its row of the latent to the FP32 sum
-// of squares a following norm needs ("Optionally gather the Kimi3 prefill
-// latent instead of reducing it", Reviewer Notes): the squares of the BF16
-// values the projection stored (exact in FP32) are summed as two-floats in a
-// fixed order and rounded once.
+// Optionally the same warp also adds up its row's latent sum-of-squares
+// parts into the FP32 statistic a following norm needs ("Optionally gather
+// the Kimi3 prefill latent instead of reducing it", Reviewer Notes): the
+// projection's epilogue left one two-float part per 32 latent columns (the
+// squares of the BF16 values it stored, exact in FP32); the parts are summed
+// as two-floats in a fixed order and rounded once.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -19,37 +20,22 @@ namespace {
 
 constexpr int kRowsPerBlock = 8;
 
-// Sum of squares of one latent row (3584 BF16 values) by one warp: lane l
-// takes the 16-byte groups l, l + 32, ... in order into four two-float
-// accumulators (one per 32-bit word of a group, so that four independent
-// chains run at once), adds them in order, then a fixed tree over the lanes.
-__device__ __forceinline__ float latent_row_sumsq(const uint16_t *row, int lane) {
-    const uint4 *v = reinterpret_cast<const uint4 *>(row);
-    float hi[4] = {0.f, 0.f, 0.f, 0.f}, lo[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 2
-    for (int j = lane; j < kLatent / 8; j += 32) {
-        const uint4 q = __ldcg(v + j);
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+// Lane l adds parts l, l + 32, ... in order, then a fixed tree over the lanes.
+__device__ __forceinline__ float row_sumsq_from_parts(const float2 *parts, int lane) {
+    float hi = 0.f, lo = 0.f;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float a = __uint_as_float(w[e] << 16);          // low BF16 of the word
-            const float b = __uint_as_float(w[e] & 0xFFFF0000u);  // high BF16
-            two_sum_acc(hi[e], lo[e], a * a);
-            two_sum_acc(hi[e], lo[e], b * b);
-        }
+    for (int j = lane; j < kSsParts; j += 32) {
+        const float2 p = __ldcg(parts + j);
+        two_sum_acc(hi, lo, p.x);
+        lo += p.y;
     }
-#pragma unroll
-    for (int e = 1; e < 4; ++e) {
-        two_sum_acc(hi[0], lo[0], hi[e]);
-        lo[0] += lo[e];
-    }
-    warp_two_sum(hi[0], lo[0]);
-    return two_float_value(hi[0], lo[0]);
+    warp_two_sum(hi, lo);
+    return two_float_value(hi, lo);
 }
 
 __global__ void __launch_bounds__(32 * kRowsPerBlock)
     topk16_kernel(const float *__restrict__ logits, int rows, int32_t *__restrict__ ids,
-                  float *__restrict__ weights, const uint16_t *__restrict__ latent,
+                  float *__restrict__ weights, const float2 *__restrict__ ss_part,
                   float *__restrict__ sumsq) {
     __shared__ uint2 cand[kRowsPerBlock][kCandMax];
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -61,7 +47,7 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock)
     topk16_warp(logits + (size_t)row * kExperts, ids + (size_t)row * kTopK,
                 weights + (size_t)row * kTopK, lane, cand[warp]);
     if (sumsq != nullptr) {
-        const float ss = latent_row_sumsq(latent + (size_t)row * kLatent, lane);
+        const float ss = row_sumsq_from_parts(ss_part + (size_t)row * kSsParts, lane);
         if (lane == 0) sumsq[row] = ss;
     }
 }
@@ -69,7 +55,7 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock)
 }  // namespace
 
 cudaError_t topk_launch(const float *logits, int rows, int32_t *ids, float *weights,
-                        const uint16_t *latent, float *sumsq, cudaStream_t stream) {
+                        const float2 *ss_part, float *sumsq, cudaStream_t stream) {
     if (rows <= 0) return cudaSuccess;
     cudaLaunchConfig_t c = {};
     cudaLaunchAttribute attr[1];
@@ -80,7 +66,7 @@ cudaError_t topk_launch(const float *logits, int rows, int32_t *ids, float *weig
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     c.attrs = attr;
     c.numAttrs = 1;
-    return cudaLaunchKernelEx(&c, topk16_kernel, logits, rows, ids, weights, latent, sumsq);
+    return cudaLaunchKernelEx(&c, topk16_kernel, logits, rows, ids, weights, ss_part, sumsq);
 }
 
 }  // namespace route

@@ -4,6 +4,8 @@ through the C ABI, and a cache of oracle results (computed once per input)."""
 from __future__ import annotations
 
 import functools
+import os
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 import torch
@@ -66,12 +68,29 @@ def bank(workload: str, b: int):
     return hid, wl, wr
 
 
+def oracle_block(h, wl, wr) -> dict:
+    """The oracle (single-threaded C) on row blocks of `h`, one block per host
+    core at a time: each block is an independent oracle call (the ctypes call
+    releases the interpreter lock), and the blocks are put back in row order."""
+    from gates import abs_dot
+    h = np.ascontiguousarray(h)
+    n = h.shape[0]
+    workers = max(1, min(os.cpu_count() or 1, 32, (n + 3) // 4))
+    chunks = [c for c in np.array_split(np.arange(n), workers) if c.size]
+
+    def one(ix):
+        hh = np.ascontiguousarray(h[ix])
+        lat, lg, y_lat, y_log = oracle.latent_router(hh, wl, wr)
+        return lat, lg, y_lat, y_log, abs_dot(hh, wl), abs_dot(hh, wr)
+
+    with ThreadPoolExecutor(len(chunks)) as ex:
+        parts = list(ex.map(one, chunks))
+    keys = ("latent", "logits", "y_lat", "y_log", "abs_lat", "abs_log")
+    return {k: np.concatenate([p[i] for p in parts]) for i, k in enumerate(keys)}
+
+
 @functools.lru_cache(maxsize=16)
 def oracle_rows(workload: str, b: int, rows: tuple):
     """Oracle latent/logits (and float64 sums, sum|hw|) for the given row indices."""
     hid, wl, wr = bank(workload, b)
-    h = np.ascontiguousarray(hid[list(rows)])
-    lat, lg, y_lat, y_log = oracle.latent_router(h, wl, wr)
-    from gates import abs_dot
-    return {"latent": lat, "logits": lg, "y_lat": y_lat, "y_log": y_log,
-            "abs_lat": abs_dot(h, wl), "abs_log": abs_dot(h, wr)}
+    return oracle_block(hid[list(rows)], wl, wr)

@@ -122,28 +122,50 @@ DECODE_CASES = [("decode_r1", 1), ("decode_r8", 8), ("decode_sweep", 9), ("decod
                 ("decode_sweep", 16), ("decode_sweep", 20)]
 
 
-@pytest.mark.parametrize("workload,rows", DECODE_CASES)
-def test_decode_route_step_parity(workload, rows):
-    hid, wl, wr = bank(workload, 0)
-    ref = oracle_rows(workload, 0, tuple(range(max(synth.WORKLOADS[workload].rows))))
+def _near_tie_rows(workload, rows):
+    """Rows built as near ties at ranks 16/17 (the only rows where the GPU's
+    ids may differ from the oracle's)."""
+    wk = synth.WORKLOADS[workload]
+    return [r for r in range(rows) if wk.near_tie and r % 4 == 3]
+
+
+def _decode_parity(workload, b, rows, check_unfused=False):
+    hid, wl, wr = bank(workload, b)
+    ref = oracle_rows(workload, b, tuple(range(max(synth.WORKLOADS[workload].rows))))
     h = to_dev_bf16(hid[:rows])
     dwl, dwr = to_dev_bf16(wl), to_dev_bf16(wr)
     with route.Plan(route.DECODE, rows) as plan:
         lat, lg, ids, w = run_step(plan, h, dwl, dwr, fused=True)
-        lat2, lg2, ids2, w2 = run_step(plan, h, dwl, dwr, fused=False)
+        if check_unfused:
+            unfused = run_step(plan, h, dwl, dwr, fused=False)
     sl = slice(0, rows)
     s1 = check_latent(lat, ref["latent"][sl], ref["y_lat"][sl], ref["abs_lat"][sl])
-    s2 = check_logits(lg, ref["y_log"][sl], ref["abs_log"][sl])
+    s2 = check_logits(lg, ref["y_log"][sl], ref["abs_log"][sl], "decode")
     # the fused top-16 equals the oracle's top-16 on the same (GPU) logits
     ids_o, w_o = oracle.topk(lg)
     s3 = check_topk_exact(ids, w, ids_o, w_o)
     # end to end against the oracle's own logits
     ids_ref, _ = oracle.topk(ref["logits"][sl])
-    s4 = check_ids_end_to_end(ids, ids_ref, ref["logits"][sl], ref["y_log"][sl], ref["abs_log"][sl])
-    record(f"decode_{workload}_r{rows}", **s1, **s2, **s3, **s4)
-    # the unfused path computes the same bits
-    assert np.array_equal(lat, lat2) and np.array_equal(lg.view(np.uint32), lg2.view(np.uint32))
-    assert np.array_equal(ids, ids2) and np.array_equal(w.view(np.uint32), w2.view(np.uint32))
+    s4 = check_ids_end_to_end(ids, ids_ref, ref["logits"][sl], _near_tie_rows(workload, rows))
+    record(f"decode_{workload}_b{b}_r{rows}", **s1, **s2, **s3, **s4)
+    if check_unfused:  # the unfused path computes the same bits
+        lat2, lg2, ids2, w2 = unfused
+        assert np.array_equal(lat, lat2) and np.array_equal(lg.view(np.uint32), lg2.view(np.uint32))
+        assert np.array_equal(ids, ids2) and np.array_equal(w.view(np.uint32), w2.view(np.uint32))
+    return s4
+
+
+@pytest.mark.parametrize("workload,rows", DECODE_CASES)
+def test_decode_route_step_parity(workload, rows):
+    _decode_parity(workload, 0, rows, check_unfused=True)
+
+
+@pytest.mark.parametrize("workload,b,rows", [("decode_r8", b, 8) for b in range(1, 8)] +
+                         [("decode_sweep", b, r) for b in range(1, 6) for r in (16, 20)])
+def test_decode_parity_every_bank(workload, b, rows):
+    """Every weight bank of the 8-row workload and of the 9..20-row sweep (16
+    rows run the 16-row tile, 20 rows the 32-row one) against the oracle."""
+    _decode_parity(workload, b, rows)
 
 
 def test_decode_batch_invariance_and_determinism():
@@ -267,11 +289,11 @@ def test_prefill_ragged_parity(rows, sample):
         lat, lg, ids, w = run_step(plan, to_dev_bf16(hid[:rows]), to_dev_bf16(wl), to_dev_bf16(wr))
     sel = list(idx)
     s1 = check_latent(lat[sel], ref["latent"], ref["y_lat"], ref["abs_lat"])
-    s2 = check_logits(lg[sel], ref["y_log"], ref["abs_log"])
+    s2 = check_logits(lg[sel], ref["y_log"], ref["abs_log"], "prefill")
     ids_o, w_o = oracle.topk(lg)
     s3 = check_topk_exact(ids, w, ids_o, w_o)
     ids_ref, _ = oracle.topk(ref["logits"])
-    s4 = check_ids_end_to_end(ids[sel], ids_ref, ref["logits"], ref["y_log"], ref["abs_log"])
+    s4 = check_ids_end_to_end(ids[sel], ids_ref, ref["logits"], y64=ref["y_log"], logits_out=lg[sel])
     record(f"prefill_ragged_r{rows}", **s1, **s2, **s3, **s4)
 
 
@@ -284,11 +306,11 @@ def test_prefill_1024_cancel_group_sampled():
         lat, lg, ids, w = run_step(plan, to_dev_bf16(hid), to_dev_bf16(wl), to_dev_bf16(wr))
     sel = list(idx)
     s1 = check_latent(lat[sel], ref["latent"], ref["y_lat"], ref["abs_lat"])
-    s2 = check_logits(lg[sel], ref["y_log"], ref["abs_log"])
+    s2 = check_logits(lg[sel], ref["y_log"], ref["abs_log"], "prefill")
     ids_o, w_o = oracle.topk(lg)
     s3 = check_topk_exact(ids, w, ids_o, w_o)
     ids_ref, _ = oracle.topk(ref["logits"])
-    s4 = check_ids_end_to_end(ids[sel], ids_ref, ref["logits"], ref["y_log"], ref["abs_log"])
+    s4 = check_ids_end_to_end(ids[sel], ids_ref, ref["logits"], y64=ref["y_log"], logits_out=lg[sel])
     record("prefill_r1024_cancel_sampled", **s1, **s2, **s3, **s4)
     # the cancel-group columns of the sampled rows d < 448, on their own
     cols = [(i, d) for i, d in enumerate(idx) if d < 448]
@@ -299,9 +321,44 @@ def test_prefill_1024_cancel_group_sampled():
     record("prefill_r1024_cancel_columns", **check_latent(out, refc, yc, ac, rms_bar=False))
 
 
+def _prefill_gates(lat, lg, ids, w, ref, sel, case):
+    s1 = check_latent(lat[sel], ref["latent"], ref["y_lat"], ref["abs_lat"])
+    s2 = check_logits(lg[sel], ref["y_log"], ref["abs_log"], "prefill")
+    ids_o, w_o = oracle.topk(lg[sel])
+    s3 = check_topk_exact(ids[sel], w[sel], ids_o, w_o)
+    ids_ref, _ = oracle.topk(ref["logits"])
+    s4 = check_ids_end_to_end(ids[sel], ids_ref, ref["logits"], y64=ref["y_log"],
+                              logits_out=lg[sel])
+    record(case, **s1, **s2, **s3, **s4)
+
+
+def test_prefill_1024_every_row():
+    """All 1024 rows of the cancel-group workload against the oracle (G2-G4);
+    the oracle runs on row blocks in parallel (see gpu_util.oracle_block)."""
+    hid, wl, wr = bank("prefill_r1024", 0)
+    ref = oracle_rows("prefill_r1024", 0, tuple(range(1024)))
+    with route.Plan(route.PREFILL, 1024) as plan:
+        lat, lg, ids, w = run_step(plan, to_dev_bf16(hid), to_dev_bf16(wl), to_dev_bf16(wr))
+    _prefill_gates(lat, lg, ids, w, ref, list(range(1024)), "prefill_r1024_all")
+
+
+@pytest.mark.parametrize("b", [1, 2, 45, 91])
+def test_prefill_3072_other_banks_sampled(b):
+    """64 seeded rows of a 3072-row chunk on weight banks other than 0 (the
+    workload has 92, one per MoE layer) against the oracle (G2-G4)."""
+    hid, wl, wr = bank("prefill_r3072", b)
+    idx = tuple(int(i) for i in np.sort(np.random.default_rng(1000 + b).choice(3072, 64, replace=False)))
+    ref = oracle_rows("prefill_r3072", b, idx)
+    with route.Plan(route.PREFILL, 3072) as plan:
+        lat, lg, ids, w = run_step(plan, to_dev_bf16(hid), to_dev_bf16(wl), to_dev_bf16(wr))
+    _prefill_gates(lat, lg, ids, w, ref, list(idx), f"prefill_r3072_b{b}_s64")
+
+
 def test_prefill_3072_sampled_and_deterministic():
     hid, wl, wr = bank("prefill_r3072", 0)
-    idx = (0, 1, 255, 256, 1000, 1535, 2047, 2048, 2900, 3071)
+    rng = np.random.default_rng(1000)
+    idx = tuple(sorted(set((0, 1, 255, 256, 1000, 1535, 2047, 2048, 2900, 3071)) |
+                       set(int(i) for i in rng.choice(3072, 54, replace=False))))
     ref = oracle_rows("prefill_r3072", 0, idx)
     dh, dwl, dwr = to_dev_bf16(hid), to_dev_bf16(wl), to_dev_bf16(wr)
     with route.Plan(route.PREFILL, 3072) as plan:
@@ -310,9 +367,7 @@ def test_prefill_3072_sampled_and_deterministic():
     for x, y in zip(a, b):
         assert np.array_equal(np.asarray(x).view(np.uint8), np.asarray(y).view(np.uint8))
     lat, lg, ids, w = a
-    sel = list(idx)
-    check_latent(lat[sel], ref["latent"], ref["y_lat"], ref["abs_lat"])
-    check_logits(lg[sel], ref["y_log"], ref["abs_log"])
+    _prefill_gates(lat, lg, ids, w, ref, list(idx), "prefill_r3072_b0_s64")
     ids_o, w_o = oracle.topk(lg)
     check_topk_exact(ids, w, ids_o, w_o)
 
@@ -332,7 +387,7 @@ def test_prefill_8192_rows_sampled_and_position_independent():
         sel = [b + off for b in base if b + off < rows]
         k = len(sel)
         check_latent(lat[sel], ref["latent"][:k], ref["y_lat"][:k], ref["abs_lat"][:k])
-        check_logits(lg[sel], ref["y_log"][:k], ref["abs_log"][:k])
+        check_logits(lg[sel], ref["y_log"][:k], ref["abs_log"][:k], "prefill")
     for r in (0, 1000, 2047):
         for off in (3072, 6144):
             assert np.array_equal(lat[r], lat[r + off]) and np.array_equal(
