@@ -40,17 +40,19 @@ constexpr unsigned kStatusTimeout = 1u;
 
 // Prefill work is a list of tiles per CTA pair, built on the host.  A tile
 // is 256 weight columns (one column tile c: 0..13 latent, 14..17 router) by
-// the token rows from row0 on:
-//   full -- 256 rows, one FP32 accumulation over the whole K;
-//   K-split half -- 128 rows of a latent column tile, eight 896-deep K slices
-//     whose results are rounded to BF16 and added in FP32 (the general
-//     path's latent).
-// Packed into one int: row0 (a multiple of 128) + 32 * kind + c.
-enum PrefillTileKind : int { kTileFull = 0, kTileKsplitHalf = 2 };
+// the 256 token rows from row0 on, computed as one FP32 accumulation over
+// the whole K, or (K-split kind, latent tiles) as eight 896-deep K slices
+// whose results are rounded to BF16 and added in FP32 (the general path's
+// latent).  Packed into one int: row0 (a multiple of 256) + 32 * kind + c.
+enum PrefillTileKind : int { kTileFull = 0, kTileKsplit = 1 };
 __host__ __device__ constexpr int pack_tile(int c, int kind, int row0) { return row0 + 32 * kind + c; }
 __host__ __device__ constexpr int tile_col(int t) { return t & 31; }
 __host__ __device__ constexpr int tile_kind(int t) { return (t >> 5) & 3; }
-__host__ __device__ constexpr int tile_row0(int t) { return t & ~127; }
+__host__ __device__ constexpr int tile_row0(int t) { return t & ~255; }
+
+// Longest tile list of one pair (the host checks it): 65536 rows give 4608
+// tiles over 76 pairs, at most 61 a pair.
+constexpr int kMaxPairTiles = 256;
 
 // Per-row latent sum-of-squares parts written by the prefill epilogue: one
 // per (latent column tile, CTA of the pair, 32-column warp group).

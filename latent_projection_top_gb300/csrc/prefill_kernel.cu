@@ -18,16 +18,16 @@
 // weight columns x N token rows of the FP32 accumulator in its own TMEM.
 //
 // Tile kinds (the host builds each pair's list; see common.cuh):
-//   full (256 rows): one accumulation over the whole K; the epilogue stores
-//     the latent (rounded to BF16, with per-row sum-of-squares parts when
-//     asked) or the FP32 router logits.
-//   K-split half (latent, 128 rows): the general path's eight 896-deep K
-//     slices (same page, Numerics bullet and commit body), each rounded to
-//     BF16 and added in FP32 in slice order.
-// Every job accumulates into an aligned pair of TMEM quarters (a full tile's
-// 256 columns, or two slices of a K-split tile in 128 columns each), and the
-// pairs {0,1} and {2,3} alternate, so one job is drained while the next is
-// computed.  A K-split tile's running sums stay in registers.
+//   plain: one accumulation over the whole K; the epilogue stores the latent
+//     (rounded to BF16, with per-row sum-of-squares parts when asked) or the
+//     FP32 router logits.
+//   K-split (latent): the general path's eight 896-deep K slices (same page,
+//     Numerics bullet and commit body) as eight jobs, each slice's result
+//     rounded to BF16 and added in FP32, in slice order, to a running sum the
+//     epilogue keeps in registers (128 a thread).
+// Every job accumulates 256 TMEM columns, an aligned pair of quarters, and
+// the pairs {0,1} and {2,3} alternate from job to job, so one job is drained
+// while the next is computed.
 //
 // Warp roles (320 threads, persistent, one CTA per SM, pairs = clusters):
 //   warp 0      TMA producer (both CTAs); completion is counted on the leader
@@ -71,7 +71,7 @@ constexpr uint32_t kStoreBufBytes = 16 * 32 * 4;           // 16 rows x 32 colum
 constexpr uint32_t kStoreBytes = kEpiWarps * 2 * kStoreBufBytes;
 constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + kStoreBytes + 256;
 constexpr uint32_t kTmemCols = 512;                        // four quarters of 128 columns
-constexpr int kKsplitJobs = kKSplitSlices / 2;                    // 4 jobs of two slices
+static_assert(kMaxPairTiles >= 64, "tile list");
 
 // tcgen05 instruction descriptor, kind::f16: FP32 accumulator, BF16 A and B,
 // A MN-major (transposed), B K-major, M = 256 (over the pair), N = n.
@@ -79,8 +79,7 @@ constexpr uint32_t idesc_for(int n) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | ((uint32_t)(n >> 3) << 17) |
            ((uint32_t)(2 * kHalf >> 4) << 24);
 }
-constexpr uint32_t kIdescFull = idesc_for(kPrefillBN);
-constexpr uint32_t kIdescHalf = idesc_for(kPrefillBN / 2);
+constexpr uint32_t kIdesc = idesc_for(kPrefillBN);
 static_assert(kProjThreads == 64 + kEpiThreads, "warp roles");
 static_assert(kHalf == 2 * kPrefillHiddenBoxRows, "two hidden boxes per CTA and full tile");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -98,12 +97,10 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
     return d;
 }
 
-__device__ __forceinline__ int tile_jobs(int kind) { return kind == kTileFull ? 1 : kKsplitJobs; }
+__device__ __forceinline__ int tile_jobs(int kind) { return kind == kTileFull ? 1 : kKSplitSlices; }
 
-// Transaction bytes of one stage of a tile of this kind, both CTAs.
-__device__ __forceinline__ uint32_t stage_tx(int kind) {
-    return 2u * (kABytes + (kind == kTileFull ? kBBytes : kBoxBytes));
-}
+// Transaction bytes of one stage, both CTAs.
+constexpr uint32_t kStageTx = 2u * kStageBytes;
 
 // Bounded wait for the completion of phase `parity` of `bar` (acquire at
 // cluster scope: other CTAs of the pair arrive on these barriers).
@@ -153,6 +150,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t s_tmem_base;
     __shared__ volatile int s_abort;
+    __shared__ int s_tiles[kMaxPairTiles];  // this pair's tile list (read every k-block)
 
     // Both CTAs of a pair lay out shared memory identically, so an offset in
     // one names the same operand or barrier in the other.
@@ -171,9 +169,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int pair = blockIdx.x >> 1;
-    const int* const sched = args.sched + args.sched_off[pair];
-    const int ntiles = args.sched_off[pair + 1] - args.sched_off[pair];
+    const int tile0 = args.sched_off[pair];
+    const int ntiles = args.sched_off[pair + 1] - tile0;
     const int total = ntiles * kKBlocks;
+    const int *const sched = s_tiles;
+    for (int i = threadIdx.x; i < ntiles; i += blockDim.x) s_tiles[i] = args.sched[tile0 + i];
+    __syncthreads();
 
     if (threadIdx.x == 0) {
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -192,7 +193,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
         const int first = total < kStages ? total : kStages;
         if (leader && ntiles > 0)
             for (int s = 0; s < first; ++s)
-                ptx::mbar_arrive_expect_tx(full_bar(s), stage_tx(tile_kind(sched[0])));
+                ptx::mbar_arrive_expect_tx(full_bar(s), kStageTx);
         ptx::fence_barrier_init();
         ptx::prefetch_tensormap(&map_h);
         ptx::prefetch_tensormap(&map_wl);
@@ -228,16 +229,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
                 ptx::tma_load_2d_pair(st + kBBytes + kBoxBytes, wmap, bar, x0 + 64, kb * kKBlock,
                                       pol_w);
             };
-            auto hidden_of = [&](int it, uint32_t st, uint32_t bar) {
-                const int t = sched[it / kKBlocks];
+            auto hidden_of = [&](int it, uint32_t st, uint32_t bar) {  // this CTA's 128 of 256 rows
+                const int y0 = tile_row0(sched[it / kKBlocks]) + (int)rank * kHalf;
                 const int k0 = (it % kKBlocks) * kKBlock;
-                if (tile_kind(t) == kTileFull) {  // this CTA's 128 of the tile's 256 rows
-                    const int y0 = tile_row0(t) + (int)rank * kHalf;
-                    ptx::tma_load_2d_pair(st, &map_h, bar, k0, y0, pol_h);
-                    ptx::tma_load_2d_pair(st + kBoxBytes, &map_h, bar, k0, y0 + 64, pol_h);
-                } else {                          // this CTA's 64 of the tile's 128 rows
-                    ptx::tma_load_2d_pair(st, &map_h, bar, k0, tile_row0(t) + (int)rank * 64, pol_h);
-                }
+                ptx::tma_load_2d_pair(st, &map_h, bar, k0, y0, pol_h);
+                ptx::tma_load_2d_pair(st + kBoxBytes, &map_h, bar, k0, y0 + 64, pol_h);
             };
             // Weight boxes of the first stages go out before the grid
             // dependency resolves (no predecessor writes the weights).
@@ -285,11 +281,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
             int it = 0, job = 0;
             bool ok = true;
             for (int i = 0; i < ntiles && ok; ++i) {
-                const int kind = tile_kind(sched[i]);
-                const bool full = kind == kTileFull;
-                const int njobs = tile_jobs(kind);
-                const int kbpj = kKBlocks / njobs;        // k-blocks of one job
-                const int kbpa = full ? kbpj : kbpj / 2;  // k-blocks of one accumulator
+                const int njobs = tile_jobs(tile_kind(sched[i]));
+                const int kbpj = kKBlocks / njobs;  // k-blocks of one job
                 for (int j = 0; j < njobs && ok; ++j, ++job) {
                     const int q = 2 * (job & 1);
                     if (!(acquire(q) && acquire(q + 1))) {
@@ -297,7 +290,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t idesc = full ? kIdescFull : kIdescHalf;
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(128 * q);
                     for (int kb = 0; kb < kbpj; ++kb, ++it) {
                         const int s = it % kStages;
                         const uint32_t ph = (uint32_t)(it / kStages) & 1u;
@@ -306,9 +299,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
                             break;
                         }
                         ptx::tc_fence_after();
-                        // a half tile's second accumulator starts half-way through the job
-                        const uint32_t d_tmem = tmem_base + (uint32_t)(128 * q + (kb >= kbpa ? 128 : 0));
-                        const int kba = kb % kbpa;  // k-block within this accumulator
                         const uint32_t b = sbase + s * kStageBytes;
                         const uint32_t a = b + kBBytes;
 #pragma unroll
@@ -320,13 +310,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
                             //    8-row groups of token rows are 1024 B apart (SBO).
                             const uint64_t da = smem_desc(a + kk * 2048u, kBoxBytes, 1024u);
                             const uint64_t db = smem_desc(b + kk * 32u, 16u, 1024u);
-                            ptx::mma_bf16_pair(d_tmem, da, db, idesc, (kba > 0 || kk > 0) ? 1u : 0u);
+                            ptx::mma_bf16_pair(d_tmem, da, db, kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
                         }
                         // re-arm stage s for its next round before it is freed:
                         // the copies that fill it can only start after the commit
-                        if (it + kStages < total)
-                            ptx::mbar_arrive_expect_tx(
-                                full_bar(s), stage_tx(tile_kind(sched[(it + kStages) / kKBlocks])));
+                        if (it + kStages < total) ptx::mbar_arrive_expect_tx(full_bar(s), kStageTx);
                         ptx::mma_commit_pair(empty_bar(s), 0x3);  // frees stage s in both CTAs
                     }
                     if (ok) ptx::mma_commit_pair(qfull_bar(q), 0x3);
@@ -372,16 +360,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
             }
             sb ^= 1;
         };
-        // Per-row sum of squares of the 32 BF16 values of this warp (exact
-        // squares, a fixed warp tree of two-floats): one part per row.
-        auto sumsq_parts = [&](const uint32_t (&b)[16], int part, int y) {
+        // Per-row sum of squares of the 32 BF16 values this warp just staged
+        // for rows y .. y + 15 (exact squares; lanes 2r and 2r + 1 take 16
+        // values of row r each, two-floats joined in a fixed order): one part
+        // per row.  Reads the staging buffer before it can be written again.
+        auto sumsq_parts = [&](int part, int y) {
+            const uint4 *row = reinterpret_cast<const uint4 *>(
+                store_gen + (sb ^ 1) * kStoreBufBytes + (lane >> 1) * 64 + (lane & 1) * 32);
+            float hi = 0.f, lo = 0.f;
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-                const float f = __uint_as_float(b[jj] << 16);
-                float hi = f * f, lo = 0.f;
-                warp_two_sum(hi, lo);
-                if (lane == 0 && y + jj < rows)
-                    args.ss_part[(size_t)(y + jj) * kSsParts + part] = make_float2(hi, lo);
+            for (int g = 0; g < 2; ++g) {
+                const uint4 w4 = row[g];
+                const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float a = __uint_as_float(w[e] << 16), b = __uint_as_float(w[e] & 0xFFFF0000u);
+                    two_sum_acc(hi, lo, a * a);
+                    two_sum_acc(hi, lo, b * b);
+                }
+            }
+            const float ohi = __shfl_xor_sync(0xFFFFFFFFu, hi, 1);
+            const float olo = __shfl_xor_sync(0xFFFFFFFFu, lo, 1);
+            if ((lane & 1) == 0) {
+                two_sum_acc(hi, lo, ohi);
+                lo += olo;
+                if (y + (lane >> 1) < rows)
+                    args.ss_part[(size_t)(y + (lane >> 1)) * kSsParts + part] = make_float2(hi, lo);
             }
         };
         // This warp is done reading quarter q (one of the 16 arrivals the
@@ -412,17 +416,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
             const int xw = (lat ? c : c - kPrefillLatTiles) * 2 * kHalf + (int)rank * kHalf + 32 * lq;
             const bool valid = lat || xw < kExperts;
             const int part = c * 8 + (int)rank * 4 + lq;
+            const uint32_t acc0 = lanes + (uint32_t)(128 * cs);  // this warp's token rows 128 cs ..
             if (kind == kTileFull) {
                 const int q = 2 * (job++ & 1);
                 if (!wait_full(q)) {
                     go = false;
                     break;
                 }
-                const uint32_t acc = lanes + (uint32_t)(128 * q + 128 * cs);  // token rows 128 cs ..
 #pragma unroll 1
                 for (int ch = 0; ch < 8; ++ch) {
                     uint32_t u[16];
-                    ptx::tmem_ld_x16(acc + 16 * ch, u);
+                    ptx::tmem_ld_x16(acc0 + (uint32_t)(128 * q + 16 * ch), u);
                     ptx::tmem_ld_wait();
                     if (ch == 7) {  // every column of the accumulator is in registers
                         release(q);
@@ -433,51 +437,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
 #pragma unroll
                         for (int jj = 0; jj < 16; ++jj) u[jj] = bf16_bits(__uint_as_float(u[jj]));
                         store_chunk(u, false, &map_lat, xw, y, true);
-                        if (args.ss_part != nullptr) sumsq_parts(u, part, y);
+                        if (args.ss_part != nullptr) sumsq_parts(part, y);
                     } else {
                         store_chunk(u, true, &map_lg, xw, y, valid);
                     }
                 }
             } else {
-                // The K-split sums of this warp's 64 token rows, in registers:
-                // the BF16-rounded slice partials added in FP32 in slice order.
-                float sum[64];
+                // K-split latent: the BF16-rounded slice partials of this
+                // warp's 128 token rows, added in FP32 in slice order.
+                float sum[128];
 #pragma unroll 1
-                for (int j = 0; j < kKsplitJobs; ++j) {
+                for (int j = 0; j < kKSplitSlices; ++j) {
                     const int q = 2 * (job++ & 1);
                     if (!wait_full(q)) {
                         go = false;
                         break;
                     }
-                    const uint32_t acc = lanes + (uint32_t)(128 * q + 64 * cs);  // token rows 64 cs ..
 #pragma unroll
-                    for (int hh = 0; hh < 4; ++hh) {  // slices 2j and 2j + 1, 16 rows at a time
-                        uint32_t u[16], v[16];
-                        ptx::tmem_ld_x16(acc + 16 * hh, u);
-                        ptx::tmem_ld_x16(acc + 128 + 16 * hh, v);
+                    for (int ch = 0; ch < 8; ++ch) {
+                        uint32_t u[16];
+                        ptx::tmem_ld_x16(acc0 + (uint32_t)(128 * q + 16 * ch), u);
                         ptx::tmem_ld_wait();
-                        if (hh == 3) {
+                        if (ch == 7) {
                             release(q);
                             release(q + 1);
                         }
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
-                            const int x = 16 * hh + e;
-                            const float p0 = bf16_round(__uint_as_float(u[e]));
-                            const float p1 = bf16_round(__uint_as_float(v[e]));
-                            sum[x] = (j == 0 ? p0 : sum[x] + p0) + p1;
+                            const float p = bf16_round(__uint_as_float(u[e]));
+                            sum[16 * ch + e] = j == 0 ? p : sum[16 * ch + e] + p;
                         }
                     }
                 }
                 if (!go) break;
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
+                for (int ch = 0; ch < 8; ++ch) {
                     uint32_t v[16];
-                    const int y = row0 + 64 * cs + 16 * ch;
+                    const int y = row0 + 128 * cs + 16 * ch;
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) v[jj] = bf16_bits(sum[16 * ch + jj]);
                     store_chunk(v, false, &map_lat, xw, y, true);
-                    if (args.ss_part != nullptr) sumsq_parts(v, part, y);
+                    if (args.ss_part != nullptr) sumsq_parts(part, y);
                 }
             }
         }

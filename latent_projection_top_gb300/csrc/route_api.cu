@@ -306,12 +306,8 @@ route_status run_step(const route_plan *p, const void *hidden, const void *W_lat
 // column tiles over every 256-row block, then the next band, with B = the
 // pair count over the row blocks (at least 1, at most all 18), so that the
 // pairs at work at one time read few weight tiles and every hidden row block.
-// Column tiles are full tiles (256 rows); with the K-split latent, latent
-// column tiles are two half tiles of 128 rows instead (one when the second
-// would start past the last row).  Each tile goes, in that order, to the
-// pair with the least work so far (a half tile counts 11/20 of a full one:
-// half the MMAs plus its slower feed).
-void build_schedule(int rows, bool ksplit, int max_pairs, std::vector<int> &off,
+// Each tile goes, in that order, to the pair with the fewest tiles so far.
+bool build_schedule(int rows, bool ksplit, int max_pairs, std::vector<int> &off,
                     std::vector<int> &tiles, int *pairs) {
     const int row_blocks = (rows + kPrefillBN - 1) / kPrefillBN;
     int band = max_pairs / row_blocks;
@@ -321,13 +317,8 @@ void build_schedule(int rows, bool ksplit, int max_pairs, std::vector<int> &off,
         for (int r = 0; r < row_blocks; ++r)
             for (int c = c0; c < c0 + band && c < kPrefillColTiles; ++c) {
                 const int row0 = r * kPrefillBN;
-                if (c >= kPrefillLatTiles || !ksplit) {
-                    order.push_back(pack_tile(c, kTileFull, row0));
-                } else {
-                    order.push_back(pack_tile(c, kTileKsplitHalf, row0));
-                    if (row0 + kPrefillBN / 2 < rows)
-                        order.push_back(pack_tile(c, kTileKsplitHalf, row0 + kPrefillBN / 2));
-                }
+                order.push_back(
+                    pack_tile(c, ksplit && c < kPrefillLatTiles ? kTileKsplit : kTileFull, row0));
             }
     const int np = max_pairs < (int)order.size() ? max_pairs : (int)order.size();
     std::vector<std::vector<int>> lists(np);
@@ -337,15 +328,17 @@ void build_schedule(int rows, bool ksplit, int max_pairs, std::vector<int> &off,
         for (int q = 1; q < np; ++q)
             if (load[q] < load[best]) best = q;
         lists[best].push_back(t);
-        load[best] += tile_kind(t) == kTileFull ? 20 : 11;
+        load[best] += 1;
     }
     off.assign(1, 0);
     tiles.clear();
     for (auto &l : lists) {
+        if ((int)l.size() > kMaxPairTiles) return false;
         tiles.insert(tiles.end(), l.begin(), l.end());
         off.push_back((int)tiles.size());
     }
     *pairs = np;
+    return true;
 }
 
 // Decode stream grid: the largest CTA count, at most one per SM and at most
@@ -540,7 +533,10 @@ route_status route_prepare(int mode, int rows, int device, route_plan **out) {
         a.status = p->words + kWordStatus;
         std::vector<int> off[2], tiles[2];
         for (int ks = 0; ks < 2; ++ks)
-            build_schedule(rows, ks == 1, sms / 2, off[ks], tiles[ks], &p->sched_pairs[ks]);
+            if (!build_schedule(rows, ks == 1, sms / 2, off[ks], tiles[ks], &p->sched_pairs[ks])) {
+                free_plan(p);
+                return fail(ROUTE_ERR_PLAN, "prefill tile list longer than %d tiles a pair", kMaxPairTiles);
+            }
         size_t n = 0;
         for (int ks = 0; ks < 2; ++ks) n += off[ks].size() + tiles[ks].size();
         if ((e = cudaMalloc(&p->sched, n * sizeof(int))) != cudaSuccess) {
