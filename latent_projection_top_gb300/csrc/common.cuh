@@ -84,23 +84,11 @@ constexpr int kWordSsCount = 8;  // [8, 8 + 20): per-row arrivals of latent sum-
 constexpr int kWords = 64;
 static_assert(kWordSsCount + kDecodeMaxRows <= kWords, "word area");
 
-// Without overlap, a decode step's CTAs start as the previous step's stream
-// CTAs leave: just when the previous finish kernel (or whatever kernel
-// precedes the step) does its last reads.  A burst of weight prefetches from
-// every CTA at that moment queues those reads behind ~19 MB of HBM traffic
-// (measured: the finish kernel's partial sums took 2.8 us instead of 0.8),
-// and the dependency resolves that much later.  So without overlap the
-// first weight boxes go out this long after the CTA starts (measured best
-// among 0.5 .. 4 us at 1, 8 and 20 rows).  Not after the host-buffer path's
-// copy in (its staging kernel ends sooner than that).
-constexpr unsigned kPrefetchHoldNs = 1000;
-
 struct DecodeArgs {
     int rows;            // 1..20
     int grid;            // CTAs of the stream kernel (<= kMaxGrid)
     int test_stall;      // test hook: skip each CTA's last copy so a wait must time out
     int overlap;         // read hidden before the grid dependency resolves
-    unsigned hold_ns;    // delay of the first weight boxes (0 with overlap)
     int ksplit;          // latent with the general path's K-split arithmetic
     unsigned long long timeout_ns;
     int cta_unit[kMaxGrid + 1];  // CTA g owns units [cta_unit[g], cta_unit[g+1]); unit u =

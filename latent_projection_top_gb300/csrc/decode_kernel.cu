@@ -253,10 +253,6 @@ __global__ void __maxnreg__(BN == 16 ? 72 : 80)
             uint32_t armed = 0u, armed_par = 0u;
             // Weight boxes of the first stages go out before the grid
             // dependency resolves (no predecessor writes the weights).
-            if (args.hold_ns != 0u) {  // see kPrefetchHoldNs
-                const uint64_t t0 = ptx::global_timer_ns();
-                while (ptx::global_timer_ns() - t0 < args.hold_ns) __nanosleep(64);
-            }
             for (int i = 0; i < n_pre; ++i) {
                 ptx::mbar_arrive_expect_tx(full_bar(i), C::kStageBytes);
                 weights_of(u0 + i, sbase + i * C::kStageBytes, full_bar(i));

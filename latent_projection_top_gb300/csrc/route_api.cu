@@ -242,9 +242,8 @@ route_status launch_forward(const route_plan *p, const void *hidden, const void 
         a.weights = weights;
         a.sumsq = sumsq;
         // After the host path's copy in (a staging kernel or a copy), hidden
-        // is the predecessor's output, and no finish kernel precedes.
+        // is the predecessor's output.
         if (after_copy_in) a.overlap = 0;
-        a.hold_ns = a.overlap || after_copy_in ? 0u : kPrefetchHoldNs;
         e = decode_launch(p->bn, mh, ml, mr, a, do_topk, stream);
         if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
     } else {
@@ -443,7 +442,6 @@ route_status noalloc_setup(int device, NoAllocDevice **out) {
                     kNoAllocMaxSlots);
     d.scratch = static_cast<unsigned char *>(ptr);
     d.base.timeout_ns = kDefaultTimeoutNs;
-    d.base.hold_ns = kPrefetchHoldNs;  // no overlap here
     d.base.words = reinterpret_cast<unsigned *>(d.scratch);
     d.base.ws = reinterpret_cast<float2 *>(d.scratch + kNoAllocWordBytes);
     d.ready = true;
@@ -662,7 +660,7 @@ static route_status enqueue_mapped_step(const route_plan *plan, const void *h,
     cudaError_t e;
     if ((e = stage_in_launch(h, d.hidden, (size_t)plan->rows * kHidden * 2, s)) != cudaSuccess)
         return cuda_fail(e, "stage hidden rows");
-    // after the staging kernel: no overlap, no hold
+    // after the staging kernel: no overlap
     return launch_forward(plan, d.hidden, W_latent, W_router, lat, static_cast<float *>(lg),
                           static_cast<int32_t *>(ids), static_cast<float *>(w), 1, nullptr, s,
                           true);
