@@ -59,7 +59,9 @@ typedef enum {
     ROUTE_ERR_CUDA = 5,           /* a CUDA call failed; see route_last_error() */
     ROUTE_ERR_DEVICE_TIMEOUT = 6, /* a kernel gave up waiting and returned */
     ROUTE_ERR_PLAN = 7,           /* the plan cannot run this call */
-    ROUTE_ERR_DEVICE = 8          /* the device is not an sm_103 GPU */
+    ROUTE_ERR_DEVICE = 8,         /* the device is not an sm_103 GPU */
+    ROUTE_ERR_DEVICE_BOUNDS = 9   /* (debug library) a kernel computed an index out of
+                                     range and skipped that access */
 } route_status;
 
 typedef enum {

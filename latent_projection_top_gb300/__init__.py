@@ -39,12 +39,16 @@ ROUTE_OK = 0
 STATUS_NAMES = {
     0: "ROUTE_OK", 1: "ROUTE_ERR_ROWS", 2: "ROUTE_ERR_MODE", 3: "ROUTE_ERR_NULL",
     4: "ROUTE_ERR_ALIGN", 5: "ROUTE_ERR_CUDA", 6: "ROUTE_ERR_DEVICE_TIMEOUT",
-    7: "ROUTE_ERR_PLAN", 8: "ROUTE_ERR_DEVICE",
+    7: "ROUTE_ERR_PLAN", 8: "ROUTE_ERR_DEVICE", 9: "ROUTE_ERR_DEVICE_BOUNDS",
 }
 STATUS_CODES = {name: code for code, name in STATUS_NAMES.items()}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_build", "libroute.so")
+RELEASE_LIB_PATH = os.path.join(_HERE, "_build", "libroute.so")
+DEBUG_LIB_PATH = os.path.join(_HERE, "_build", "debug", "libroute_debug.so")
+# ROUTE_DEBUG_LIB=1 selects the checked library (every computed global index
+# of the kernels bounds-checked; see builder.py), e.g. for a test process.
+LIB_PATH = DEBUG_LIB_PATH if os.environ.get("ROUTE_DEBUG_LIB") == "1" else RELEASE_LIB_PATH
 
 # Every symbol the header declares (checked by the CPU tests).
 EXPORTS = (
@@ -66,9 +70,11 @@ class RouteError(RuntimeError):
 _lib = None
 
 
-def build(force: bool = False) -> str:
+def build(force: bool = False, debug: bool = False, both: bool = False) -> str:
+    """Compile the route library (see builder.py): the release one, the checked
+    one (debug=True), or both (both=True)."""
     from . import builder as _b
-    return _b.build(force=force)
+    return _b.build(force=force, debug=debug or LIB_PATH == DEBUG_LIB_PATH, both=both)
 
 
 def lib() -> ctypes.CDLL:

@@ -37,6 +37,21 @@ enum Mode : int { kDecode = 0, kPrefill = 1 };
 
 // Device status bits (the kernels set them instead of hanging).
 constexpr unsigned kStatusTimeout = 1u;
+constexpr unsigned kStatusBounds = 2u;  // debug library: an index out of range was skipped
+
+// ROUTE_IN_BOUNDS(ok, status): in the debug library (built with -DROUTE_DEBUG)
+// every computed global index is checked before its access; a failed check
+// sets kStatusBounds in the status word and the access is skipped, so the
+// kernel neither faults nor traps.  In the release library it is `true`.
+#ifdef ROUTE_DEBUG
+__device__ __forceinline__ bool route_in_bounds(bool ok, unsigned *status) {
+    if (!ok) atomicOr(status, kStatusBounds);
+    return ok;
+}
+#define ROUTE_IN_BOUNDS(ok, status) route_in_bounds((ok), (status))
+#else
+#define ROUTE_IN_BOUNDS(ok, status) true
+#endif
 
 // Prefill work is a list of tiles per CTA pair, built on the host.  A tile
 // is 256 weight columns (one column tile c: 0..13 latent, 14..17 router) by

@@ -345,8 +345,11 @@ __global__ void __maxnreg__(BN == 16 ? 72 : 80)
             // Scratch may still be read by the predecessor's finish kernel.
             if (last) asm volatile("griddepcontrol.wait;" ::: "memory");
             const int slot = args.seg_base[t] + (g - args.cta_first[t]);
+            const int nslots = args.seg_base[kDTiles - 1] + args.seg_count[kDTiles - 1];
+            const bool slot_ok = ROUTE_IN_BOUNDS(
+                t < kDTiles && slot >= 0 && slot < nslots && col < kDTileCols, args.words);
             float2 *const out =
-                last ? args.ws + (size_t)slot * kDecodeMaxRows * kDTileCols : stash;
+                last && slot_ok ? args.ws + (size_t)slot * kDecodeMaxRows * kDTileCols : stash;
             const uint32_t acc = lanes + (uint32_t)(buf * C::kAccCols + blk * BN);
             // Rows 0..15, then (BN = 32) rows 16..19: no row past the
             // 20-row envelope is ever read from TMEM.
@@ -357,7 +360,7 @@ __global__ void __maxnreg__(BN == 16 ? 72 : 80)
                                                accempty_bar(buf), out, col, rows);
             if (!run_end) ptx::tmem_st_wait();  // the next pair reads these sums back
             if (run_end && !last) first_slot = slot;
-            if (last && first_slot >= 0) {
+            if (last && first_slot >= 0 && ROUTE_IN_BOUNDS(first_slot < nslots, args.words)) {
                 float2 *p0 = args.ws + (size_t)first_slot * kDecodeMaxRows * kDTileCols;
                 for (int r = 0; r < rows; ++r) p0[r * kDTileCols + col] = stash[r * kDTileCols + col];
             }
@@ -393,6 +396,10 @@ struct SlotRun {
 
 __device__ __forceinline__ SlotRun slot_run(const DecodeArgs &a, int r, int t, int cc) {
     SlotRun s;
+    if (!ROUTE_IN_BOUNDS(r >= 0 && r < a.rows && t >= 0 && t < kDTiles && cc >= 0 &&
+                             cc + 1 < kDTileCols,
+                         a.words))
+        return SlotRun{reinterpret_cast<const float4 *>(a.ws), 0};
     s.p = reinterpret_cast<const float4 *>(a.ws) +
           ((size_t)a.seg_base[t] * kDecodeMaxRows + r) * (kDTileCols / 2) + cc / 2;
     s.n = a.seg_count[t];
@@ -533,6 +540,7 @@ __device__ __forceinline__ void latent_sumsq_part(const DecodeArgs &a, int r, in
         two_sum_acc(hi, lo, ss[w].x);
         lo += ss[w].y;
     }
+    if (!ROUTE_IN_BOUNDS(r < a.rows && t < kDLatTiles, a.words)) return;
     a.ss_part[r * kDLatTiles + t] = make_float2(hi, lo);
     // acq_rel: this part is visible before the arrival counts, and the last
     // arrival sees every other part
@@ -596,8 +604,9 @@ __device__ __forceinline__ void finish_latent(const DecodeArgs &a, int per_half,
             if (q >= per_half || i >= n_items) break;  // the same for the whole half
             const int r = i / kDLatTiles, t = i % kDLatTiles;
             const uint16_t b0 = bf16_bits(y[q].x), b1 = bf16_bits(y[q].y);
-            *reinterpret_cast<uint32_t *>(a.latent + (size_t)r * kLatent + t * kDTileCols + cc) =
-                (uint32_t)b0 | ((uint32_t)b1 << 16);
+            if (ROUTE_IN_BOUNDS(r < rows && t < kDLatTiles && cc + 1 < kDTileCols, a.words))
+                *reinterpret_cast<uint32_t *>(a.latent + (size_t)r * kLatent + t * kDTileCols + cc) =
+                    (uint32_t)b0 | ((uint32_t)b1 << 16);
             if (a.sumsq != nullptr)
                 latent_sumsq_part(a, r, t, b0, b1, half, tid % kLatentThreads,
                                   s_ss[calls++ & 1][half]);
@@ -625,6 +634,7 @@ __global__ void __maxnreg__(112) decode_finish_kernel(const __grid_constant__ De
         float2 y[2];
         sum_slot_pairs<2>(run, y);
         float *lrow = a.logits + (size_t)r * kExperts;
+        if (!ROUTE_IN_BOUNDS(r < rows && c1 + 1 < kExperts, a.words)) return;
         *reinterpret_cast<float2 *>(lrow + c0) = y[0];
         *reinterpret_cast<float2 *>(lrow + c1) = y[1];
         if (!do_topk) return;

@@ -173,7 +173,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
     const int ntiles = args.sched_off[pair + 1] - tile0;
     const int total = ntiles * kKBlocks;
     const int *const sched = s_tiles;
-    for (int i = threadIdx.x; i < ntiles; i += blockDim.x) s_tiles[i] = args.sched[tile0 + i];
+    for (int i = threadIdx.x; i < ntiles; i += blockDim.x)
+        if (ROUTE_IN_BOUNDS(i < kMaxPairTiles, args.status)) s_tiles[i] = args.sched[tile0 + i];
     __syncthreads();
 
     if (threadIdx.x == 0) {
@@ -353,7 +354,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
             ptx::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                if (valid && y < rows) ptx::tma_store_2d(map, store_sh + sb * kStoreBufBytes, x, y);
+                if (valid && y < rows && ROUTE_IN_BOUNDS(y >= 0 && (x & 31) == 0, args.status))
+                    ptx::tma_store_2d(map, store_sh + sb * kStoreBufBytes, x, y);
                 // one group per chunk, empty when nothing is stored, so that
                 // "at most one group pending" always means this buffer is free
                 ptx::bulk_commit_group();
@@ -384,7 +386,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
             if ((lane & 1) == 0) {
                 two_sum_acc(hi, lo, ohi);
                 lo += olo;
-                if (y + (lane >> 1) < rows)
+                if (y + (lane >> 1) < rows &&
+                    ROUTE_IN_BOUNDS(y >= 0 && part >= 0 && part < kSsParts, args.status))
                     args.ss_part[(size_t)(y + (lane >> 1)) * kSsParts + part] = make_float2(hi, lo);
             }
         };

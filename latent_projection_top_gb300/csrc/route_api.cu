@@ -733,6 +733,11 @@ route_status route_device_status(const route_plan *plan) {
     if (status == 0) return ROUTE_OK;
     cudaMemset(plan->words, 0, kWords * sizeof(unsigned));  // status and counters
     cudaDeviceSynchronize();
+    if (status & kStatusBounds)
+        return fail(ROUTE_ERR_DEVICE_BOUNDS,
+                    "a kernel computed an index out of range and skipped that access (status "
+                    "0x%x, debug library); that launch's outputs are invalid",
+                    status);
     return fail(ROUTE_ERR_DEVICE_TIMEOUT,
                 "a kernel gave up waiting (status 0x%x); that launch's outputs are invalid", status);
 }

@@ -38,6 +38,17 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+@pytest.mark.slow
+def test_debug_library_builds_and_exports_every_declared_symbol():
+    """The bounds-checked library (-DROUTE_DEBUG) builds from the same sources
+    and exports the same entry points."""
+    path = route.build(debug=True)
+    assert path.endswith("libroute_debug.so")
+    dbg = ctypes.CDLL(path)
+    for name in header_functions():
+        assert hasattr(dbg, name), name
+
+
 def _prepare(lib, mode, rows):
     h = ctypes.c_void_p(123)
     st = lib.route_prepare(mode, rows, 0, ctypes.byref(h))
