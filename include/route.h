@@ -79,8 +79,9 @@ typedef struct route_plan route_plan; /* opaque */
  * Decode accepts 1 <= rows <= 20 and rejects anything else with
  * ROUTE_ERR_ROWS before touching the device -- the envelope is checked at
  * preparation, loudly, with no fallback ("Kimi K3.1 recipe ...", commit
- * message: "prepares 1-20 rows or raises at preparation"; Tests: the 21-row
- * envelope rejection).  Prefill accepts 1 <= rows <= 65536.
+ * message: the recipe prepares only 1 to 20 rows and otherwise fails at
+ * preparation; Tests: the 21-row envelope rejection).  Prefill accepts
+ * 1 <= rows <= 65536.
  * On success *out receives the plan; on failure *out is set to NULL.
  */
 route_status route_prepare(int mode, int rows, int device, route_plan **out);
@@ -115,8 +116,8 @@ route_status latent_router_forward(const route_plan *plan, const void *hidden,
  *                                       in FP32 with compensated (two-float)
  *                                       steps and one final rounding: within
  *                                       5 FP32 ULP of the value in double
- * ("Kimi K3.1 recipe ...", commit message: "the standalone top-16 selects
- * their experts"; the routing-weight formula is this library's convention.)
+ * ("Kimi K3.1 recipe ...", commit message: a standalone top-16 picks each
+ * row's experts; the routing-weight formula is this library's convention.)
  */
 route_status topk16_select(const route_plan *plan, const float *logits, int32_t *ids,
                            float *weights, void *stream);
@@ -274,12 +275,30 @@ route_status route_test_poison_scratch(const route_plan *plan, void *stream);
  * overlaps on the GPU (other streams, other host threads) race: serialise
  * them, e.g. on one stream.  The first call on a device does a one-time
  * set-up (the array's device address, the kernels' shared-memory limit):
- * make that first call before any stream capture.  This entry point reports
- * no device-side timeout status.
+ * make that first call before any stream capture.  A device-side timeout of
+ * these calls is read with route_noalloc_status.
  */
 route_status route_step_decode_noalloc(int rows, const void *hidden, const void *W_latent,
                                        const void *W_router, void *latent, float *logits,
                                        int32_t *ids, float *weights, void *stream);
+
+/*
+ * route_noalloc_status: synchronises `device` and reports whether a kernel of
+ * route_step_decode_noalloc on it gave up waiting (ROUTE_ERR_DEVICE_TIMEOUT;
+ * the outputs of that call are invalid) since the last query, then clears
+ * the fixed array's status and counters.  ROUTE_OK when nothing failed or no
+ * call has run on the device.  device outside 0..63: ROUTE_ERR_DEVICE before
+ * any CUDA call.  Allocates nothing.
+ */
+route_status route_noalloc_status(int device);
+
+/*
+ * route_noalloc_grid: the CTA count route_step_decode_noalloc's weight stream
+ * uses on `device` (a function of its SM count, capped at 160); the same as
+ * route_plan_grid of a decode plan on devices with up to 160 SMs.  -1 when
+ * the device cannot be queried.
+ */
+int route_noalloc_grid(int device);
 
 /* Plan properties: rows, mode, launch grid (CTAs) and split-K segments. */
 int route_plan_rows(const route_plan *plan);

@@ -57,7 +57,8 @@ EXPORTS = (
     "route_plan_grid", "route_plan_segments", "route_last_error", "route_test_stall",
     "route_set_overlap", "route_step_decode_noalloc", "route_step_sumsq",
     "route_set_latent_ksplit", "route_host_step_create", "route_host_step_run",
-    "route_host_step_destroy", "route_test_poison_scratch",
+    "route_host_step_destroy", "route_test_poison_scratch", "route_noalloc_status",
+    "route_noalloc_grid",
 )
 
 
@@ -106,6 +107,10 @@ def lib() -> ctypes.CDLL:
         L.route_host_step_run.argtypes = [vp]
         L.route_host_step_destroy.argtypes = [vp]
         L.route_test_poison_scratch.argtypes = [vp, vp]
+        L.route_noalloc_status.argtypes = [i32]
+        L.route_noalloc_status.restype = i32
+        L.route_noalloc_grid.argtypes = [i32]
+        L.route_noalloc_grid.restype = i32
         for f in ("route_host_step_create", "route_host_step_run", "route_host_step_destroy",
                   "route_test_poison_scratch"):
             getattr(L, f).restype = i32

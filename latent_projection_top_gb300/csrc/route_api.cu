@@ -914,6 +914,42 @@ route_status route_step_decode_noalloc(int rows, const void *hidden, const void 
     return ROUTE_OK;
 }
 
+route_status route_noalloc_status(int device) {
+    g_err[0] = '\0';
+    if (device < 0 || device >= kNoAllocMaxDevices)
+        return fail(ROUTE_ERR_DEVICE, "device %d is out of range", device);
+    unsigned char *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_noalloc_mu);
+        if (g_noalloc[device].ready) scratch = g_noalloc[device].scratch;
+    }
+    if (!scratch) return ROUTE_OK;  // no call has run on this device
+    DeviceGuard guard(device);
+    if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    unsigned status = 0;
+    if ((e = cudaMemcpy(&status, scratch, sizeof status, cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_fail(e, "read the no-allocation status word");
+    if (status == 0) return ROUTE_OK;
+    if ((e = cudaMemset(scratch, 0, kNoAllocWordBytes)) != cudaSuccess ||
+        (e = cudaDeviceSynchronize()) != cudaSuccess)
+        return cuda_fail(e, "clear the no-allocation status");
+    return fail(ROUTE_ERR_DEVICE_TIMEOUT,
+                "a kernel of route_step_decode_noalloc gave up waiting (status 0x%x); that call's "
+                "outputs are invalid",
+                status);
+}
+
+int route_noalloc_grid(int device) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    return decode_grid(prop.multiProcessorCount, kNoAllocMaxGrid);
+}
+
 int route_plan_rows(const route_plan *plan) { return plan ? plan->rows : -1; }
 int route_plan_mode(const route_plan *plan) { return plan ? plan->mode : -1; }
 int route_plan_grid(const route_plan *plan) { return plan ? plan->grid : -1; }

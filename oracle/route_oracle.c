@@ -11,14 +11,15 @@
  *             is more accurate against float64 than the K-split path.
  *   [P2-Cmp]  same page, Description, Compile bullet: the projection is
  *             M = rows, K = 7168; 3584 latent columns in total.
- *   [P2-Body] same page, commit body: "(today: BF16 partials, FP32 sum,
- *             BF16 again)" -- the general path's two roundings.
+ *   [P2-Body] same page, commit body: the general path rounds each K-slice
+ *             partial to BF16, adds the partials in FP32 and rounds the sum
+ *             to BF16 again -- two roundings.
  *   [P3]      "Use two row blocks for eight-row Kimi paired gathers", body:
  *             FP32 router logits, 56 per rank at TP16, i.e. 896 experts.
  *   [P1]      "Kimi K3.1 recipe: route 9..20 decode rows through the pushed
  *             pair gather and standalone top-16", commit message: a
  *             standalone top-16 selects each row's experts; routing weights
- *             are compared "within 5 fp32 ULP".
+ *             are compared to within 5 FP32 ULP.
  *
  * Readings where the pages are silent (each is listed in the design notes):
  *   - weights are stored [K, N] row-major (N contiguous);

@@ -4,7 +4,8 @@ A quarter of the rows (r mod 4 == 3) are edited so that the experts at ranks
 16 and 17 have float64 logits within 1 FP32 ULP (alternate rows: within 2 ULP)
 of each other.  This exercises the near-tie rule of "Kimi K3.1 recipe: route
 9..20 decode rows through the pushed pair gather and standalone top-16",
-commit message: "every set difference a 1-for-1 swap within 2 fp32 ULP".
+commit message: a difference in the selected set may only be a one-for-one
+exchange of two experts whose logits lie at most 2 FP32 ULP apart.
 
 The pages give no construction; this one edits only hidden coordinates of the
 row (weights are shared by every row):

@@ -51,6 +51,14 @@ def _p(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def test_status_query_rejects_a_device_out_of_range():
+    """route_noalloc_status checks the device index before any CUDA call."""
+    route.build()
+    lib = route.lib()
+    for dev in (-1, 64, 1000):
+        assert lib.route_noalloc_status(dev) == 8  # ROUTE_ERR_DEVICE
+
+
 def test_rows_beyond_the_fixed_scratch_are_rejected():
     """rows outside 1..20 fail with ROUTE_ERR_ROWS before any device work."""
     route.build()
@@ -87,9 +95,9 @@ def test_noalloc_matches_route_step_on_two_calls(rows):
         w = _host(want)
         assert np.all(g[2] >= 0), f"call {call}: ids not written"
         sms = torch.cuda.get_device_properties(0).multi_processor_count
-        # the stream grid: the largest count <= min(SMs, cap) dividing the
-        # 18 * 112 units; the allocation-free entry point caps it at 160
-        noalloc_grid = next(g for g in range(min(sms, 160), 17, -1) if 1008 % g == 0)
+        noalloc_grid = lib.route_noalloc_grid(0)
+        if sms <= 160:  # the cap does not bind: the plan's partition exactly
+            assert noalloc_grid == plan_grid, (noalloc_grid, plan_grid)
         if plan_grid == noalloc_grid:
             # Same kernels and the same split-K partition: identical bits.
             for name, a, b in zip(("latent", "logits", "ids", "weights"), g, w):
@@ -102,3 +110,4 @@ def test_noalloc_matches_route_step_on_two_calls(rows):
             assert np.all(np.abs(lat_g - lat_w) <= ulp)
             lg_g, lg_w = g[1].view(np.float32), w[1].view(np.float32)
             assert np.allclose(lg_g, lg_w, rtol=1e-5, atol=1e-6)
+        assert lib.route_noalloc_status(0) == 0, lib.route_last_error().decode()
