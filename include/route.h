@@ -255,6 +255,71 @@ route_status route_test_stall(route_plan *plan, int enable, uint64_t timeout_ns)
 route_status route_test_poison_scratch(const route_plan *plan, void *stream);
 
 /*
+ * Column shards.  Shard s of W computes, from the full hidden rows, latent
+ * columns [3584 s / W, 3584 (s+1) / W) and experts [896 s / W, 896 (s+1) / W)
+ * of the layer, and picks its own top-16 of those experts; a merge of the
+ * W x 16 candidates finishes the selection.  This is how the step divides
+ * over W GPUs with one exchange and no reduction: every rank computes its
+ * own latent columns from the full hidden row and the results are gathered
+ * ("Optionally gather the Kimi3 prefill latent instead of reducing it",
+ * Description: each of 8 ranks computes its own 448 latent columns, then an
+ * all-gather), the decode gather pairs each rank's latent and router columns
+ * (at TP16, 224 latent and 56 router columns a rank: "Use two row blocks for
+ * eight-row Kimi paired gathers", body), and candidate selection and merge
+ * are what that page's tests and the first page's tests name.  The exchange
+ * itself (an all-gather of the candidates, and of the latent and logit
+ * columns where the caller wants them whole) is the caller's collective;
+ * this library computes each shard and the merge.  Every result of shard s
+ * equals the matching columns of route_step on a prefill plan of the same
+ * rows (the per-column arithmetic is the same), so the merged ids and
+ * weights are those of the top-16 of the whole logit row.
+ *
+ * route_prepare_shard: a plan for shard `shard` (0 <= shard < num_shards) of
+ * `num_shards` W in {1, 2, 4, 7, 8, 14, 16} (W divides 896 experts, with at
+ * least 16 experts a shard), for 1 <= rows <= 65536 on `device`; it runs the
+ * prefill kernel over the shard's column tiles.  Anything else returns
+ * ROUTE_ERR_PLAN or ROUTE_ERR_ROWS before touching the device.  A shard plan
+ * runs route_shard_step (and the set-up calls route_set_overlap,
+ * route_set_latent_ksplit, route_test_stall, route_device_status); every
+ * other step entry point refuses it with ROUTE_ERR_PLAN.
+ */
+route_status route_prepare_shard(int rows, int device, int shard, int num_shards,
+                                 route_plan **out);
+
+/*
+ * route_shard_step: steps a1..a3 of one column shard, NL = 3584 / W latent
+ * columns and NE = 896 / W experts (device memory, 16-byte aligned):
+ *   hidden         [rows, 7168] BF16  (read)   the full hidden rows
+ *   W_latent_shard [7168, NL]   BF16  (read)   columns s NL .. of W_latent
+ *   W_router_shard [7168, NE]   BF16  (read)   columns s NE .. of W_router
+ *   latent_shard   [rows, NL]   BF16  (written)
+ *   logits_shard   [rows, NE]   FP32  (written)
+ *   cand_ids       [rows, 16]   int32 (written) the shard's top-16, global
+ *                                               expert ids (s NE + local id)
+ *   cand_logits    [rows, 16]   FP32  (written) their logits
+ * Two kernels on `stream`: the projection, then the shard's top-16.
+ */
+route_status route_shard_step(const route_plan *plan, const void *hidden,
+                              const void *W_latent_shard, const void *W_router_shard,
+                              void *latent_shard, float *logits_shard, int32_t *cand_ids,
+                              float *cand_logits, void *stream);
+
+/*
+ * route_merge_candidates: steps a3 and a4 over the W shards' candidates, on
+ * the current device (no plan; one kernel on `stream`):
+ *   cand_ids    [W, rows, 16] int32 (read)  shard after shard, as an
+ *   cand_logits [W, rows, 16] FP32  (read)  all-gather of route_shard_step's
+ *                                           outputs lays them out
+ *   ids         [rows, 16]    int32 (written) as topk16_select
+ *   weights     [rows, 16]    FP32  (written) as topk16_select
+ * rows 1..65536 (ROUTE_ERR_ROWS), W 1..16 (ROUTE_ERR_PLAN), pointers
+ * non-NULL and 16-byte aligned.  Candidates must hold distinct ids.
+ */
+route_status route_merge_candidates(int rows, int num_shards, const int32_t *cand_ids,
+                                    const float *cand_logits, int32_t *ids, float *weights,
+                                    void *stream);
+
+/*
  * route_step_decode_noalloc: the decode route step (route_step for 1..20
  * rows) without a plan and without allocating any memory.  The pages have no
  * counterpart; this exists for callers that cannot allocate device memory:
@@ -300,11 +365,15 @@ route_status route_noalloc_status(int device);
  */
 int route_noalloc_grid(int device);
 
-/* Plan properties: rows, mode, launch grid (CTAs) and split-K segments. */
+/* Plan properties: rows, mode, launch grid (CTAs), split-K segments (decode)
+ * or tiles (prefill), and the latent columns and experts the plan computes
+ * (3584 and 896, or a column shard's share).  -1 for a NULL plan. */
 int route_plan_rows(const route_plan *plan);
 int route_plan_mode(const route_plan *plan);
 int route_plan_grid(const route_plan *plan);
 int route_plan_segments(const route_plan *plan);
+int route_plan_latent_cols(const route_plan *plan);
+int route_plan_experts(const route_plan *plan);
 
 /* Message for the calling thread's most recent failure ("" if none). */
 const char *route_last_error(void);

@@ -17,7 +17,11 @@ The route step of one MoE layer (see ``include/route.h``):
 * ``route_step_host`` -- ``route_step`` with host tensors (transfers included);
   ``HostStep`` -- the same on fixed buffers, checked once and (decode,
   page-locked buffers) captured as a CUDA graph, for serving loops;
-* ``route_set_overlap``, ``route_set_latent_ksplit`` -- plan options.
+* ``route_set_overlap``, ``route_set_latent_ksplit`` -- plan options;
+* ``ShardPlan``, ``route_shard_step``, ``route_merge_candidates`` -- one column
+  shard of the step (its latent columns, its experts and its local top-16)
+  and the merge of the shards' candidates into the final top-16;
+  ``gather_candidates`` is the exchange between them (torch.distributed).
 """
 
 from __future__ import annotations
@@ -58,8 +62,10 @@ EXPORTS = (
     "route_set_overlap", "route_step_decode_noalloc", "route_step_sumsq",
     "route_set_latent_ksplit", "route_host_step_create", "route_host_step_run",
     "route_host_step_destroy", "route_test_poison_scratch", "route_noalloc_status",
-    "route_noalloc_grid",
+    "route_noalloc_grid", "route_prepare_shard", "route_shard_step", "route_merge_candidates",
+    "route_plan_latent_cols", "route_plan_experts",
 )
+SHARD_COUNTS = (1, 2, 4, 7, 8, 14, 16)
 
 
 class RouteError(RuntimeError):
@@ -111,10 +117,17 @@ def lib() -> ctypes.CDLL:
         L.route_noalloc_status.restype = i32
         L.route_noalloc_grid.argtypes = [i32]
         L.route_noalloc_grid.restype = i32
+        L.route_prepare_shard.argtypes = [i32, i32, i32, i32, ctypes.POINTER(vp)]
+        L.route_prepare_shard.restype = i32
+        L.route_shard_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.route_shard_step.restype = i32
+        L.route_merge_candidates.argtypes = [i32, i32, vp, vp, vp, vp, vp]
+        L.route_merge_candidates.restype = i32
         for f in ("route_host_step_create", "route_host_step_run", "route_host_step_destroy",
                   "route_test_poison_scratch"):
             getattr(L, f).restype = i32
-        for f in ("route_plan_rows", "route_plan_mode", "route_plan_grid", "route_plan_segments"):
+        for f in ("route_plan_rows", "route_plan_mode", "route_plan_grid", "route_plan_segments",
+                  "route_plan_latent_cols", "route_plan_experts"):
             getattr(L, f).argtypes = [vp]
             getattr(L, f).restype = i32
         L.route_last_error.argtypes = []
@@ -182,6 +195,29 @@ class Plan:
 
 def route_prepare(mode: int, rows: int, device: int = 0) -> Plan:
     return Plan(mode, rows, device)
+
+
+def shard_columns(num_shards: int) -> tuple[int, int]:
+    """(latent columns, experts) of each of `num_shards` column shards."""
+    return N_LATENT // num_shards, N_EXPERTS // num_shards
+
+
+class ShardPlan(Plan):
+    """A plan for column shard `shard` of `num_shards` (``route_prepare_shard``):
+    latent columns [NL shard, NL (shard + 1)) and experts [NE shard, NE (shard
+    + 1)), NL, NE = ``shard_columns(num_shards)``."""
+
+    def __init__(self, rows: int, shard: int, num_shards: int, device: int = 0):
+        h = ctypes.c_void_p()
+        _check(lib().route_prepare_shard(int(rows), int(device), int(shard), int(num_shards),
+                                         ctypes.byref(h)))
+        self._h = h
+        self.mode = PREFILL
+        self.rows = int(rows)
+        self.device = int(device)
+        self.shard = int(shard)
+        self.num_shards = int(num_shards)
+        self.n_latent, self.n_experts = shard_columns(num_shards)
 
 
 # ---- marshalling helpers ---------------------------------------------------
@@ -292,6 +328,57 @@ def route_step_sumsq(plan: Plan, hidden, W_latent, W_router, latent, logits, ids
     i, w = _topk_ptrs(plan, ids, weights)
     ss = _dev_tensor(latent_sumsq, "latent_sumsq", (plan.rows,), (torch.float32,), plan.device)
     _check(lib().route_step_sumsq(plan.handle, *p, i, w, ss, _stream(stream, plan.device)))
+
+
+def route_shard_step(plan: ShardPlan, hidden, W_latent_shard, W_router_shard, latent_shard,
+                     logits_shard, cand_ids, cand_logits, stream=None) -> None:
+    """One column shard: its latent columns, its logits and its local top-16
+    (global expert ids and their logits)."""
+    torch = _torch()
+    R, d, NL, NE = plan.rows, plan.device, plan.n_latent, plan.n_experts
+    bf = _bf16_types()
+    p = (_dev_tensor(hidden, "hidden", (R, K_HIDDEN), bf, d),
+         _dev_tensor(W_latent_shard, "W_latent_shard", (K_HIDDEN, NL), bf, d),
+         _dev_tensor(W_router_shard, "W_router_shard", (K_HIDDEN, NE), bf, d),
+         _dev_tensor(latent_shard, "latent_shard", (R, NL), bf, d),
+         _dev_tensor(logits_shard, "logits_shard", (R, NE), (torch.float32,), d),
+         _dev_tensor(cand_ids, "cand_ids", (R, TOPK), (torch.int32,), d),
+         _dev_tensor(cand_logits, "cand_logits", (R, TOPK), (torch.float32,), d))
+    _check(lib().route_shard_step(plan.handle, *p, _stream(stream, d)))
+
+
+def route_merge_candidates(cand_ids, cand_logits, ids, weights, stream=None) -> None:
+    """The top-16 and weights of each row from the shards' candidates
+    ([num_shards, rows, 16] ids and logits, shard after shard)."""
+    torch = _torch()
+    if not isinstance(cand_ids, torch.Tensor) or cand_ids.dim() != 3:
+        raise ValueError("cand_ids must be a [num_shards, rows, 16] tensor")
+    W, R = int(cand_ids.shape[0]), int(cand_ids.shape[1])
+    d = cand_ids.device.index if cand_ids.is_cuda else -1
+    p = (_dev_tensor(cand_ids, "cand_ids", (W, R, TOPK), (torch.int32,), d),
+         _dev_tensor(cand_logits, "cand_logits", (W, R, TOPK), (torch.float32,), d),
+         _dev_tensor(ids, "ids", (R, TOPK), (torch.int32,), d),
+         _dev_tensor(weights, "weights", (R, TOPK), (torch.float32,), d))
+    with torch.cuda.device(d):
+        _check(lib().route_merge_candidates(R, W, *p, _stream(stream, d)))
+
+
+def gather_candidates(cand_ids, cand_logits, group=None):
+    """The exchange step of a column-sharded route step, one shard per rank:
+    every rank's [rows, 16] candidate ids and logits all-gathered into the
+    [num_shards, rows, 16] layout ``route_merge_candidates`` reads (the block
+    of group rank r at index r).  Needs an initialised torch.distributed
+    group; device tensors need a GPU backend (NCCL)."""
+    torch = _torch()
+    import torch.distributed as dist
+    W = dist.get_world_size(group)
+    out = []
+    for t in (cand_ids, cand_logits):
+        t = t.contiguous()
+        g = torch.empty((W,) + tuple(t.shape), dtype=t.dtype, device=t.device)
+        dist.all_gather(list(g.unbind(0)), t, group=group)
+        out.append(g)
+    return out[0], out[1]
 
 
 def _host_step_args(plan, hidden_host, W_latent, W_router, latent_host, logits_host, ids_host,

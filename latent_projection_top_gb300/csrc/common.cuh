@@ -84,6 +84,8 @@ struct ProjArgs {
     const int *sched;          // packed tiles of every pair, pair after pair
     const int *sched_off;      // pair p's tiles: sched[sched_off[p] .. sched_off[p + 1])
     float2 *ss_part;           // optional [rows][kSsParts] latent sum-of-squares parts (hi, lo)
+    int n_latent;              // latent columns stored: 3584, or a column shard's share
+    int n_experts;             // router columns of W_router: 896, or a column shard's share
 };
 
 // Decode split-K: 18 column tiles of 256 columns (14 latent, 4 router -- the
@@ -148,5 +150,20 @@ cudaError_t stage_in_launch(const void *src_mapped, void *dst, size_t bytes, cud
 // predecessor wrote).
 cudaError_t topk_launch(const float *logits, int rows, int32_t *ids, float *weights,
                         const float2 *ss_part, float *sumsq, cudaStream_t stream);
+
+// A column shard's local top-16: of the `n` logits of each row (row stride
+// n), the 16 largest (the same ranking), written as global expert ids
+// (id_base + local id) and their logits.
+cudaError_t shard_topk_launch(const float *logits, int rows, int n, int id_base, int32_t *cand_ids,
+                              float *cand_logits, cudaStream_t stream);
+
+// The top-16 of each row over num_shards x 16 candidates (shard-major:
+// [shard][row][16] ids and logits) and their routing weights.
+cudaError_t merge_launch(const int32_t *cand_ids, const float *cand_logits, int rows,
+                         int num_shards, int32_t *ids, float *weights, cudaStream_t stream);
+
+// Column shards: shard s of W owns latent columns [kLatent s / W, kLatent
+// (s+1) / W) and experts [kExperts s / W, kExperts (s+1) / W).
+constexpr int kMaxShards = 16;
 
 }  // namespace route

@@ -417,7 +417,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
             const bool lat = c < kPrefillLatTiles;
             // global column of lane 0 of this warp
             const int xw = (lat ? c : c - kPrefillLatTiles) * 2 * kHalf + (int)rank * kHalf + 32 * lq;
-            const bool valid = lat || xw < kExperts;
+            const bool valid = xw < (lat ? args.n_latent : args.n_experts);
             const int part = c * 8 + (int)rank * 4 + lq;
             const uint32_t acc0 = lanes + (uint32_t)(128 * cs);  // this warp's token rows 128 cs ..
             if (kind == kTileFull) {
@@ -439,7 +439,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
                     if (lat) {
 #pragma unroll
                         for (int jj = 0; jj < 16; ++jj) u[jj] = bf16_bits(__uint_as_float(u[jj]));
-                        store_chunk(u, false, &map_lat, xw, y, true);
+                        store_chunk(u, false, &map_lat, xw, y, valid);
                         if (args.ss_part != nullptr) sumsq_parts(part, y);
                     } else {
                         store_chunk(u, true, &map_lg, xw, y, valid);
@@ -479,7 +479,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
                     const int y = row0 + 128 * cs + 16 * ch;
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) v[jj] = bf16_bits(sum[16 * ch + jj]);
-                    store_chunk(v, false, &map_lat, xw, y, true);
+                    store_chunk(v, false, &map_lat, xw, y, valid);
                     if (args.ss_part != nullptr) sumsq_parts(part, y);
                 }
             }

@@ -33,6 +33,9 @@ struct route_plan {
     const int *sched_tiles[2], *sched_off[2];  // [0] plain, [1] K-split latent
     int sched_pairs[2];
     int pre_ksplit;           // prefill: latent with the general path's K-split arithmetic
+    int num_shards;           // column-shard plans: W (0 for a plan of the whole layer)
+    int shard;                // column-shard plans: this plan's shard, 0 .. W-1
+    int n_lat, n_exp;         // latent columns and experts the plan computes
     unsigned *words;          // device status word (+ spare)
     uint8_t *staging;         // device staging for route_step_host
     size_t staging_bytes;
@@ -219,10 +222,10 @@ route_status encode_all(const route_plan *p, const void *hidden, const void *W_l
     if ((st = cached_map(p->map_h, hidden, kHidden, (uint64_t)p->rows, kKBlock, hbox, "hidden",
                          mh)) != ROUTE_OK)
         return st;
-    if ((st = cached_map(p->map_wl, W_latent, kLatent, kHidden, 64, kKBlock, "W_latent", ml)) !=
-        ROUTE_OK)
+    if ((st = cached_map(p->map_wl, W_latent, (uint64_t)p->n_lat, kHidden, 64, kKBlock, "W_latent",
+                         ml)) != ROUTE_OK)
         return st;
-    return cached_map(p->map_wr, W_router, kExperts, kHidden, 64, kKBlock, "W_router", mr);
+    return cached_map(p->map_wr, W_router, (uint64_t)p->n_exp, kHidden, 64, kKBlock, "W_router", mr);
 }
 
 // The projection (and, for decode with do_topk, the top-16) of one step.
@@ -249,10 +252,10 @@ route_status launch_forward(const route_plan *p, const void *hidden, const void 
     } else {
         // the epilogue's TMA stores: 32 columns x 16 rows per box
         CUtensorMap mlat, mlg;
-        if ((st = cached_map(p->map_lat, latent, kLatent, (uint64_t)p->rows, 32, 16, "latent", &mlat,
-                             false, false)) != ROUTE_OK ||
-            (st = cached_map(p->map_lg, logits, kExperts, (uint64_t)p->rows, 32, 16, "logits", &mlg,
-                             true, false)) != ROUTE_OK)
+        if ((st = cached_map(p->map_lat, latent, (uint64_t)p->n_lat, (uint64_t)p->rows, 32, 16,
+                             "latent", &mlat, false, false)) != ROUTE_OK ||
+            (st = cached_map(p->map_lg, logits, (uint64_t)p->n_exp, (uint64_t)p->rows, 32, 16,
+                             "logits", &mlg, true, false)) != ROUTE_OK)
             return st;
         ProjArgs a = p->pre;
         const int ks = p->pre_ksplit ? 1 : 0;
@@ -271,9 +274,17 @@ route_status launch_forward(const route_plan *p, const void *hidden, const void 
     return ROUTE_OK;
 }
 
+route_status check_whole_plan(const route_plan *p) {
+    route_status st = check_plan(p);
+    if (st != ROUTE_OK) return st;
+    if (p->num_shards != 0)
+        return fail(ROUTE_ERR_PLAN, "a column-shard plan runs route_shard_step only");
+    return ROUTE_OK;
+}
+
 route_status check_forward_args(const route_plan *p, const void *hidden, const void *W_latent,
                                 const void *W_router, const void *latent, const float *logits) {
-    route_status st = check_plan(p);
+    route_status st = check_whole_plan(p);
     if (st != ROUTE_OK) return st;
     if (!hidden || !W_latent || !W_router || !latent || !logits)
         return fail(ROUTE_ERR_NULL, "hidden, W_latent, W_router, latent and logits must be non-NULL");
@@ -285,7 +296,7 @@ route_status check_forward_args(const route_plan *p, const void *hidden, const v
 
 route_status check_topk_args(const route_plan *p, const float *logits, const int32_t *ids,
                              const float *weights) {
-    route_status st = check_plan(p);
+    route_status st = check_whole_plan(p);
     if (st != ROUTE_OK) return st;
     if (!logits || !ids || !weights)
         return fail(ROUTE_ERR_NULL, "logits, ids and weights must be non-NULL");
@@ -303,19 +314,25 @@ route_status run_step(const route_plan *p, const void *hidden, const void *W_lat
 
 // Prefill work lists.  The tiles of a call, in column bands: a band of B
 // column tiles over every 256-row block, then the next band, with B = the
-// pair count over the row blocks (at least 1, at most all 18), so that the
-// pairs at work at one time read few weight tiles and every hidden row block.
-// Each tile goes, in that order, to the pair with the fewest tiles so far.
-bool build_schedule(int rows, bool ksplit, int max_pairs, std::vector<int> &off,
-                    std::vector<int> &tiles, int *pairs) {
+// pair count over the row blocks (at least 1, at most all the columns), so
+// that the pairs at work at one time read few weight tiles and every hidden
+// row block.  Each tile goes, in that order, to the pair with the fewest
+// tiles so far.  The column tiles are the first `lat_tiles` latent tiles and
+// the first `router_tiles` router tiles (all 14 and 4 for a whole layer).
+bool build_schedule(int rows, bool ksplit, int max_pairs, int lat_tiles, int router_tiles,
+                    std::vector<int> &off, std::vector<int> &tiles, int *pairs) {
+    std::vector<int> cols;
+    for (int c = 0; c < lat_tiles; ++c) cols.push_back(c);
+    for (int c = 0; c < router_tiles; ++c) cols.push_back(kPrefillLatTiles + c);
+    const int ncols = (int)cols.size();
     const int row_blocks = (rows + kPrefillBN - 1) / kPrefillBN;
     int band = max_pairs / row_blocks;
-    band = band < 1 ? 1 : band > kPrefillColTiles ? kPrefillColTiles : band;
+    band = band < 1 ? 1 : band > ncols ? ncols : band;
     std::vector<int> order;
-    for (int c0 = 0; c0 < kPrefillColTiles; c0 += band)
+    for (int c0 = 0; c0 < ncols; c0 += band)
         for (int r = 0; r < row_blocks; ++r)
-            for (int c = c0; c < c0 + band && c < kPrefillColTiles; ++c) {
-                const int row0 = r * kPrefillBN;
+            for (int ci = c0; ci < c0 + band && ci < ncols; ++ci) {
+                const int c = cols[ci], row0 = r * kPrefillBN;
                 order.push_back(
                     pack_tile(c, ksplit && c < kPrefillLatTiles ? kTileKsplit : kTileFull, row0));
             }
@@ -449,13 +466,10 @@ route_status noalloc_setup(int device, NoAllocDevice **out) {
     return ROUTE_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-const char *route_last_error(void) { return g_err; }
-
-route_status route_prepare(int mode, int rows, int device, route_plan **out) {
+// A plan of the whole layer (num_shards == 0) or of column shard `shard` of
+// `num_shards` (prefill kernel; checked by the caller).
+route_status prepare_plan(int mode, int rows, int device, int shard, int num_shards,
+                          route_plan **out) {
     g_err[0] = '\0';
     if (!out) return fail(ROUTE_ERR_NULL, "out is NULL");
     *out = nullptr;
@@ -489,6 +503,10 @@ route_status route_prepare(int mode, int rows, int device, route_plan **out) {
     p->mode = mode;
     p->rows = rows;
     p->device = device;
+    p->num_shards = num_shards;
+    p->shard = shard;
+    p->n_lat = num_shards ? kLatent / num_shards : kLatent;
+    p->n_exp = num_shards ? kExperts / num_shards : kExperts;
     p->bn = mode == ROUTE_DECODE ? decode_bn_for(rows) : kPrefillBN;
     const int smem = mode == ROUTE_DECODE ? decode_smem_bytes(p->bn) : prefill_smem_bytes();
     if (smem < 0 || (size_t)smem > prop.sharedMemPerBlockOptin) {
@@ -528,10 +546,13 @@ route_status route_prepare(int mode, int rows, int device, route_plan **out) {
         ProjArgs &a = p->pre;
         a.rows = rows;
         a.timeout_ns = kDefaultTimeoutNs;
+        a.n_latent = p->n_lat;
+        a.n_experts = p->n_exp;
         a.status = p->words + kWordStatus;
         std::vector<int> off[2], tiles[2];
         for (int ks = 0; ks < 2; ++ks)
-            if (!build_schedule(rows, ks == 1, sms / 2, off[ks], tiles[ks], &p->sched_pairs[ks])) {
+            if (!build_schedule(rows, ks == 1, sms / 2, (p->n_lat + 255) / 256,
+                                (p->n_exp + 255) / 256, off[ks], tiles[ks], &p->sched_pairs[ks])) {
                 free_plan(p);
                 return fail(ROUTE_ERR_PLAN, "prefill tile list longer than %d tiles a pair", kMaxPairTiles);
             }
@@ -557,17 +578,17 @@ route_status route_prepare(int mode, int rows, int device, route_plan **out) {
             free_plan(p);
             return cuda_fail(e, "copy the prefill schedule");
         }
-        // per-row latent sum-of-squares parts (route_step_sumsq)
-        p->ws_bytes = (size_t)rows * kSsParts * sizeof(float2);
-        if ((e = cudaMalloc(&p->ws, p->ws_bytes)) != cudaSuccess) {
+        // per-row latent sum-of-squares parts (route_step_sumsq; not for shards)
+        p->ws_bytes = num_shards ? 0 : (size_t)rows * kSsParts * sizeof(float2);
+        if (p->ws_bytes && (e = cudaMalloc(&p->ws, p->ws_bytes)) != cudaSuccess) {
             free_plan(p);
             return cuda_fail(e, "cudaMalloc(sum-of-squares parts)");
         }
         p->segments = (int)tiles[0].size();
         p->grid = 2 * p->sched_pairs[0];
     }
-    p->staging_bytes = staging_size(rows);
-    if ((e = cudaMalloc(&p->staging, p->staging_bytes)) != cudaSuccess) {
+    p->staging_bytes = num_shards ? 0 : staging_size(rows);
+    if (p->staging_bytes && (e = cudaMalloc(&p->staging, p->staging_bytes)) != cudaSuccess) {
         free_plan(p);
         return cuda_fail(e, "cudaMalloc(staging)");
     }
@@ -577,6 +598,32 @@ route_status route_prepare(int mode, int rows, int device, route_plan **out) {
     }
     *out = p;
     return ROUTE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *route_last_error(void) { return g_err; }
+
+route_status route_prepare(int mode, int rows, int device, route_plan **out) {
+    return prepare_plan(mode, rows, device, 0, 0, out);
+}
+
+route_status route_prepare_shard(int rows, int device, int shard, int num_shards,
+                                 route_plan **out) {
+    g_err[0] = '\0';
+    if (!out) return fail(ROUTE_ERR_NULL, "out is NULL");
+    *out = nullptr;
+    if (num_shards < 1 || num_shards > kMaxShards || kExperts % num_shards != 0 ||
+        kExperts / num_shards < kTopK)
+        return fail(ROUTE_ERR_PLAN,
+                    "num_shards must divide %d experts and %d latent columns with at least %d "
+                    "experts a shard, at most %d shards (1, 2, 4, 7, 8, 14 or 16); got %d",
+                    kExperts, kLatent, kTopK, kMaxShards, num_shards);
+    if (shard < 0 || shard >= num_shards)
+        return fail(ROUTE_ERR_PLAN, "shard %d is not in 0..%d", shard, num_shards - 1);
+    return prepare_plan(ROUTE_PREFILL, rows, device, shard, num_shards, out);
 }
 
 route_status route_destroy(route_plan *plan) {
@@ -638,6 +685,49 @@ route_status route_step_sumsq(const route_plan *plan, const void *hidden, const 
                     static_cast<cudaStream_t>(stream), latent_sumsq);
 }
 
+route_status route_shard_step(const route_plan *plan, const void *hidden,
+                              const void *W_latent_shard, const void *W_router_shard,
+                              void *latent_shard, float *logits_shard, int32_t *cand_ids,
+                              float *cand_logits, void *stream) {
+    route_status st = check_plan(plan);
+    if (st != ROUTE_OK) return st;
+    if (plan->num_shards == 0)
+        return fail(ROUTE_ERR_PLAN, "route_shard_step needs a plan from route_prepare_shard");
+    if (!hidden || !W_latent_shard || !W_router_shard || !latent_shard || !logits_shard ||
+        !cand_ids || !cand_logits)
+        return fail(ROUTE_ERR_NULL, "every pointer must be non-NULL");
+    if (!aligned16(hidden) || !aligned16(W_latent_shard) || !aligned16(W_router_shard) ||
+        !aligned16(latent_shard) || !aligned16(logits_shard) || !aligned16(cand_ids) ||
+        !aligned16(cand_logits))
+        return fail(ROUTE_ERR_ALIGN, "every device pointer must be 16-byte aligned");
+    DeviceGuard guard(plan->device);
+    if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((st = launch_forward(plan, hidden, W_latent_shard, W_router_shard, latent_shard,
+                             logits_shard, nullptr, nullptr, 0, nullptr, s)) != ROUTE_OK)
+        return st;
+    const cudaError_t e = shard_topk_launch(logits_shard, plan->rows, plan->n_exp,
+                                            plan->shard * plan->n_exp, cand_ids, cand_logits, s);
+    return e == cudaSuccess ? ROUTE_OK : cuda_fail(e, "shard top-16 kernel launch");
+}
+
+route_status route_merge_candidates(int rows, int num_shards, const int32_t *cand_ids,
+                                    const float *cand_logits, int32_t *ids, float *weights,
+                                    void *stream) {
+    g_err[0] = '\0';
+    if (rows < 1 || rows > ROUTE_PREFILL_MAX_ROWS)
+        return fail(ROUTE_ERR_ROWS, "rows must be 1-%d; got %d", ROUTE_PREFILL_MAX_ROWS, rows);
+    if (num_shards < 1 || num_shards > kMaxShards)
+        return fail(ROUTE_ERR_PLAN, "num_shards must be 1-%d; got %d", kMaxShards, num_shards);
+    if (!cand_ids || !cand_logits || !ids || !weights)
+        return fail(ROUTE_ERR_NULL, "every pointer must be non-NULL");
+    if (!aligned16(cand_ids) || !aligned16(cand_logits) || !aligned16(ids) || !aligned16(weights))
+        return fail(ROUTE_ERR_ALIGN, "every device pointer must be 16-byte aligned");
+    const cudaError_t e = merge_launch(cand_ids, cand_logits, rows, num_shards, ids, weights,
+                                       static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ROUTE_OK : cuda_fail(e, "candidate merge kernel launch");
+}
+
 // Device-mapped address of page-locked host memory, or nullptr for memory the
 // GPU cannot reach directly (pageable memory takes the copy path).
 void *mapped_host(const void *p) {
@@ -670,7 +760,7 @@ route_status route_step_host(const route_plan *plan, const void *hidden_host,
                              const void *W_latent, const void *W_router, void *latent_host,
                              float *logits_host, int32_t *ids_host, float *weights_host,
                              void *stream) {
-    route_status st = check_plan(plan);
+    route_status st = check_whole_plan(plan);
     if (st != ROUTE_OK) return st;
     if (!hidden_host || !W_latent || !W_router || !latent_host || !logits_host || !ids_host ||
         !weights_host)
@@ -755,7 +845,7 @@ route_status route_host_step_create(route_plan *plan, const void *hidden_host,
         return fail(ROUTE_ERR_NULL, "every pointer must be non-NULL");
     if (!aligned16(W_latent) || !aligned16(W_router))
         return fail(ROUTE_ERR_ALIGN, "weight pointers must be 16-byte aligned");
-    if (plan->mode != ROUTE_DECODE)
+    if (plan->mode != ROUTE_DECODE || plan->num_shards != 0)
         return fail(ROUTE_ERR_PLAN, "host steps are prepared for decode plans only");
     DeviceGuard guard(plan->device);
     if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
@@ -954,5 +1044,7 @@ int route_plan_rows(const route_plan *plan) { return plan ? plan->rows : -1; }
 int route_plan_mode(const route_plan *plan) { return plan ? plan->mode : -1; }
 int route_plan_grid(const route_plan *plan) { return plan ? plan->grid : -1; }
 int route_plan_segments(const route_plan *plan) { return plan ? plan->segments : -1; }
+int route_plan_latent_cols(const route_plan *plan) { return plan ? plan->n_lat : -1; }
+int route_plan_experts(const route_plan *plan) { return plan ? plan->n_exp : -1; }
 
 }  // extern "C"

@@ -206,6 +206,74 @@ __device__ __forceinline__ void topk16_warp(const float *row, int32_t *ids_out, 
     weights16_store(mine_key, mine_id, lane, ids_out, w_out);
 }
 
+// The 16 picks (lane i < 16 keeps the i-th, as a key and an id) of the n
+// logits of `row` (n <= kExpertsTopk; entries past n take the removed key 0,
+// which no real logit maps to, so with n >= 16 none is picked), by the same
+// threshold, compaction and ranking as topk16_warp.  All 32 lanes call it.
+__device__ __forceinline__ void topk16_warp_picks(const float *row, int n, int lane, uint2 *cand,
+                                                  uint32_t &mine_key, uint32_t &mine_id) {
+    uint32_t key[kPerLane];
+#pragma unroll
+    for (int j = 0; j < kPerLane; ++j)
+        key[j] = 32 * j + lane < n ? rank_key(row[32 * j + lane]) : 0u;
+    uint32_t lane_max = 0u;
+#pragma unroll
+    for (int j = 0; j < kPerLane; ++j) lane_max = max(lane_max, key[j]);
+    const uint32_t T = max(warp_16th_largest(lane_max, lane), 1u);
+    uint32_t cnt = 0u;
+#pragma unroll
+    for (int j = 0; j < kPerLane; ++j) cnt += (key[j] >= T) ? 1u : 0u;
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    mine_key = 0u;
+    mine_id = 0u;
+    if (total <= (uint32_t)kCandMax) {
+        uint32_t pos = incl - cnt;
+#pragma unroll
+        for (int j = 0; j < kPerLane; ++j)
+            if (key[j] >= T) cand[pos++] = make_uint2(key[j], (uint32_t)(32 * j + lane));
+        __syncwarp();
+        pick16_from_candidates(cand, total, lane, mine_key, mine_id);
+        return;
+    }
+    uint32_t best = 0u;
+    int best_j = 0;
+#pragma unroll
+    for (int j = 0; j < kPerLane; ++j)
+        if (key[j] > best) {
+            best = key[j];
+            best_j = j;
+        }
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, best);
+        const uint32_t c = (best == top) ? (uint32_t)(32 * best_j + lane) : 0xFFFFFFFFu;
+        const uint32_t pick = __reduce_min_sync(0xFFFFFFFFu, c);
+        if (lane == i) {
+            mine_key = top;
+            mine_id = pick;
+        }
+        if ((int)(pick & 31u) == lane) {
+            const int js = (int)(pick >> 5);
+            best = 0u;
+            best_j = 0;
+#pragma unroll
+            for (int j = 0; j < kPerLane; ++j) {
+                if (j == js) key[j] = 0u;
+                if (key[j] > best) {
+                    best = key[j];
+                    best_j = j;
+                }
+            }
+        }
+    }
+}
+
 // Shared memory of topk16_block.
 struct TopkBlockSmem {
     uint32_t tmax[kExpertsTopk / 4];  // one key maximum per thread

@@ -107,8 +107,10 @@ def test_calls_with_null_plan(lib):
     assert lib.route_host_step_destroy(null) == 0
     assert lib.route_test_poison_scratch(null, None) == 3
     assert lib.route_destroy(null) == 0
-    for f in ("route_plan_rows", "route_plan_mode", "route_plan_grid", "route_plan_segments"):
+    for f in ("route_plan_rows", "route_plan_mode", "route_plan_grid", "route_plan_segments",
+              "route_plan_latent_cols", "route_plan_experts"):
         assert getattr(lib, f)(null) == -1
+    assert lib.route_shard_step(null, x, x, x, x, x, x, x, None) == 3
 
 
 def test_binding_refuses_to_run_without_library(monkeypatch, tmp_path):
@@ -145,3 +147,39 @@ def test_binding_checks_tensors_before_any_call():
                            "hidden_host", (4, route.K_HIDDEN), route._bf16_types())
     with pytest.raises(TypeError, match="CPU torch.Tensor"):
         route._host_tensor(None, "hidden_host", (4, route.K_HIDDEN), route._bf16_types())
+
+
+@pytest.mark.parametrize("W", [0, 3, 5, 6, 9, 17, 32, -2])
+def test_shard_counts_outside_the_supported_set_are_rejected(lib, W):
+    """A shard count must divide the 896 experts (and so the 3584 latent
+    columns) with at least 16 experts a shard, at most 16 shards."""
+    h = ctypes.c_void_p(123)
+    assert lib.route_prepare_shard(8, 0, 0, W, ctypes.byref(h)) == 7  # ROUTE_ERR_PLAN
+    assert h.value is None
+
+
+def test_supported_shard_counts_divide_both_widths():
+    for W in route.SHARD_COUNTS:
+        NL, NE = route.shard_columns(W)
+        assert NL * W == route.N_LATENT and NE * W == route.N_EXPERTS and NE >= route.TOPK
+        assert (NL * 2) % 16 == 0 and (NE * 2) % 16 == 0 and (NE * 4) % 16 == 0  # TMA strides
+
+
+def test_shard_index_and_rows_checked_before_the_device(lib):
+    h = ctypes.c_void_p(123)
+    assert lib.route_prepare_shard(8, 0, 8, 8, ctypes.byref(h)) == 7
+    assert lib.route_prepare_shard(8, 0, -1, 8, ctypes.byref(h)) == 7
+    assert lib.route_prepare_shard(0, 0, 0, 8, ctypes.byref(h)) == 1  # ROUTE_ERR_ROWS
+    assert lib.route_prepare_shard(route.PREFILL_MAX_ROWS + 1, 0, 0, 8, ctypes.byref(h)) == 1
+    assert lib.route_prepare_shard(8, 0, 0, 8, None) == 3
+
+
+def test_merge_arguments_checked_before_the_device(lib):
+    x = ctypes.c_void_p(0x1000)
+    odd = ctypes.c_void_p(0x1004)
+    assert lib.route_merge_candidates(0, 2, x, x, x, x, None) == 1
+    assert lib.route_merge_candidates(route.PREFILL_MAX_ROWS + 1, 2, x, x, x, x, None) == 1
+    assert lib.route_merge_candidates(8, 0, x, x, x, x, None) == 7
+    assert lib.route_merge_candidates(8, 17, x, x, x, x, None) == 7
+    assert lib.route_merge_candidates(8, 2, None, x, x, x, None) == 3
+    assert lib.route_merge_candidates(8, 2, x, x, odd, x, None) == 4
