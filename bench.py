@@ -73,6 +73,8 @@ def parse_args():
     p.add_argument("--no-sweep", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--no-spread", action="store_true",
+                   help="skip the 5-run spread and the no-overlap figure (profiling runs)")
     p.add_argument("--prefill-banks", type=int, default=92,
                    help="distinct weight banks of a prefill chunk (one per layer)")
     p.add_argument("--no-overlap", action="store_true",
@@ -717,8 +719,9 @@ def main_ours(args):
     # the same configuration timed the decode page's way: median (min, max)
     # over 5 runs of many graph replays (steady state, no pipeline fill)
     sp = DECODE_SPREAD if decode else PREFILL_SPREAD
-    out["spread"] = dict(summarise(rb.spread(steps, dist=dist, **sp)), method=SPREAD_METHOD)
-    if overlap:
+    if not args.no_spread:
+        out["spread"] = dict(summarise(rb.spread(steps, dist=dist, **sp)), method=SPREAD_METHOD)
+    if overlap and not args.no_spread:
         # the same workload with each step held behind the previous one's tail
         p3, s3, _ = rb.make_steps(wk, rows, nbanks, overlap=False)
         sm = summarise(rb.spread(s3, dist=dist, **sp))

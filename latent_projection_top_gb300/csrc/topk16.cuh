@@ -94,27 +94,31 @@ __device__ __forceinline__ void pick16_from_candidates(uint2 *cand, uint32_t tot
 // exactly as a two-float (TwoSum), q = 1 / (1 + t) as a two-float (FMA
 // residual), s = q (v >= 0) or t * q (v < 0); the 16 s are summed as
 // two-floats in a fixed tree order; w = s / S is rounded once.
-__device__ __forceinline__ void weights16_store(uint32_t mine_key, uint32_t mine_id, int lane,
-                                                int32_t *ids_out, float *w_out) {
-    float s_hi = 0.f, s_lo = 0.f;
-    if (lane < 16) {
-        const float v = key_to_float(mine_key);
-        const float t = expf(-fabsf(v));
-        const float d_hi = 1.0f + t;
-        const float bp = d_hi - 1.0f;
-        const float d_lo = (1.0f - (d_hi - bp)) + (t - bp);
-        const float q_hi = 1.0f / d_hi;
-        float r = fmaf(-q_hi, d_hi, 1.0f);
-        r = fmaf(-q_hi, d_lo, r);
-        const float q_lo = q_hi * r;
-        if (v >= 0.0f || v != v) {
-            s_hi = q_hi;
-            s_lo = q_lo;
-        } else {  // t * (q_hi + q_lo) as a two-float
-            s_hi = t * q_hi;
-            s_lo = fmaf(t, q_hi, -s_hi) + t * q_lo;
-        }
+//
+// sigmoid_terms: s of one pick as a two-float (s_hi, s_lo).
+__device__ __forceinline__ void sigmoid_terms(uint32_t key, float &s_hi, float &s_lo) {
+    const float v = key_to_float(key);
+    const float t = expf(-fabsf(v));
+    const float d_hi = 1.0f + t;
+    const float bp = d_hi - 1.0f;
+    const float d_lo = (1.0f - (d_hi - bp)) + (t - bp);
+    const float q_hi = 1.0f / d_hi;
+    float r = fmaf(-q_hi, d_hi, 1.0f);
+    r = fmaf(-q_hi, d_lo, r);
+    const float q_lo = q_hi * r;
+    if (v >= 0.0f || v != v) {
+        s_hi = q_hi;
+        s_lo = q_lo;
+    } else {  // t * (q_hi + q_lo) as a two-float
+        s_hi = t * q_hi;
+        s_lo = fmaf(t, q_hi, -s_hi) + t * q_lo;
     }
+}
+
+// The fixed-order two-float total of the 16 lanes' terms (lanes 16..31 hold
+// zeros), the weights and the stores.  All 32 lanes call it.
+__device__ __forceinline__ void weights16_store_terms(float s_hi, float s_lo, uint32_t mine_id,
+                                                      int lane, int32_t *ids_out, float *w_out) {
     float tot_hi = s_hi, tot_lo = s_lo;
 #pragma unroll
     for (int off = 8; off > 0; off >>= 1) {
@@ -134,6 +138,13 @@ __device__ __forceinline__ void weights16_store(uint32_t mine_key, uint32_t mine
         ids_out[lane] = (int32_t)mine_id;
         w_out[lane] = q0 + res / tot_hi;
     }
+}
+
+__device__ __forceinline__ void weights16_store(uint32_t mine_key, uint32_t mine_id, int lane,
+                                                int32_t *ids_out, float *w_out) {
+    float s_hi = 0.f, s_lo = 0.f;
+    if (lane < 16) sigmoid_terms(mine_key, s_hi, s_lo);
+    weights16_store_terms(s_hi, s_lo, mine_id, lane, ids_out, w_out);
 }
 
 // The calling warp selects row `row` (896 logits in global or shared memory,
@@ -277,26 +288,37 @@ __device__ __forceinline__ void topk16_warp_picks(const float *row, int n, int l
 // Shared memory of topk16_block.
 struct TopkBlockSmem {
     uint32_t tmax[kExpertsTopk / 4];  // one key maximum per thread
+    alignas(16) uint32_t lmax[32];    // maxima of seven threads' maxima
     uint32_t T;
     uint32_t count;
     uint2 cand[kCandMax];
+    uint4 pick[16];                   // (key, id, s_hi, s_lo) of the picks in rank order
 };
 
 // The same selection by the 224 threads that hold a row, four logits each
-// (v[j] with ids id[j]), so that the threshold and the candidate compaction
-// take every thread's share at once.  The threshold is the one above: each
-// lane of warp 0 takes the maximum of seven threads' maxima (28 logits), and
-// T = the 16th largest of those 32.  Candidates >= T are compacted with a
-// shared counter, one atomic per warp (their order is not fixed; the
-// ranking is).  Rows with more
-// than kCandMax candidates fall back to topk16_warp over `row`, the same 896
-// logits in shared memory.  Every one of the 224 threads calls it; it uses
-// named barrier `bar`.
+// (v[j] with ids id[j]), spread over every thread so that each step is a
+// short one:
+//  1. the threshold above: each lane of warp 0 takes the maximum of seven
+//     threads' maxima (28 logits); T = the 16th largest of those 32, found
+//     by counting (a value's rank is the number of values that precede it,
+//     equal values ordered by lane);
+//  2. candidates >= T are compacted with a shared counter, one atomic per
+//     warp (their order is not fixed; the ranking is);
+//  3. each candidate's rank is counted by a quad of threads, each comparing
+//     it with a quarter of the candidates, the four counts added by
+//     shuffles; ranks 0..15 are the picks, whose sigmoid terms the quad
+//     computes before storing them in rank order;
+//  4. warp 0 sums the terms and stores ids and weights.
+// Rows with more than kCandMax candidates fall back to topk16_warp over
+// `row`, the same 896 logits in global memory.  Every one of the 224 threads
+// calls it; it uses named barrier `bar`.
 __device__ __forceinline__ void topk16_block(const float (&v)[4], const int (&id)[4],
                                              const float *row, int tid, int bar,
                                              TopkBlockSmem &sh, int32_t *ids_out,
                                              float *w_out) {
-    constexpr int kThreads = kExpertsTopk / 4;
+    constexpr int kThreads = kExpertsTopk / 4;  // 224
+    constexpr int kQuads = kThreads / 4;        // 56
+    static_assert(2 * kQuads >= kCandMax, "two candidates a quad cover the buffer");
     uint32_t key[4];
     uint32_t m = 0u;
 #pragma unroll
@@ -307,18 +329,28 @@ __device__ __forceinline__ void topk16_block(const float (&v)[4], const int (&id
     sh.tmax[tid] = m;
     if (tid == 0) sh.count = 0u;
     asm volatile("barrier.sync %0, %1;" ::"r"(bar), "n"(kThreads) : "memory");
+    const int lane = tid & 31;
     if (tid < 32) {
         uint32_t lm = 0u;
 #pragma unroll
         for (int j = 0; j < kThreads / 32; ++j) lm = max(lm, sh.tmax[tid + 32 * j]);
-        const uint32_t T = warp_16th_largest(lm, tid);
-        if (tid == 0) sh.T = T;
+        sh.lmax[lane] = lm;
+        __syncwarp();
+        uint32_t before = 0u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint4 o = reinterpret_cast<const uint4 *>(sh.lmax)[j];
+            const uint32_t ov[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                before += (ov[e] > lm || (ov[e] == lm && 4 * j + e < lane)) ? 1u : 0u;
+        }
+        if (before == 15u) sh.T = lm;  // exactly one lane holds rank 15
     }
     asm volatile("barrier.sync %0, %1;" ::"r"(bar), "n"(kThreads) : "memory");
     const uint32_t T = sh.T;
     // Compaction, one shared atomic per warp: a ballot per key slot gives
     // each candidate its place within the warp's share.
-    const int lane = tid & 31;
     const uint32_t below = (1u << lane) - 1u;
     uint32_t ball[4], wcount = 0u;
 #pragma unroll
@@ -338,15 +370,40 @@ __device__ __forceinline__ void topk16_block(const float (&v)[4], const int (&id
         base += __popc(ball[j]);
     }
     asm volatile("barrier.sync %0, %1;" ::"r"(bar), "n"(kThreads) : "memory");
-    if (tid >= 32) return;
     const uint32_t total = sh.count;
-    if (total > (uint32_t)kCandMax) {
-        topk16_warp(row, ids_out, w_out, tid, sh.cand);
+    if (total > (uint32_t)kCandMax) {  // the same for every thread
+        if (tid < 32) topk16_warp(row, ids_out, w_out, tid, sh.cand);
         return;
     }
-    uint32_t mine_key, mine_id;
-    pick16_from_candidates(sh.cand, total, tid, mine_key, mine_id);
-    weights16_store(mine_key, mine_id, tid, ids_out, w_out);
+    const uint32_t q = (uint32_t)tid >> 2, part = (uint32_t)tid & 3u;
+    const bool has0 = q < total, has1 = q + kQuads < total;
+    const uint2 c0 = has0 ? sh.cand[q] : make_uint2(0u, 0xFFFFFFFFu);
+    const uint2 c1 = has1 ? sh.cand[q + kQuads] : make_uint2(0u, 0xFFFFFFFFu);
+    uint32_t rank0 = 0u, rank1 = 0u;
+#pragma unroll 4
+    for (uint32_t j = part; j < total; j += 4u) {
+        const uint2 o = sh.cand[j];
+        rank0 += (o.x > c0.x || (o.x == c0.x && o.y < c0.y)) ? 1u : 0u;
+        rank1 += (o.x > c1.x || (o.x == c1.x && o.y < c1.y)) ? 1u : 0u;
+    }
+    rank0 += __shfl_xor_sync(0xFFFFFFFFu, rank0, 1);
+    rank1 += __shfl_xor_sync(0xFFFFFFFFu, rank1, 1);
+    rank0 += __shfl_xor_sync(0xFFFFFFFFu, rank0, 2);
+    rank1 += __shfl_xor_sync(0xFFFFFFFFu, rank1, 2);
+    // Parts 0 and 1 of the quad place candidates c0 and c1 (ranks are distinct).
+    const bool mine = part == 0u ? has0 && rank0 < 16u : part == 1u && has1 && rank1 < 16u;
+    if (mine) {
+        const uint2 c = part == 0u ? c0 : c1;
+        float s_hi, s_lo;
+        sigmoid_terms(c.x, s_hi, s_lo);
+        sh.pick[part == 0u ? rank0 : rank1] =
+            make_uint4(c.x, c.y, __float_as_uint(s_hi), __float_as_uint(s_lo));
+    }
+    asm volatile("barrier.sync %0, %1;" ::"r"(bar), "n"(kThreads) : "memory");
+    if (tid >= 32) return;
+    uint4 p = make_uint4(0u, 0u, 0u, 0u);
+    if (lane < 16) p = sh.pick[lane];
+    weights16_store_terms(__uint_as_float(p.z), __uint_as_float(p.w), p.y, lane, ids_out, w_out);
 }
 
 }  // namespace route
