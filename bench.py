@@ -18,8 +18,10 @@ step): `HostStep`, the checked-once form of route_step_host, with the plain
 route_step_host call timed beside it.
 `cpu_baseline` times the oracle on the host cores on a bounded sample.
 
-Multi-GPU: the route step does not shard (the weights are per layer and the
-rows are few), so N GPUs run N independent replicas ("scaling": "weak").
+Multi-GPU: the step this benchmark times runs on one GPU (the weights are per
+layer and the rows are few), so N GPUs run N independent replicas ("scaling":
+"weak").  The library's column-shard plans are the sharded form; their
+exchange is the caller's collective and is not timed here.
 
 `--impl reference` times the oracle itself (the only reference this work
 has), on a bounded sample per step, and prints the same line.

@@ -11,8 +11,8 @@
 // the hidden operand and run as one N = 3584 + 896 problem.
 //
 // The weights are [K, N] with N contiguous, so their tensor-core operand is
-// MN-major.  A tile is 256 weight columns (the MMA's M) by 256 or 128 token
-// rows (its N), computed by a cluster of two CTAs with
+// MN-major.  A tile is 256 weight columns (the MMA's M) by 256 token rows
+// (its N), computed by a cluster of two CTAs with
 // tcgen05.mma.cta_group::2: each CTA stages its 128 weight columns (A) and
 // its half of the token rows (B) per 64-deep k-block, and holds its 128
 // weight columns x N token rows of the FP32 accumulator in its own TMEM.
@@ -20,7 +20,9 @@
 // Tile kinds (the host builds each pair's list; see common.cuh):
 //   plain: one accumulation over the whole K; the epilogue stores the latent
 //     (rounded to BF16, with per-row sum-of-squares parts when asked) or the
-//     FP32 router logits.
+//     FP32 router logits.  Columns past the plan's latent or expert count (a
+//     column shard's share, or 896 experts in four 256-column tiles) are not
+//     stored.
 //   K-split (latent): the general path's eight 896-deep K slices (same page,
 //     Numerics bullet and commit body) as eight jobs, each slice's result
 //     rounded to BF16 and added in FP32, in slice order, to a running sum the
