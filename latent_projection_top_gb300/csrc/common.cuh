@@ -97,9 +97,7 @@ constexpr int kDTiles = kDLatTiles + kDRouterTiles;                        // 18
 constexpr int kMaxGrid = 256;
 // device words: [0] status (the rest spare)
 constexpr int kWordStatus = 0;
-constexpr int kWordSsCount = 8;  // [8, 8 + 20): per-row arrivals of latent sum-of-squares parts
 constexpr int kWords = 64;
-static_assert(kWordSsCount + kDecodeMaxRows <= kWords, "word area");
 
 struct DecodeArgs {
     int rows;            // 1..20
@@ -120,7 +118,6 @@ struct DecodeArgs {
     int32_t *ids;
     float *weights;
     float *sumsq;                // optional [rows]: sum of squares of each latent row
-    float2 *ss_part;             // with sumsq: [kDecodeMaxRows][14] per-tile parts (hi, lo)
 };
 
 // Internal launchers (defined next to their kernels).  Every launch uses

