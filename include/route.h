@@ -141,9 +141,12 @@ route_status route_step(const route_plan *plan, const void *hidden, const void *
  * instead of reducing it", Reviewer Notes: an FP32 sum of squares for the
  * latent norm).  The squares are exact in FP32 and are summed as two-floats
  * in a fixed order, then rounded once, so the result is bitwise reproducible.
- * Prefill computes it in the top-16 kernel; decode in the kernel that
- * finishes the split-K sums.  latent, logits, ids and weights are exactly
- * those route_step writes.  NULL latent_sumsq: ROUTE_ERR_NULL.
+ * Prefill: the projection's epilogue writes two-float parts of the values it
+ * stores and the top-16 kernel adds them; decode: the kernel that finishes
+ * the split-K sums runs as one thread-block cluster per row, whose latent
+ * CTAs hand their parts to the row's router CTA.  latent, logits, ids and
+ * weights are exactly those route_step writes.  NULL latent_sumsq:
+ * ROUTE_ERR_NULL.
  */
 route_status route_step_sumsq(const route_plan *plan, const void *hidden, const void *W_latent,
                               const void *W_router, void *latent, float *logits, int32_t *ids,
