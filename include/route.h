@@ -249,11 +249,11 @@ route_status route_set_latent_ksplit(route_plan *plan, int enable);
 route_status route_test_stall(route_plan *plan, int enable, uint64_t timeout_ns);
 
 /*
- * route_test_poison_scratch: TEST HOOK.  Fill the plan's split-K scratch (the
- * partials and the sum-of-squares parts, not the arrival counters) with 0xFF
- * bytes on `stream`, so that a test can show that no launch reads a partial
- * it did not write first.  Prefill plans keep no partials: a no-op.
- * Capturable in a CUDA graph.
+ * route_test_poison_scratch: TEST HOOK.  Fill the plan's scratch (decode:
+ * the split-K partials; prefill: the latent sum-of-squares parts; column
+ * shards keep none: a no-op) with 0xFF bytes on `stream`, so that a test can
+ * show that no launch reads scratch it did not write first.  Capturable in a
+ * CUDA graph.
  */
 route_status route_test_poison_scratch(const route_plan *plan, void *stream);
 
@@ -359,6 +359,17 @@ route_status route_step_decode_noalloc(int rows, const void *hidden, const void 
  * any CUDA call.  Allocates nothing.
  */
 route_status route_noalloc_status(int device);
+
+/*
+ * route_test_noalloc_stall: TEST HOOK, as route_test_stall for the calls of
+ * route_step_decode_noalloc on `device` (set up on first use, like a call):
+ * with enable != 0 each CTA of the weight stream skips a copy so that its
+ * wait gives up after timeout_ns (0: 1 ms) and route_noalloc_status reports
+ * ROUTE_ERR_DEVICE_TIMEOUT; enable == 0 restores the default bound (2 s).
+ * device outside 0..63: ROUTE_ERR_DEVICE.  Not for concurrent use with calls
+ * on the device.
+ */
+route_status route_test_noalloc_stall(int device, int enable, uint64_t timeout_ns);
 
 /*
  * route_noalloc_grid: the CTA count route_step_decode_noalloc's weight stream

@@ -63,7 +63,7 @@ EXPORTS = (
     "route_set_latent_ksplit", "route_host_step_create", "route_host_step_run",
     "route_host_step_destroy", "route_test_poison_scratch", "route_noalloc_status",
     "route_noalloc_grid", "route_prepare_shard", "route_shard_step", "route_merge_candidates",
-    "route_plan_latent_cols", "route_plan_experts",
+    "route_plan_latent_cols", "route_plan_experts", "route_test_noalloc_stall",
 )
 SHARD_COUNTS = (1, 2, 4, 7, 8, 14, 16)
 
@@ -123,6 +123,8 @@ def lib() -> ctypes.CDLL:
         L.route_shard_step.restype = i32
         L.route_merge_candidates.argtypes = [i32, i32, vp, vp, vp, vp, vp]
         L.route_merge_candidates.restype = i32
+        L.route_test_noalloc_stall.argtypes = [i32, i32, ctypes.c_uint64]
+        L.route_test_noalloc_stall.restype = i32
         for f in ("route_host_step_create", "route_host_step_run", "route_host_step_destroy",
                   "route_test_poison_scratch"):
             getattr(L, f).restype = i32

@@ -1028,6 +1028,21 @@ route_status route_noalloc_status(int device) {
                 status);
 }
 
+route_status route_test_noalloc_stall(int device, int enable, uint64_t timeout_ns) {
+    g_err[0] = '\0';
+    if (device < 0 || device >= kNoAllocMaxDevices)
+        return fail(ROUTE_ERR_DEVICE, "device %d is out of range", device);
+    DeviceGuard guard(device);
+    if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+    NoAllocDevice *d = nullptr;
+    route_status st = noalloc_setup(device, &d);
+    if (st != ROUTE_OK) return st;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    d->base.test_stall = enable ? 1 : 0;
+    d->base.timeout_ns = enable ? (timeout_ns ? timeout_ns : 1000000ull) : kDefaultTimeoutNs;
+    return ROUTE_OK;
+}
+
 int route_noalloc_grid(int device) {
     cudaDeviceProp prop;
     if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) {

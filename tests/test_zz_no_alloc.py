@@ -111,3 +111,48 @@ def test_noalloc_matches_route_step_on_two_calls(rows):
             lg_g, lg_w = g[1].view(np.float32), w[1].view(np.float32)
             assert np.allclose(lg_g, lg_w, rtol=1e-5, atol=1e-6)
         assert lib.route_noalloc_status(0) == 0, lib.route_last_error().decode()
+
+
+def test_noalloc_stall_hook_rejects_a_device_out_of_range():
+    route.build()
+    lib = route.lib()
+    for dev in (-1, 64):
+        assert lib.route_test_noalloc_stall(dev, 1, 0) == 8  # ROUTE_ERR_DEVICE
+
+
+@pytest.mark.gpu
+def test_noalloc_timeout_is_reported_then_cleared():
+    """A wait of route_step_decode_noalloc that runs out (the stall hook) is
+    reported by route_noalloc_status, which then clears it; the next call,
+    without the hook, matches route_step again."""
+    assert torch.cuda.is_available(), "GPU test needs a CUDA device"
+    route.build()
+    lib = route.lib()
+    torch.cuda.set_device(0)
+    rows = 8
+    wk = synth.WORKLOADS["decode_r8"]
+    stream = torch.cuda.current_stream(0)
+    hid = _dev(synth.hidden(wk.seed, 2, rows))
+    wl, wr = (_dev(w) for w in synth.weight_bank(wk.seed, 2))
+    args = (_p(hid), _p(wl), _p(wr))
+    try:
+        assert lib.route_test_noalloc_stall(0, 1, 1_000_000) == 0, lib.route_last_error().decode()
+        got = _outputs(rows)
+        assert lib.route_step_decode_noalloc(rows, *args, *(_p(t) for t in got),
+                                             ctypes.c_void_p(stream.cuda_stream)) == 0
+        torch.cuda.synchronize()
+        assert lib.route_noalloc_status(0) == route.STATUS_CODES["ROUTE_ERR_DEVICE_TIMEOUT"]
+        assert lib.route_noalloc_status(0) == 0  # cleared by the query
+    finally:
+        assert lib.route_test_noalloc_stall(0, 0, 0) == 0
+    want = _outputs(rows)
+    with route.Plan(route.DECODE, rows) as plan:
+        route.route_step(plan, hid, wl, wr, *want)
+        route.route_device_status(plan)
+    got = _outputs(rows)
+    assert lib.route_step_decode_noalloc(rows, *args, *(_p(t) for t in got),
+                                         ctypes.c_void_p(stream.cuda_stream)) == 0
+    torch.cuda.synchronize()
+    assert lib.route_noalloc_status(0) == 0
+    for name, a, b in zip(("latent", "logits", "ids", "weights"), _host(got), _host(want)):
+        assert np.array_equal(a, b), f"{name} differs after the stall"
