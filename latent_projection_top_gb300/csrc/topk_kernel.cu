@@ -33,15 +33,26 @@ namespace {
 
 constexpr int kRowsPerBlock = 8;
 
-// Lane l adds parts l, l + 32, ... in order, then a fixed tree over the lanes.
-__device__ __forceinline__ float row_sumsq_from_parts(const float2 *parts, int lane) {
+// A row's sum-of-squares parts in two steps, so that their loads overlap the
+// top-16's: lane l loads parts l, l + 32, ... (row_parts_load), then adds
+// them in that order and a fixed tree joins the lanes (row_parts_sum).
+constexpr int kPartsPerLane = (kSsParts + 31) / 32;  // 4
+
+__device__ __forceinline__ void row_parts_load(const float2 *parts, int lane,
+                                               float2 (&p)[kPartsPerLane]) {
+#pragma unroll
+    for (int j = 0; j < kPartsPerLane; ++j)
+        p[j] = lane + 32 * j < kSsParts ? __ldcg(parts + lane + 32 * j) : make_float2(0.f, 0.f);
+}
+
+__device__ __forceinline__ float row_parts_sum(const float2 (&p)[kPartsPerLane], int lane) {
     float hi = 0.f, lo = 0.f;
 #pragma unroll
-    for (int j = lane; j < kSsParts; j += 32) {
-        const float2 p = __ldcg(parts + j);
-        two_sum_acc(hi, lo, p.x);
-        lo += p.y;
-    }
+    for (int j = 0; j < kPartsPerLane; ++j)
+        if (lane + 32 * j < kSsParts) {
+            two_sum_acc(hi, lo, p[j].x);
+            lo += p[j].y;
+        }
     warp_two_sum(hi, lo);
     return two_float_value(hi, lo);
 }
@@ -57,10 +68,12 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock)
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * kRowsPerBlock + warp;
     if (row >= rows) return;  // whole warps leave together
+    float2 parts[kPartsPerLane];
+    if (sumsq != nullptr) row_parts_load(ss_part + (size_t)row * kSsParts, lane, parts);
     topk16_warp(logits + (size_t)row * kExperts, ids + (size_t)row * kTopK,
                 weights + (size_t)row * kTopK, lane, cand[warp]);
     if (sumsq != nullptr) {
-        const float ss = row_sumsq_from_parts(ss_part + (size_t)row * kSsParts, lane);
+        const float ss = row_parts_sum(parts, lane);
         if (lane == 0) sumsq[row] = ss;
     }
 }
