@@ -28,8 +28,9 @@
  *    enqueued asynchronously; no entry point synchronises the device unless it
  *    says so.  Forward calls never allocate and may be captured in a CUDA
  *    graph.
- *  - A plan holds scratch memory (split-K partials and counters), so one plan
- *    must not run on two streams at the same time.
+ *  - A plan holds scratch memory (split-K partials or sum-of-squares parts,
+ *    and a status word), so one plan must not run on two streams at the same
+ *    time.
  *  - Errors are status codes; no C++ exception crosses this interface.
  *    route_last_error() returns a message for the calling thread's last
  *    failure.
@@ -198,9 +199,10 @@ route_status route_host_step_destroy(route_host_step *step);
 
 /*
  * route_device_status: synchronise the plan's device, then report (and clear)
- * the device-side error word that kernels set instead of hanging: ROUTE_OK
- * or ROUTE_ERR_DEVICE_TIMEOUT (a bounded wait expired; outputs of that launch
- * are invalid and the plan's split-K counters have been cleared).
+ * the device-side error word that kernels set instead of hanging or
+ * faulting: ROUTE_OK, ROUTE_ERR_DEVICE_TIMEOUT (a bounded wait expired) or,
+ * in the checked library, ROUTE_ERR_DEVICE_BOUNDS (an index out of range was
+ * skipped); the outputs of that launch are invalid.
  */
 route_status route_device_status(const route_plan *plan);
 
@@ -354,7 +356,7 @@ route_status route_step_decode_noalloc(int rows, const void *hidden, const void 
  * route_noalloc_status: synchronises `device` and reports whether a kernel of
  * route_step_decode_noalloc on it gave up waiting (ROUTE_ERR_DEVICE_TIMEOUT;
  * the outputs of that call are invalid) since the last query, then clears
- * the fixed array's status and counters.  ROUTE_OK when nothing failed or no
+ * the fixed array's status word.  ROUTE_OK when nothing failed or no
  * call has run on the device.  device outside 0..63: ROUTE_ERR_DEVICE before
  * any CUDA call.  Allocates nothing.
  */

@@ -30,12 +30,12 @@
 // decode_finish_kernel -- at most one small CTA per SM, so that it fits next
 //   to a stream CTA: one CTA per row sums the row's 896 router logits and
 //   runs the top-16 on them with all its threads; the others sum the latent
-//   tiles, two or four (row, tile) items per memory round trip (and, when
-//   asked, each latent row's sum of squares, or the general path's K-split
-//   latent).  Slots are
-//   summed in segment order as two-floats and rounded once, so results are
-//   bitwise reproducible and a row's bits do not depend on the row count
-//   (the partition depends only on the grid).
+//   tiles, two or four (row, tile) items per memory round trip (or the
+//   general path's K-split latent).  Slots are summed in segment order as
+//   two-floats and rounded once, so results are bitwise reproducible and a
+//   row's bits do not depend on the row count (the partition depends only on
+//   the grid).  With each latent row's sum of squares asked for, the same
+//   work runs as decode_finish_ss_kernel, one thread-block cluster per row.
 //
 // Programmatic dependent launch: both kernels let their successor launch at
 // once.  The stream kernel prefetches its first weight boxes (model

@@ -818,7 +818,7 @@ route_status route_device_status(const route_plan *plan) {
         cudaSuccess)
         return cuda_fail(e, "read device status");
     if (status == 0) return ROUTE_OK;
-    cudaMemset(plan->words, 0, kWords * sizeof(unsigned));  // status and counters
+    cudaMemset(plan->words, 0, kWords * sizeof(unsigned));  // the status word area
     cudaDeviceSynchronize();
     if (status & kStatusBounds)
         return fail(ROUTE_ERR_DEVICE_BOUNDS,
