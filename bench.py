@@ -34,6 +34,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -102,11 +103,18 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+_COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
+
+
 def kernel_source_sha(kernel: str):
+    """Hash of a kernel's sources with comments and whitespace removed, so
+    that an edit of a comment keeps a recorded ncu figure valid and any change
+    of the code voids it."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            code = _COMMENT.sub(" ", f.read())
+        h.update(" ".join(code.split()).encode())
     return h.hexdigest()[:16]
 
 
