@@ -785,7 +785,7 @@ def sweep(rb, dist, peaks, args):
             rb.route.route_device_status(plan)
             plan.close()
             t = sm["median"] / 1e6
-            sfx = "" if ov else "_without_overlap"
+            sfx = "_with_overlap" if ov else ""
             entry.update({"us_per_layer" + sfx: sm["median"], "us_spread" + sfx: sm,
                           "rows_per_s" + sfx: round(rows / t, 1),
                           "achieved_gbs" + sfx: round(algo / t / 1e9, 1),
@@ -818,7 +818,9 @@ def sweep(rb, dist, peaks, args):
              "note": "burst: one 92-layer graph after two (against the burst bf16 peak); "
                      "sustained: 5 runs of 10 such graphs back to back, under the power cap "
                      "(against the sustained peak)"}
-        for ov in (True, False):
+        # the plain mode first (always valid); overlap beside it: for prefill
+        # its gain varies from box to box and has been negative
+        for ov in (False, True):
             plan, steps, _ = rb.make_steps(wk, rows, nb, overlap=ov)
             p2, gsteps, _ = rb.make_steps(wk, rows, nb, gemm_only=True, overlap=ov)
             tb = dist.max(rb.run(steps, 92, 2 * 92, dist, graph_len=92)[0]) / 1e3 / 92
@@ -828,7 +830,7 @@ def sweep(rb, dist, peaks, args):
             rb.route.route_device_status(plan)
             rb.route.route_device_status(p2)
             t, tg = st["median"] / 1e6, gm["median"] / 1e6
-            sfx = "" if ov else "_without_overlap"
+            sfx = "_with_overlap" if ov else ""
             e.update({"us_per_layer" + sfx: round(tb * 1e6, 3),
                       "chunk_ms_92_layers" + sfx: round(tb * 92 * 1e3, 3),
                       "rows_per_s" + sfx: round(rows / tb, 1),
@@ -839,7 +841,7 @@ def sweep(rb, dist, peaks, args):
                       "gemm_us_sustained" + sfx: gm["median"], "gemm_us_spread_sustained" + sfx: gm,
                       "frac_sustained" + sfx: round(
                           flop / tg / 1e12 / peaks["bf16_tflops_sustained"], 4)})
-            if rows == 3072 and ov:
+            if rows == 3072 and not ov:
                 e["per_layer_us"] = rb.per_layer_us(steps[:92], dist)
             plan.close()
             p2.close()
