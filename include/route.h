@@ -274,19 +274,23 @@ route_status route_test_poison_scratch(const route_plan *plan, void *stream);
  * are what that page's tests and the first page's tests name.  The exchange
  * itself (an all-gather of the candidates, and of the latent and logit
  * columns where the caller wants them whole) is the caller's collective;
- * this library computes each shard and the merge.  Every result of shard s
- * equals the matching columns of route_step on a prefill plan of the same
- * rows (the per-column arithmetic is the same), so the merged ids and
- * weights are those of the top-16 of the whole logit row.
+ * this library computes each shard and the merge.  The merged ids and
+ * weights are those of the top-16 of the whole logit row the shards computed.
  *
  * route_prepare_shard: a plan for shard `shard` (0 <= shard < num_shards) of
  * `num_shards` W in {1, 2, 4, 7, 8, 14, 16} (W divides 896 experts, with at
- * least 16 experts a shard), for 1 <= rows <= 65536 on `device`; it runs the
- * prefill kernel over the shard's column tiles.  Anything else returns
- * ROUTE_ERR_PLAN or ROUTE_ERR_ROWS before touching the device.  A shard plan
- * runs route_shard_step (and the set-up calls route_set_overlap,
- * route_set_latent_ksplit, route_test_stall, route_device_status); every
- * other step entry point refuses it with ROUTE_ERR_PLAN.
+ * least 16 experts a shard), for 1 <= rows <= 65536 on `device`.  Up to 20
+ * rows it runs the decode weight stream (split-K over the SMs) over the
+ * shard's column tiles and a kernel that sums the partials and picks the
+ * candidates: the decode path's arithmetic, within the same bounds of the
+ * float64 values.  Above 20 rows it runs the prefill kernel over the shard's
+ * column tiles, and every result equals the matching columns of route_step
+ * on a prefill plan of the same rows (the per-column arithmetic is the
+ * same).  Anything else returns ROUTE_ERR_PLAN or ROUTE_ERR_ROWS before
+ * touching the device.  A shard plan runs route_shard_step (and the set-up
+ * calls route_set_overlap, route_set_latent_ksplit -- above 20 rows only --,
+ * route_test_stall, route_device_status); every other step entry point
+ * refuses it with ROUTE_ERR_PLAN.
  */
 route_status route_prepare_shard(int rows, int device, int shard, int num_shards,
                                  route_plan **out);
@@ -302,7 +306,8 @@ route_status route_prepare_shard(int rows, int device, int shard, int num_shards
  *   cand_ids       [rows, 16]   int32 (written) the shard's top-16, global
  *                                               expert ids (s NE + local id)
  *   cand_logits    [rows, 16]   FP32  (written) their logits
- * Two kernels on `stream`: the projection, then the shard's top-16.
+ * Two kernels on `stream`: the projection, then the shard's top-16 (up to
+ * 20 rows: the weight stream, then the split-K sums and the top-16).
  */
 route_status route_shard_step(const route_plan *plan, const void *hidden,
                               const void *W_latent_shard, const void *W_router_shard,

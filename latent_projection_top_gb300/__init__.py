@@ -214,7 +214,8 @@ class ShardPlan(Plan):
         _check(lib().route_prepare_shard(int(rows), int(device), int(shard), int(num_shards),
                                          ctypes.byref(h)))
         self._h = h
-        self.mode = PREFILL
+        # up to 20 rows the decode weight stream, else the prefill GEMM
+        self.mode = DECODE if int(rows) <= DECODE_MAX_ROWS else PREFILL
         self.rows = int(rows)
         self.device = int(device)
         self.shard = int(shard)

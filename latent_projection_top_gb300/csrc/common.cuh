@@ -105,6 +105,8 @@ struct DecodeArgs {
     int test_stall;      // test hook: skip each CTA's last copy so a wait must time out
     int overlap;         // read hidden before the grid dependency resolves
     int ksplit;          // latent with the general path's K-split arithmetic
+    int lat_tiles;       // latent column tiles (14; a column shard's: ceil(its columns / 256))
+    int tiles;           // latent + router column tiles (18, or a column shard's)
     unsigned long long timeout_ns;
     int cta_unit[kMaxGrid + 1];  // CTA g owns units [cta_unit[g], cta_unit[g+1]); unit u =
                                  // (tile u / 112, k-block u % 112)
@@ -147,6 +149,16 @@ cudaError_t stage_in_launch(const void *src_mapped, void *dst, size_t bytes, cud
 // predecessor wrote).
 cudaError_t topk_launch(const float *logits, int rows, int32_t *ids, float *weights,
                         const float2 *ss_part, float *sumsq, cudaStream_t stream);
+
+// A column shard at decode sizes (1..20 rows): the split-K weight stream over
+// the shard's args.tiles column tiles, then a kernel that sums the partials
+// into the shard's latent [rows, n_lat] and logits [rows, n_exp] (args.latent,
+// args.logits) and writes the shard's top-16 as candidates (global ids
+// id_base + local id, and their logits).
+cudaError_t decode_shard_launch(int bn, const CUtensorMap &map_h, const CUtensorMap &map_wl,
+                                const CUtensorMap &map_wr, const DecodeArgs &args, int n_lat,
+                                int n_exp, int id_base, int32_t *cand_ids, float *cand_logits,
+                                cudaStream_t stream);
 
 // A column shard's local top-16: of the `n` logits of each row (row stride
 // n), the 16 largest (the same ranking), written as global expert ids

@@ -243,9 +243,9 @@ __global__ void __maxnreg__(BN == 16 ? 72 : 80)
             const int n_pre = n_units < C::kStages ? n_units : C::kStages;
             auto weights_of = [&](int u, uint32_t a, uint32_t bar) {
                 const int t = u / kKBlocks, kb = u % kKBlocks;
-                const bool lat = t < kDLatTiles;
+                const bool lat = t < args.lat_tiles;
                 const CUtensorMap *wmap = lat ? &map_wl : &map_wr;
-                const int x0 = (lat ? t : t - kDLatTiles) * kDTileCols;
+                const int x0 = (lat ? t : t - args.lat_tiles) * kDTileCols;
 #pragma unroll
                 for (int b = 0; b < 4; ++b)
                     ptx::tma_load_2d(a + b * kBoxBytes, wmap, bar, x0 + 64 * b, kb * kKBlock, pol_w);
@@ -345,9 +345,9 @@ __global__ void __maxnreg__(BN == 16 ? 72 : 80)
             // Scratch may still be read by the predecessor's finish kernel.
             if (last) asm volatile("griddepcontrol.wait;" ::: "memory");
             const int slot = args.seg_base[t] + (g - args.cta_first[t]);
-            const int nslots = args.seg_base[kDTiles - 1] + args.seg_count[kDTiles - 1];
+            const int nslots = args.seg_base[args.tiles - 1] + args.seg_count[args.tiles - 1];
             const bool slot_ok = ROUTE_IN_BOUNDS(
-                t < kDTiles && slot >= 0 && slot < nslots && col < kDTileCols, args.words);
+                t < args.tiles && slot >= 0 && slot < nslots && col < kDTileCols, args.words);
             float2 *const out =
                 last && slot_ok ? args.ws + (size_t)slot * kDecodeMaxRows * kDTileCols : stash;
             const uint32_t acc = lanes + (uint32_t)(buf * C::kAccCols + blk * BN);
@@ -396,7 +396,7 @@ struct SlotRun {
 
 __device__ __forceinline__ SlotRun slot_run(const DecodeArgs &a, int r, int t, int cc) {
     SlotRun s;
-    if (!ROUTE_IN_BOUNDS(r >= 0 && r < a.rows && t >= 0 && t < kDTiles && cc >= 0 &&
+    if (!ROUTE_IN_BOUNDS(r >= 0 && r < a.rows && t >= 0 && t < a.tiles && cc >= 0 &&
                              cc + 1 < kDTileCols,
                          a.words))
         return SlotRun{reinterpret_cast<const float4 *>(a.ws), 0};
@@ -719,6 +719,56 @@ __global__ void __maxnreg__(112) decode_finish_ss_kernel(const __grid_constant__
     }
 }
 
+// The finish of a column shard at decode sizes: CTA r < rows sums row r's
+// n_exp router logits (one column pair a thread), stores them, and its first
+// warp picks the shard's top-16 of them as candidates (the same selection
+// as the standalone shard top-16); CTA rows + i sums latent item i = (row,
+// latent tile), one column pair a thread, and stores the columns below
+// n_lat.  Slots are summed in segment order as two-floats, as for the whole
+// layer.
+__global__ void __maxnreg__(112)
+    decode_shard_finish_kernel(const __grid_constant__ DecodeArgs a, int n_lat, int n_exp,
+                               int id_base, int32_t *__restrict__ cand_ids,
+                               float *__restrict__ cand_logits) {
+    __shared__ uint2 s_cand[kCandMax];
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int tid = threadIdx.x;
+    const int b = blockIdx.x;
+    const int rows = a.rows;
+    if (b < rows) {
+        const int r = b;
+        float *lrow = a.logits + (size_t)r * n_exp;
+        asm volatile("griddepcontrol.wait;" ::: "memory");  // the stream kernel's partials are complete
+        for (int c = 2 * tid; c < n_exp; c += 2 * kFinishThreads) {  // one pass below 513 experts
+            SlotRun run[1] = {slot_run(a, r, a.lat_tiles + c / kDTileCols, c % kDTileCols)};
+            float2 y[1];
+            sum_slot_pairs<1, 16>(run, y);
+            if (ROUTE_IN_BOUNDS(c + 1 < n_exp, a.words)) *reinterpret_cast<float2 *>(lrow + c) = y[0];
+        }
+        __syncthreads();  // the row's logits are stored
+        if (tid < 32) {
+            uint32_t key, id;
+            topk16_warp_picks(lrow, n_exp, tid, s_cand, key, id);
+            if (tid < kTopK) {
+                cand_ids[(size_t)r * kTopK + tid] = id_base + (int32_t)id;
+                cand_logits[(size_t)r * kTopK + tid] = key_to_float(key);
+            }
+        }
+    } else {
+        const int i = b - rows, r = i / a.lat_tiles, t = i % a.lat_tiles;
+        const int cc = 2 * tid, col = t * kDTileCols + cc;
+        const bool mine = cc < kDTileCols && col < n_lat;
+        SlotRun run[1] = {mine ? slot_run(a, r, t, cc) : SlotRun{nullptr, 0}};
+        pin(run[0]);
+        asm volatile("griddepcontrol.wait;" ::: "memory");  // the stream kernel's partials are complete
+        float2 y[1];
+        sum_slot_pairs<1, 16>(run, y);
+        if (mine && ROUTE_IN_BOUNDS(r < rows && col + 1 < n_lat, a.words))
+            *reinterpret_cast<uint32_t *>(a.latent + (size_t)r * n_lat + col) =
+                (uint32_t)bf16_bits(y[0].x) | ((uint32_t)bf16_bits(y[0].y) << 16);
+    }
+}
+
 cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                               cudaLaunchAttribute *attr) {
     cudaLaunchConfig_t c = {};
@@ -758,6 +808,22 @@ int decode_smem_bytes(int bn) {
 
 cudaError_t decode_configure(int bn) {
     return bn == 16 ? configure_bn<16>() : bn == 32 ? configure_bn<32>() : cudaErrorInvalidValue;
+}
+
+cudaError_t decode_shard_launch(int bn, const CUtensorMap &map_h, const CUtensorMap &map_wl,
+                                const CUtensorMap &map_wr, const DecodeArgs &args, int n_lat,
+                                int n_exp, int id_base, int32_t *cand_ids, float *cand_logits,
+                                cudaStream_t stream) {
+    if (n_exp < kTopK || n_exp > kExpertsTopk || args.lat_tiles < 1) return cudaErrorInvalidValue;
+    cudaError_t e = bn == 16   ? launch_bn<16>(map_h, map_wl, map_wr, args, stream)
+                    : bn == 32 ? launch_bn<32>(map_h, map_wl, map_wr, args, stream)
+                               : cudaErrorInvalidValue;
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t c = pdl_config(dim3(args.rows * (1 + args.lat_tiles)), dim3(kFinishThreads),
+                                      0, stream, attr);
+    return cudaLaunchKernelEx(&c, decode_shard_finish_kernel, args, n_lat, n_exp, id_base, cand_ids,
+                              cand_logits);
 }
 
 cudaError_t decode_launch(int bn, const CUtensorMap &map_h, const CUtensorMap &map_wl,

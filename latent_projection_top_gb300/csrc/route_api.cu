@@ -358,27 +358,34 @@ bool build_schedule(int rows, bool ksplit, int max_pairs, int lat_tiles, int rou
 }
 
 // Decode stream grid: the largest CTA count, at most one per SM and at most
-// `cap`, that divides the 18 * 112 (tile, k-block) units into equal, even
+// `cap`, that divides the tiles * 112 (tile, k-block) units into equal, even
 // runs: every CTA streams the same number of bytes, and its k-blocks pair up
 // on one accumulator without a pair crossing a tile (tiles start at even
-// units).  144 CTAs of 14 units on 152 SMs.  Never below the tile count,
-// which route_prepare requires of the device.
-int decode_grid(int sms, int cap) {
-    const int U = kDTiles * kKBlocks;
-    const int hi = sms < cap ? sms : cap;
-    for (int g = hi; g > kDTiles; --g)
+// units).  The whole layer's 18 tiles: 144 CTAs of 14 units on 152 SMs.
+// At most 16 CTAs a tile, so that the finish adds at most 16 partials per
+// value in one memory round trip (this binds only a column shard's few
+// tiles).  Never below the tile count, which route_prepare requires of the
+// device.
+int decode_grid(int sms, int cap, int tiles = kDTiles) {
+    const int U = tiles * kKBlocks;
+    int hi = sms < cap ? sms : cap;
+    hi = hi < 16 * tiles ? hi : 16 * tiles;
+    for (int g = hi; g > tiles; --g)
         if ((U / 2) % g == 0) return g;
-    return kDTiles;
+    return tiles;
 }
 
 // Decode split-K partition: CTA g owns a contiguous run of (tile, k-block)
 // units, the same number (+-1) for every CTA.
-void decode_partition(DecodeArgs &a, int grid, int *segments) {
-    const int U = kDTiles * kKBlocks;
+void decode_partition(DecodeArgs &a, int grid, int *segments, int lat_tiles = kDLatTiles,
+                      int tiles = kDTiles) {
+    const int U = tiles * kKBlocks;
     a.grid = grid;
+    a.lat_tiles = lat_tiles;
+    a.tiles = tiles;
     for (int g = 0; g <= grid; ++g) a.cta_unit[g] = (int)((long long)U * g / grid);
     int slots = 0;
-    for (int t = 0; t < kDTiles; ++t) {
+    for (int t = 0; t < tiles; ++t) {
         const int first_u = t * kKBlocks, last_u = first_u + kKBlocks - 1;
         int g_first = -1, g_last = -1;
         for (int g = 0; g < grid; ++g) {
@@ -530,7 +537,10 @@ route_status prepare_plan(int mode, int rows, int device, int shard, int num_sha
         DecodeArgs &a = p->dec;
         a.rows = rows;
         a.timeout_ns = kDefaultTimeoutNs;
-        decode_partition(a, decode_grid(sms, kMaxGrid), &p->segments);
+        // the plan's column tiles: all 18, or a column shard's
+        const int lt = (p->n_lat + kDTileCols - 1) / kDTileCols;
+        const int nt = lt + (p->n_exp + kDTileCols - 1) / kDTileCols;
+        decode_partition(a, decode_grid(sms, kMaxGrid, nt), &p->segments, lt, nt);
         p->ws_bytes = (size_t)p->segments * kDecodeMaxRows * kDTileCols * sizeof(float2);
         if ((e = cudaMalloc(&p->ws, p->ws_bytes)) != cudaSuccess) {
             free_plan(p);
@@ -620,7 +630,10 @@ route_status route_prepare_shard(int rows, int device, int shard, int num_shards
                     kExperts, kLatent, kTopK, kMaxShards, num_shards);
     if (shard < 0 || shard >= num_shards)
         return fail(ROUTE_ERR_PLAN, "shard %d is not in 0..%d", shard, num_shards - 1);
-    return prepare_plan(ROUTE_PREFILL, rows, device, shard, num_shards, out);
+    // decode sizes stream the shard's weights with split-K over the SMs;
+    // larger chunks run the CTA-pair GEMM over the shard's tiles
+    return prepare_plan(rows <= ROUTE_DECODE_MAX_ROWS ? ROUTE_DECODE : ROUTE_PREFILL, rows, device,
+                        shard, num_shards, out);
 }
 
 route_status route_destroy(route_plan *plan) {
@@ -700,6 +713,18 @@ route_status route_shard_step(const route_plan *plan, const void *hidden,
     DeviceGuard guard(plan->device);
     if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (plan->mode == ROUTE_DECODE) {
+        CUtensorMap mh, ml, mr;
+        if ((st = encode_all(plan, hidden, W_latent_shard, W_router_shard, &mh, &ml, &mr)) !=
+            ROUTE_OK)
+            return st;
+        DecodeArgs a = plan->dec;
+        a.latent = static_cast<uint16_t *>(latent_shard);
+        a.logits = logits_shard;
+        const cudaError_t e = decode_shard_launch(plan->bn, mh, ml, mr, a, plan->n_lat, plan->n_exp,
+                                                  plan->shard * plan->n_exp, cand_ids, cand_logits, s);
+        return e == cudaSuccess ? ROUTE_OK : cuda_fail(e, "decode shard kernel launch");
+    }
     if ((st = launch_forward(plan, hidden, W_latent_shard, W_router_shard, latent_shard,
                              logits_shard, nullptr, nullptr, 0, nullptr, s)) != ROUTE_OK)
         return st;
@@ -923,6 +948,8 @@ route_status route_set_latent_ksplit(route_plan *plan, int enable) {
         plan->pre_ksplit = enable ? 1 : 0;
         return ROUTE_OK;
     }
+    if (plan->num_shards != 0 && enable)
+        return fail(ROUTE_ERR_PLAN, "a decode-size column shard has no K-split latent");
     if (enable) {
         // every CTA that touches a latent tile must own exactly one K slice of it
         constexpr int kSlice = kKBlocks / kKSplitSlices;  // 14 k-blocks = 896 of K

@@ -85,7 +85,7 @@ def test_debug_library_runs_clean_and_matches_release():
                 f"{wk} {rows} rows: output {i} differs between the debug and release libraries"
 
 
-SHARD_CASES = [(8, 40), (16, 8), (7, 300)]
+SHARD_CASES = [(8, 40), (16, 8), (8, 20), (2, 1), (7, 300)]
 
 SHARD_RUN = r"""
 def shard_outputs(W, rows):

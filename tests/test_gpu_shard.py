@@ -111,21 +111,40 @@ def test_shards_then_merge_equal_the_whole_layer_and_the_oracle(W):
     record(f"shard_W{W}_merge", **s1)
 
 
-def test_eight_decode_rows_on_eight_shards():
-    """Decode-size rows (TP8 layout: 448 latent columns and 112 experts a
-    shard) through the same shard kernels."""
-    hid, wl, wr = bank("decode_r8", 0)
-    rows = 8
+def _whole_decode(h_dev, wl, wr, rows):
+    with route.Plan(route.DECODE, rows) as plan:
+        return run_step(plan, h_dev, to_dev_bf16(wl), to_dev_bf16(wr))
+
+
+@pytest.mark.parametrize("workload,rows,W", [("decode_r8", 8, 8), ("decode_r8", 8, 2),
+                                             ("decode_r8", 8, 16), ("decode_r1", 1, 4),
+                                             ("decode_sweep", 20, 7), ("decode_r8", 8, 1)])
+def test_decode_size_shards(workload, rows, W):
+    """Up to 20 rows a shard streams its weights with the decode path's split
+    K (TP8: 448 latent columns and 112 experts a shard; TP16: 224 and 56).
+    The shards' latent and logits pass the decode gates against the oracle's
+    float64 sums; every shard's candidates are the oracle's top-16 of that
+    shard's GPU logits; the merged ids and weights are the oracle's top-16 of
+    the concatenated GPU logits (G1) and agree with the oracle's ids end to
+    end (G4, differences only on rows built as near ties); the logits agree
+    with a whole-layer decode plan's to the decode gate's bound."""
+    from gates import check_ids_end_to_end, check_latent, check_logits
+    from test_gpu_parity import _near_tie_rows
+    hid, wl, wr = bank(workload, 0)
     h_dev = to_dev_bf16(np.ascontiguousarray(hid[:rows]))
-    lat, lg, ids, w, cids, clg = _run_shards(h_dev, wl, wr, 8, rows)
-    lat0, lg0, ids0, w0 = _whole(h_dev, wl, wr, rows)
-    assert np.array_equal(lat, lat0)
-    assert np.array_equal(lg.view(np.uint32), lg0.view(np.uint32))
-    _check_candidates(lg, cids, clg, 8)
-    assert np.array_equal(ids, ids0) and np.array_equal(w.view(np.uint32), w0.view(np.uint32))
-    from test_gpu_parity import _prefill_gates
-    ref = oracle_rows("decode_r8", 0, tuple(range(rows)))
-    _prefill_gates(lat, lg, ids, w, ref, list(range(rows)), "shard_W8_decode_r8")
+    lat, lg, ids, w, cids, clg = _run_shards(h_dev, wl, wr, W, rows)
+    ref = oracle_rows(workload, 0, tuple(range(rows)))
+    s1 = check_latent(lat, ref["latent"], ref["y_lat"], ref["abs_lat"])
+    s2 = check_logits(lg, ref["y_log"], ref["abs_log"], "decode")
+    _check_candidates(lg, cids, clg, W)
+    ids_o, w_o = oracle.topk(lg)
+    s3 = check_topk_exact(ids, w, ids_o, w_o)
+    ids_ref, _ = oracle.topk(ref["logits"])
+    s4 = check_ids_end_to_end(ids, ids_ref, ref["logits"],
+                              swap_rows_allowed=_near_tie_rows(workload, rows))
+    lat0, lg0, _, _ = _whole_decode(h_dev, wl, wr, rows)
+    assert np.all(np.abs(lg.astype(np.float64) - lg0) <= 2.0 ** -24 * ref["abs_log"])
+    record(f"shard_decode_W{W}_{workload}_r{rows}", **s1, **s2, **s3, **s4)
 
 
 def test_ksplit_latent_on_shards():
@@ -195,6 +214,9 @@ def test_shard_plan_refuses_the_whole_layer_entry_points():
         h = torch.zeros((rows, route.K_HIDDEN), dtype=torch.bfloat16, device=DEV)
         wl = torch.zeros((route.K_HIDDEN, route.N_LATENT), dtype=torch.bfloat16, device=DEV)
         wr = torch.zeros((route.K_HIDDEN, route.N_EXPERTS), dtype=torch.bfloat16, device=DEV)
+        with pytest.raises(route.RouteError) as ei:  # decode-size shards: full-K latent only
+            route.route_set_latent_ksplit(plan, True)
+        assert ei.value.status == route.STATUS_CODES["ROUTE_ERR_PLAN"]
         for call in (lambda: route.route_step(plan, h, wl, wr, lat, lg, ids, w),
                      lambda: route.latent_router_forward(plan, h, wl, wr, lat, lg),
                      lambda: route.topk16_select(plan, lg, ids, w)):
