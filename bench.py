@@ -785,7 +785,7 @@ def sweep(rb, dist, peaks, args):
             rb.route.route_device_status(plan)
             plan.close()
             t = sm["median"] / 1e6
-            sfx = "_with_overlap" if ov else ""
+            sfx = "" if ov else "_without_overlap"
             entry.update({"us_per_layer" + sfx: sm["median"], "us_spread" + sfx: sm,
                           "rows_per_s" + sfx: round(rows / t, 1),
                           "achieved_gbs" + sfx: round(algo / t / 1e9, 1),
@@ -869,6 +869,40 @@ def sweep(rb, dist, peaks, args):
                 algo = WEIGHT_BYTES + rows * (ROW_BYTES + (4 if var.get("sumsq") else 0))
                 e.update({"bound": "hbm", "frac": round(algo / t / 1e9 / peaks["hbm_gbs"], 4)})
             res.append(e)
+    res += shard_sweep(rb, dist)
+    return res
+
+
+def shard_sweep(rb, dist):
+    """One rank's share of a column-sharded decode step (shard 0 of W; its
+    weights cycled over 32 banks so that they do not stay in L2), both
+    regimes.  The exchange between ranks is not part of it."""
+    route, torch = rb.route, rb.torch
+    banks = rb.weight_banks("decode", 32)
+    res = []
+    for W, rows in ((8, 8), (16, 8)):
+        NL, NE = route.shard_columns(W)
+        sb = [(wl[:, :NL].contiguous(), wr[:, :NE].contiguous()) for wl, wr in banks]
+        h = rb.hidden("decode_r8", rows, 1)[0]
+        outs = [(torch.empty((rows, NL), dtype=torch.bfloat16, device=rb.dev),
+                 torch.empty((rows, NE), dtype=torch.float32, device=rb.dev),
+                 torch.empty((rows, TOPK), dtype=torch.int32, device=rb.dev),
+                 torch.empty((rows, TOPK), dtype=torch.float32, device=rb.dev)) for _ in sb]
+        for ov in (True, False):
+            plan = route.ShardPlan(rows, 0, W, rb.device)
+            route.route_set_overlap(plan, ov)
+            steps = [lambda s, wl=wl, wr=wr, o=o: route.route_shard_step(plan, h, wl, wr, *o, stream=s)
+                     for (wl, wr), o in zip(sb, outs)]
+            sm = summarise(rb.spread(steps, dist=dist, runs=3, replays=100))
+            route.route_device_status(plan)
+            byt = (NL + NE) * K_HIDDEN * 2
+            res.append({"workload": f"column shard 0 of {W} (decode_r8 rows)", "rows": rows,
+                        "overlap": ov, "shard_latent_cols": NL, "shard_experts": NE,
+                        "us_per_layer": sm["median"], "us_spread": sm, "grid": plan.grid,
+                        "weight_bytes": byt, "achieved_gbs": round(byt / sm["median"] / 1e3, 1),
+                        "note": "one rank's compute on one GPU; the candidate exchange is not timed"})
+            plan.close()
+        del sb
     return res
 
 
