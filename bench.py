@@ -464,6 +464,43 @@ class RouteBench:
             del g
             return out
 
+    def ab(self, steps_a, steps_b, rounds: int = 5, replays: int = 200,
+           graph_len: int = GRAPH_LEN, warm_replays: int = 20, dist=None):
+        """Interleaved A/B: one graph of `graph_len` steps for each side, then
+        `rounds` times a run of `replays` replays of A followed by one of B,
+        so that both sides see the same drift of the part's power state.
+        Returns the per-step times of each side's runs (us)."""
+        with guarded(f"a/b {rounds}x{replays}"):
+            torch = self.torch
+            s = torch.cuda.Stream(device=self.dev)
+            s.wait_stream(torch.cuda.current_stream(self.dev))
+            graphs = [self.graph(st, graph_len, 0, s) for st in (steps_a, steps_b)]
+            torch.cuda.synchronize(self.dev)
+            with torch.cuda.stream(s):
+                for g in graphs:
+                    for _ in range(warm_replays):
+                        g.replay()
+            torch.cuda.synchronize(self.dev)
+            out = ([], [])
+            for _ in range(rounds):
+                for side, g in enumerate(graphs):
+                    if dist is not None:
+                        dist.barrier()
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    with torch.cuda.stream(s):
+                        e0.record(s)
+                        for _ in range(replays):
+                            g.replay()
+                        e1.record(s)
+                    e1.synchronize()
+                    ms = e0.elapsed_time(e1)
+                    if dist is not None:
+                        ms = dist.max(ms)
+                    out[side].append(ms * 1e3 / (replays * graph_len))
+            del graphs
+            return out
+
     def per_layer_us(self, steps, dist):
         """One chunk launched eagerly with an event between consecutive layers:
         per-layer time (median, min, max) and the chunk total, from the second
@@ -848,19 +885,32 @@ def sweep(rb, dist, peaks, args):
         res.append(e)
     # the route step that also returns each latent row's sum of squares, and
     # the step with the general path's K-split latent arithmetic
+    # each timed against the plain route step in interleaved runs (A/B), so
+    # that the difference is not the drift of the part's power state
     variants = [dict(sumsq=True), dict(ksplit=True)]
     for var in variants:
-        for wk, rows in [("decode_r8", 8), ("decode_sweep", 20), ("prefill_r3072", 3072)]:
+        for wk, rows in [("decode_r8", 8), ("decode_sweep", 20), ("prefill_r1024", 1024),
+                         ("prefill_r3072", 3072)]:
             decode = wk.startswith("decode")
             nb = 8 if decode else args.prefill_banks
             ov = decode
+            base, bsteps, _ = rb.make_steps(wk, rows, nb, overlap=ov)
             plan, steps, _ = rb.make_steps(wk, rows, nb, overlap=ov, **var)
-            sm = summarise(rb.spread(steps, dist=dist, **(DECODE_SPREAD if decode else PREFILL_SPREAD)))
+            kw = dict(DECODE_SPREAD if decode else PREFILL_SPREAD)
+            kw["rounds"] = kw.pop("runs")
+            ua, ub = rb.ab(bsteps, steps, dist=dist, **kw)
+            rb.route.route_device_status(base)
             rb.route.route_device_status(plan)
+            base.close()
             plan.close()
+            sm = summarise(ub)
             t = sm["median"] / 1e6
             e = {"workload": wk, "rows": rows, "overlap": ov, "us_per_layer": sm["median"],
-                 "us_spread": sm, "rows_per_s": round(rows / t, 1)}
+                 "us_spread": sm, "rows_per_s": round(rows / t, 1),
+                 "us_plain_step_interleaved": summarise(ua),
+                 "us_added": summarise([b - a for a, b in zip(ua, ub)]),
+                 "ab": "runs alternate with the plain route step's, same workload and mode; "
+                       "us_added = per-round difference (median, min, max)"}
             if var.get("sumsq"):
                 e["call"] = "route_step_sumsq"
             else:

@@ -53,6 +53,7 @@
 // final cluster barrier, so neither leaves while the other may still reach
 // its shared memory).
 #include <cuda_bf16.h>
+#include <type_traits>
 
 #include "common.cuh"
 #include "sm103_ptx.cuh"
@@ -142,7 +143,10 @@ __device__ __forceinline__ float bf16_round(float x) {
     return __uint_as_float((uint32_t)bf16_bits(x) << 16);
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
+// 168 registers a thread (320 threads, one CTA an SM): with this cap as
+// __maxnreg__ nothing spills, where __launch_bounds__(320, 1) spilled a few
+// words in the K-split epilogue
+__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap map_h,
                         const __grid_constant__ CUtensorMap map_wl,
                         const __grid_constant__ CUtensorMap map_wr,
@@ -371,21 +375,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
         };
         // Per-row sum of squares of the 32 BF16 values this warp just staged
         // for rows y .. y + 15 (exact squares; lanes 2r and 2r + 1 take 16
-        // values of row r each, two-floats joined in a fixed order): one part
-        // per row.  Reads the staging buffer before it can be written again.
-        auto sumsq_parts = [&](int part, int y) {
+        // values of row r each, joined in a fixed order): one part per row.
+        // Packed: even and odd columns as two two-float streams in FP32
+        // pairs (half the instructions); the K-split tiles, whose 128 sums
+        // are still live here, take the scalar form, which needs fewer
+        // registers.  Reads the staging buffer before it can be written again.
+        auto sumsq_parts = [&](int part, int y, auto packed) {
             const uint4 *row = reinterpret_cast<const uint4 *>(
                 store_gen + (sb ^ 1) * kStoreBufBytes + (lane >> 1) * 64 + (lane & 1) * 32);
             float hi = 0.f, lo = 0.f;
+            if constexpr (decltype(packed)::value) {
+                uint64_t hi2 = 0u, lo2 = 0u;  // +0.0f in both halves
 #pragma unroll
-            for (int g = 0; g < 2; ++g) {
-                const uint4 w4 = row[g];
-                const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+                for (int g = 0; g < 2; ++g) {
+                    const uint4 w4 = row[g];
+                    const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float a = __uint_as_float(w[e] << 16), b = __uint_as_float(w[e] & 0xFFFF0000u);
-                    two_sum_acc(hi, lo, a * a);
-                    two_sum_acc(hi, lo, b * b);
+                    for (int e = 0; e < 4; ++e) {
+                        const uint64_t x = ptx::f32x2_pack(__uint_as_float(w[e] << 16),
+                                                           __uint_as_float(w[e] & 0xFFFF0000u));
+                        two_sum_acc_x2(hi2, lo2, ptx::f32x2_mul(x, x));
+                    }
+                }
+                float hb, lb;
+                ptx::f32x2_unpack(hi2, hi, hb);
+                ptx::f32x2_unpack(lo2, lo, lb);
+                two_sum_acc(hi, lo, hb);
+                lo += lb;
+            } else {
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    const uint4 w4 = row[g];
+                    const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float a = __uint_as_float(w[e] << 16),
+                                    b = __uint_as_float(w[e] & 0xFFFF0000u);
+                        two_sum_acc(hi, lo, a * a);
+                        two_sum_acc(hi, lo, b * b);
+                    }
                 }
             }
             const float ohi = __shfl_xor_sync(0xFFFFFFFFu, hi, 1);
@@ -447,7 +475,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
 #pragma unroll
                         for (int jj = 0; jj < 16; ++jj) u[jj] = bf16_bits(__uint_as_float(u[jj]));
                         store_chunk(u, false, &map_lat, xw, y, valid);
-                        if (args.ss_part != nullptr) sumsq_parts(part, y);
+                        if (args.ss_part != nullptr) sumsq_parts(part, y, std::true_type{});
                     } else {
                         store_chunk(u, true, &map_lg, xw, y, valid);
                     }
@@ -487,7 +515,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) v[jj] = bf16_bits(sum[16 * ch + jj]);
                     store_chunk(v, false, &map_lat, xw, y, valid);
-                    if (args.ss_part != nullptr) sumsq_parts(part, y);
+                    if (args.ss_part != nullptr) sumsq_parts(part, y, std::false_type{});
                 }
             }
         }

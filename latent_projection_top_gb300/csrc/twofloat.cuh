@@ -3,6 +3,8 @@
 // warp reduction, so that results are bitwise reproducible.
 #pragma once
 
+#include "sm103_ptx.cuh"
+
 namespace route {
 
 // Error-free addition (Knuth's TwoSum): hi + x = s + e exactly; e joins lo.
@@ -12,6 +14,18 @@ __device__ __forceinline__ void two_sum_acc(float &hi, float &lo, float x) {
     const float e = (hi - (s - bp)) + (x - bp);
     hi = s;
     lo += e;
+}
+
+// TwoSum on two independent two-floats at once, in packed FP32 pairs
+// (hi, lo and x each hold one pair; the explicit rounding of every packed
+// operation keeps the steps from being fused or reordered).
+__device__ __forceinline__ void two_sum_acc_x2(uint64_t &hi, uint64_t &lo, uint64_t x) {
+    const uint64_t s = ptx::f32x2_add(hi, x);
+    const uint64_t bp = ptx::f32x2_sub(s, hi);
+    const uint64_t e =
+        ptx::f32x2_add(ptx::f32x2_sub(hi, ptx::f32x2_sub(s, bp)), ptx::f32x2_sub(x, bp));
+    hi = s;
+    lo = ptx::f32x2_add(lo, e);
 }
 
 // The value of a two-float sum.  An infinite high part is the value itself:
