@@ -121,16 +121,27 @@ __device__ __forceinline__ void epi_chunk(uint32_t acc, uint32_t s_hi, uint32_t 
         ptx::tc_fence_before();
         ptx::mbar_arrive(accempty);
     }
+    // two rows at a time, in packed FP32 pairs
+    static_assert(W % 2 == 0, "rows in pairs");
 #pragma unroll
-    for (int j = 0; j < W; ++j) {
-        float hf = __uint_as_float(v[j]), lf = 0.f;
-        if (!run_start) {
-            hf = __uint_as_float(h[j]);
-            lf = __uint_as_float(l[j]);
-            two_sum_acc(hf, lf, __uint_as_float(v[j]));
+    for (int j = 0; j < W; j += 2) {
+        if (run_start) {
+            h[j] = v[j];
+            h[j + 1] = v[j + 1];
+            l[j] = l[j + 1] = 0u;
+        } else {
+            uint64_t hp = ptx::f32x2_pack(__uint_as_float(h[j]), __uint_as_float(h[j + 1]));
+            uint64_t lp = ptx::f32x2_pack(__uint_as_float(l[j]), __uint_as_float(l[j + 1]));
+            two_sum_acc_x2(hp, lp,
+                           ptx::f32x2_pack(__uint_as_float(v[j]), __uint_as_float(v[j + 1])));
+            float a, b;
+            ptx::f32x2_unpack(hp, a, b);
+            h[j] = __float_as_uint(a);
+            h[j + 1] = __float_as_uint(b);
+            ptx::f32x2_unpack(lp, a, b);
+            l[j] = __float_as_uint(a);
+            l[j + 1] = __float_as_uint(b);
         }
-        h[j] = __float_as_uint(hf);
-        l[j] = __float_as_uint(lf);
     }
     if (!run_end) {
         ptx::tmem_st(s_hi + r0, h);
@@ -180,7 +191,7 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, const 
 // Register caps (the most each variant compiles to without spilling) leave
 // room on every SM sub-partition for two warps of a finish CTA.
 template <int BN>
-__global__ void __maxnreg__(BN == 16 ? 72 : 80)
+__global__ void __maxnreg__(BN == 16 ? 80 : 88)
     decode_stream_kernel(const __grid_constant__ CUtensorMap map_h,
                          const __grid_constant__ CUtensorMap map_wl,
                          const __grid_constant__ CUtensorMap map_wr,
