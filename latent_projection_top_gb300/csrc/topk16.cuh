@@ -147,15 +147,11 @@ __device__ __forceinline__ void weights16_store(uint32_t mine_key, uint32_t mine
     weights16_store_terms(s_hi, s_lo, mine_id, lane, ids_out, w_out);
 }
 
-// The calling warp selects row `row` (896 logits in global or shared memory,
-// final before the call) and writes 16 ids and weights.  All 32 lanes must
-// call it; `cand` is this warp's shared buffer of kCandMax entries.
-__device__ __forceinline__ void topk16_warp(const float *row, int32_t *ids_out, float *w_out,
-                                            int lane, uint2 *cand) {
-    uint32_t key[kPerLane];
-#pragma unroll
-    for (int j = 0; j < kPerLane; ++j) key[j] = rank_key(row[32 * j + lane]);
-
+// The calling warp selects the row whose 896 keys it holds (lane l: the keys
+// of ids 32 j + l) and writes 16 ids and weights.  All 32 lanes must call
+// it; `cand` is this warp's shared buffer of kCandMax entries.
+__device__ __forceinline__ void topk16_warp_keys(uint32_t (&key)[kPerLane], int32_t *ids_out,
+                                                 float *w_out, int lane, uint2 *cand) {
     uint32_t lane_max = 0u;
 #pragma unroll
     for (int j = 0; j < kPerLane; ++j) lane_max = max(lane_max, key[j]);
@@ -215,6 +211,17 @@ __device__ __forceinline__ void topk16_warp(const float *row, int32_t *ids_out, 
         }
     }
     weights16_store(mine_key, mine_id, lane, ids_out, w_out);
+}
+
+// The calling warp selects row `row` (896 logits in global or shared memory,
+// final before the call) and writes 16 ids and weights.  All 32 lanes must
+// call it; `cand` is this warp's shared buffer of kCandMax entries.
+__device__ __forceinline__ void topk16_warp(const float *row, int32_t *ids_out, float *w_out,
+                                            int lane, uint2 *cand) {
+    uint32_t key[kPerLane];
+#pragma unroll
+    for (int j = 0; j < kPerLane; ++j) key[j] = rank_key(row[32 * j + lane]);
+    topk16_warp_keys(key, ids_out, w_out, lane, cand);
 }
 
 // The 16 picks (lane i < 16 keeps the i-th, as a key and an id) of the n

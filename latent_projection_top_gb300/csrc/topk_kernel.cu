@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock)
 // every candidate's rank among all of them (larger logit first, the lower
 // expert id on equal logits; the same keys as the top-16) by counting, the
 // ranks 0..15 in order, then the routing weights of those 16.
-constexpr int kMergeMax = kMaxShards * kTopK;  // 128
+constexpr int kMergeMax = kMaxShards * kTopK;  // 256
 
 __global__ void __launch_bounds__(32 * kRowsPerBlock)
     merge_kernel(const int32_t *__restrict__ cand_ids, const float *__restrict__ cand_logits, int rows,
