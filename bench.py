@@ -636,8 +636,8 @@ class RouteBench:
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "us_per_step": round(t / k * 1e6, 3), "steps": k,
                 "path": "HostStep: route_step_host's copy-free path on pinned host buffers, "
-                        "prepared once as a CUDA graph (route_host_step_run), synchronised "
-                        "every step",
+                        "prepared once as a CUDA graph (route_host_step_run); every call "
+                        "returns once its step's results are in the host buffers",
                 "us_per_step_route_step_host": round(t_checked / k * 1e6, 3)}
 
 

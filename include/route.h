@@ -179,9 +179,14 @@ route_status route_step_host(const route_plan *plan, const void *hidden_host,
  * plans with every host buffer page-locked and 16-byte aligned only (the
  * path that copies nothing); otherwise ROUTE_ERR_PLAN, and the caller uses
  * route_step_host.  The staging, stream and finish kernels are captured once
- * into a CUDA graph (on a stream of the step's own), so that
- * route_host_step_run is one graph launch on `stream` and a synchronise of
- * `stream`; it returns after the results are in the host buffers.  The
+ * into a CUDA graph (on a stream of the step's own), with a last one-thread
+ * kernel that, once they have finished, stores the step's number into a
+ * page-locked completion word after a system-scope fence.
+ * route_host_step_run is one graph launch on `stream` and a wait for that
+ * number in the completion word (not for the stream: the last kernel may
+ * still be leaving when it returns); it returns after the results are in the
+ * host buffers.  Without the number after 4 s it synchronises `stream` and
+ * reports its error (or ROUTE_ERR_DEVICE).  The
  * graph keeps the plan's settings (route_set_latent_ksplit) as they were at
  * creation.  The step belongs to the plan: route_destroy releases its
  * graph, after which route_host_step_run returns ROUTE_ERR_NULL.

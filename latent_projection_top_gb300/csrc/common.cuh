@@ -143,6 +143,7 @@ cudaError_t decode_launch(int bn, const CUtensorMap &map_h, const CUtensorMap &m
 // device-mapped address, into device memory; PDL-chained like the route
 // kernels.
 cudaError_t stage_in_launch(const void *src_mapped, void *dst, size_t bytes, cudaStream_t stream);
+cudaError_t host_done_launch(unsigned *counter, unsigned *flag_mapped, cudaStream_t stream);
 
 // The top-16 of each row; with `sumsq` non-null also the row's latent sum
 // of squares (the sum of its kSsParts parts in `ss_part`, which the same

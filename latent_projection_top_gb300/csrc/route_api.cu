@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <chrono>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -57,12 +58,21 @@ struct route_host_step {
     route_host_step *next;    // the plan's list
     cudaGraph_t graph;
     cudaGraphExec_t exec;
-    cudaStream_t stream;      // the caller's stream: launches and waits there
+    cudaStream_t stream;      // the caller's stream: launches there
+    // Completion: the graph's last kernel stores the step's number into a
+    // page-locked word (flag_host; flag_dev is its mapped address) after a
+    // system-scope fence; run() waits for that number instead of for the
+    // stream.  counter is the device copy of the number.
+    unsigned *flag_host;
+    unsigned *flag_dev;
+    unsigned *counter;
+    unsigned done;            // the number of the last step that completed
 };
 
 namespace {
 
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // bound on every in-kernel wait
+constexpr long long kHostWaitNs = 4000000000ll;  // a host step's wait for its completion word
 
 thread_local char g_err[512] = "";
 
@@ -144,8 +154,12 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 void release_step_graph(route_host_step *h) {
     if (h->exec) cudaGraphExecDestroy(h->exec);
     if (h->graph) cudaGraphDestroy(h->graph);
+    if (h->counter) cudaFree(h->counter);
+    if (h->flag_host) cudaFreeHost(h->flag_host);
     h->exec = nullptr;
     h->graph = nullptr;
+    h->counter = nullptr;
+    h->flag_host = h->flag_dev = nullptr;
 }
 
 void free_plan(route_plan *p) {
@@ -881,13 +895,26 @@ route_status route_host_step_create(route_plan *plan, const void *hidden_host,
     route_host_step *step = new (std::nothrow) route_host_step{};
     if (!step) return fail(ROUTE_ERR_CUDA, "out of host memory");
     step->stream = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMalloc(&step->counter, sizeof(unsigned));
+    if (e == cudaSuccess) e = cudaMemset(step->counter, 0, sizeof(unsigned));
+    if (e == cudaSuccess)
+        e = cudaHostAlloc(reinterpret_cast<void **>(&step->flag_host), 64, cudaHostAllocMapped);
+    if (e == cudaSuccess) {
+        *step->flag_host = 0u;
+        e = cudaHostGetDevicePointer(reinterpret_cast<void **>(&step->flag_dev), step->flag_host, 0);
+    }
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();  // the counter's zero is in place
     // Capture on a stream of our own: the caller's may be the legacy
     // default stream, which cannot be captured.
     cudaStream_t cs = nullptr;
-    cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
     if (e == cudaSuccess) {
         st = enqueue_mapped_step(plan, h, W_latent, W_router, lat, lg, ids, w, cs);
+        if (st == ROUTE_OK) {
+            const cudaError_t e3 = host_done_launch(step->counter, step->flag_dev, cs);
+            if (e3 != cudaSuccess) st = cuda_fail(e3, "completion kernel launch");
+        }
         const cudaError_t e2 = cudaStreamEndCapture(cs, &step->graph);
         if (st == ROUTE_OK && e2 != cudaSuccess) e = e2;
     }
@@ -914,8 +941,25 @@ route_status route_host_step_run(route_host_step *step) {
     if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
     cudaError_t e = cudaGraphLaunch(step->exec, step->stream);
     if (e != cudaSuccess) return cuda_fail(e, "launch the host step");
+    // Wait for this step's number in the completion word (the results are
+    // in host memory before it); after kHostWaitNs without it, wait for the
+    // stream instead and report what it reports.
+    const unsigned want = step->done + 1u;
+    const auto t0 = std::chrono::steady_clock::now();
+    for (uint32_t it = 1;; ++it) {
+        if (__atomic_load_n(step->flag_host, __ATOMIC_ACQUIRE) == want) {
+            step->done = want;
+            return ROUTE_OK;
+        }
+        if ((it & 1023u) == 0u &&
+            std::chrono::steady_clock::now() - t0 > std::chrono::nanoseconds(kHostWaitNs))
+            break;
+    }
     if ((e = cudaStreamSynchronize(step->stream)) != cudaSuccess)
         return cuda_fail(e, "cudaStreamSynchronize");
+    if (__atomic_load_n(step->flag_host, __ATOMIC_ACQUIRE) != want)
+        return fail(ROUTE_ERR_DEVICE, "the host step finished without its completion word");
+    step->done = want;
     return ROUTE_OK;
 }
 
@@ -928,6 +972,7 @@ route_status route_host_step_destroy(route_host_step *step) {
                 break;
             }
         DeviceGuard guard(p->device);
+        cudaStreamSynchronize(step->stream);  // its last launch may still be leaving
         release_step_graph(step);
     }
     delete step;

@@ -19,7 +19,35 @@ __global__ void __launch_bounds__(kStageThreads)
         dst[i] = src[i];
 }
 
+// The last kernel of a prepared host step: once the step's kernels have
+// finished (the grid dependency) it advances the step's device counter and
+// stores the new value into a page-locked word that the calling thread
+// watches, with a system-scope fence before the store, so that the results
+// the finish kernel wrote into host memory are visible first.
+__global__ void host_done_kernel(unsigned *counter, unsigned *flag_mapped) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // every kernel of the step has finished
+    if (threadIdx.x == 0) {
+        const unsigned v = *counter + 1u;
+        *counter = v;
+        __threadfence_system();
+        asm volatile("st.release.sys.global.u32 [%0], %1;" ::"l"(flag_mapped), "r"(v) : "memory");
+    }
+}
+
 }  // namespace
+
+cudaError_t host_done_launch(unsigned *counter, unsigned *flag_mapped, cudaStream_t stream) {
+    cudaLaunchConfig_t c = {};
+    cudaLaunchAttribute attr[1];
+    c.gridDim = dim3(1);
+    c.blockDim = dim3(32);
+    c.stream = stream;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    c.attrs = attr;
+    c.numAttrs = 1;
+    return cudaLaunchKernelEx(&c, host_done_kernel, counter, flag_mapped);
+}
 
 cudaError_t stage_in_launch(const void *src_mapped, void *dst, size_t bytes, cudaStream_t stream) {
     if (bytes == 0 || bytes % 16 != 0) return cudaErrorInvalidValue;

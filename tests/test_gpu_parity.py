@@ -476,6 +476,40 @@ def test_host_step_reuses_buffers(rows):
         step()
 
 
+def test_host_step_results_visible_on_return_many_steps():
+    """route_host_step_run returns on the step's completion word, not on the
+    stream: 400 steps alternating two inputs, each step's results checked in
+    the host buffers right after the call returns."""
+    rows = 8
+    _, wl, wr = bank("decode_r8", 0)
+    dwl, dwr = to_dev_bf16(wl), to_dev_bf16(wr)
+    hs = [np.ascontiguousarray(np.resize(bank("decode_r8", b)[0], (rows, route.K_HIDDEN)))
+          for b in (0, 1)]
+    with route.Plan(route.DECODE, rows) as plan:
+        want = [run_step(plan, to_dev_bf16(h), dwl, dwr) for h in hs]
+        h_host = [torch.from_numpy(h.view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+                  for h in hs]
+        buf = torch.empty((rows, route.K_HIDDEN), dtype=torch.bfloat16).pin_memory()
+        lat = torch.empty((rows, route.N_LATENT), dtype=torch.bfloat16).pin_memory()
+        lg = torch.empty((rows, route.N_EXPERTS), dtype=torch.float32).pin_memory()
+        ids = torch.empty((rows, route.TOPK), dtype=torch.int32).pin_memory()
+        w = torch.empty((rows, route.TOPK), dtype=torch.float32).pin_memory()
+        step = route.HostStep(plan, buf, dwl, dwr, lat, lg, ids, w)
+        assert step.graph
+        for i in range(400):
+            b = i % 2
+            buf.copy_(h_host[b])
+            lat.view(torch.int16).fill_(-1)
+            ids.fill_(-1)
+            step()
+            assert np.array_equal(ids.numpy(), want[b][2]), f"step {i}"
+            assert np.array_equal(w.numpy().view(np.uint32), want[b][3].view(np.uint32)), f"step {i}"
+            assert np.array_equal(lat.view(torch.int16).numpy().view(np.uint16), want[b][0]), \
+                f"step {i}"
+        route.route_device_status(plan)
+        step.close()
+
+
 @pytest.mark.parametrize("mode,rows,pinned", [(route.DECODE, 8, False), (route.PREFILL, 40, True)])
 def test_host_step_without_graph_runs_route_step_host(mode, rows, pinned):
     """Pageable buffers, or a prefill plan: HostStep calls route_step_host."""
