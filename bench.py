@@ -467,9 +467,10 @@ class RouteBench:
     def ab(self, steps_a, steps_b, rounds: int = 5, replays: int = 200,
            graph_len: int = GRAPH_LEN, warm_replays: int = 20, dist=None):
         """Interleaved A/B: one graph of `graph_len` steps for each side, then
-        `rounds` times a run of `replays` replays of A followed by one of B,
-        so that both sides see the same drift of the part's power state.
-        Returns the per-step times of each side's runs (us)."""
+        `rounds` times a run of `replays` replays of each side, A first in
+        even rounds and B first in odd ones, so that both sides see the same
+        drift of the part's power state.  Returns the per-step times of each
+        side's runs (us)."""
         with guarded(f"a/b {rounds}x{replays}"):
             torch = self.torch
             s = torch.cuda.Stream(device=self.dev)
@@ -482,8 +483,9 @@ class RouteBench:
                         g.replay()
             torch.cuda.synchronize(self.dev)
             out = ([], [])
-            for _ in range(rounds):
-                for side, g in enumerate(graphs):
+            for r in range(rounds):
+                for side in ((0, 1) if r % 2 == 0 else (1, 0)):
+                    g = graphs[side]
                     if dist is not None:
                         dist.barrier()
                     e0 = torch.cuda.Event(enable_timing=True)
@@ -909,8 +911,8 @@ def sweep(rb, dist, peaks, args):
                  "us_spread": sm, "rows_per_s": round(rows / t, 1),
                  "us_plain_step_interleaved": summarise(ua),
                  "us_added": summarise([b - a for a, b in zip(ua, ub)]),
-                 "ab": "runs alternate with the plain route step's, same workload and mode; "
-                       "us_added = per-round difference (median, min, max)"}
+                 "ab": "runs alternate with the plain route step's (ABBA order), same "
+                       "workload and mode; us_added = per-round difference (median, min, max)"}
             if var.get("sumsq"):
                 e["call"] = "route_step_sumsq"
             else:
