@@ -60,21 +60,29 @@ __device__ __forceinline__ uint32_t warp_16th_largest(uint32_t v, int lane) {
     return __shfl_sync(0xFFFFFFFFu, v, 16);
 }
 
-// Rank the `total` (<= kCandMax) candidates in `cand` (shared memory, final
-// before the call): each candidate's rank is the number of candidates that
-// precede it in the ranking; ranks are distinct (ids are), so rank < 16
-// places a pick.  Lane i < 16 returns the i-th pick.  All 32 lanes call it.
-__device__ __forceinline__ void pick16_from_candidates(uint2 *cand, uint32_t total, int lane,
+// A candidate as one 64-bit word: the key above the complemented id, so that
+// a larger word ranks first (larger key; on equal keys, the lower id).
+__device__ __forceinline__ unsigned long long pack_cand(uint32_t key, uint32_t id) {
+    return ((unsigned long long)key << 32) | (unsigned long long)(~id);
+}
+
+// Rank the `total` (<= kCandMax) candidates in `cand` (shared memory, packed
+// words, final before the call): each candidate's rank is the number of
+// candidates that precede it in the ranking; ranks are distinct (ids are), so
+// rank < 16 places a pick.  Lane i < 16 returns the i-th pick.  All 32 lanes
+// call it.
+__device__ __forceinline__ void pick16_from_candidates(uint2 *cand_words, uint32_t total, int lane,
                                                        uint32_t &mine_key, uint32_t &mine_id) {
+    unsigned long long *cand = reinterpret_cast<unsigned long long *>(cand_words);
     const bool has0 = (uint32_t)lane < total, has1 = (uint32_t)lane + 32u < total;
-    const uint2 c0 = has0 ? cand[lane] : make_uint2(0u, 0xFFFFFFFFu);
-    const uint2 c1 = has1 ? cand[lane + 32] : make_uint2(0u, 0xFFFFFFFFu);
+    const unsigned long long c0 = has0 ? cand[lane] : 0ull;
+    const unsigned long long c1 = has1 ? cand[lane + 32] : 0ull;
     uint32_t rank0 = 0u, rank1 = 0u;
 #pragma unroll 4
     for (uint32_t j = 0; j < total; ++j) {
-        const uint2 o = cand[j];
-        rank0 += (o.x > c0.x || (o.x == c0.x && o.y < c0.y)) ? 1u : 0u;
-        rank1 += (o.x > c1.x || (o.x == c1.x && o.y < c1.y)) ? 1u : 0u;
+        const unsigned long long o = cand[j];
+        rank0 += o > c0 ? 1u : 0u;
+        rank1 += o > c1 ? 1u : 0u;
     }
     __syncwarp();
     if (has0 && rank0 < 16u) cand[rank0] = c0;
@@ -83,10 +91,60 @@ __device__ __forceinline__ void pick16_from_candidates(uint2 *cand, uint32_t tot
     mine_key = 0u;
     mine_id = 0u;
     if (lane < 16) {
-        mine_key = cand[lane].x;
-        mine_id = cand[lane].y;
+        const unsigned long long c = cand[lane];
+        mine_key = (uint32_t)(c >> 32);
+        mine_id = ~(uint32_t)c;
     }
     __syncwarp();
+}
+
+// Rows with more than kCandMax candidates (heavy ties at the threshold, or
+// fewer than 16 numbers): 16 rounds of (largest key, lowest id) over every
+// key the warp holds (lane l: ids 32 j + l); lane i < 16 gets the i-th pick.
+__device__ __forceinline__ void pick16_by_rounds(uint32_t (&key)[kPerLane], int lane,
+                                                 uint32_t &mine_key, uint32_t &mine_id) {
+    uint32_t best = 0u;
+    int best_j = 0;
+#pragma unroll
+    for (int j = 0; j < kPerLane; ++j)
+        if (key[j] > best) {
+            best = key[j];
+            best_j = j;
+        }
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, best);
+        const uint32_t c = (best == top) ? (uint32_t)(32 * best_j + lane) : 0xFFFFFFFFu;
+        const uint32_t pick = __reduce_min_sync(0xFFFFFFFFu, c);
+        if (lane == i) {
+            mine_key = top;
+            mine_id = pick;
+        }
+        if ((int)(pick & 31u) == lane) {  // the owner removes the pick and rescans
+            const int js = (int)(pick >> 5);
+            best = 0u;
+            best_j = 0;
+#pragma unroll
+            for (int j = 0; j < kPerLane; ++j) {
+                if (j == js) key[j] = 0u;
+                if (key[j] > best) {
+                    best = key[j];
+                    best_j = j;
+                }
+            }
+        }
+    }
+}
+
+// Inclusive prefix sum over the lanes; the warp total in `total`.
+__device__ __forceinline__ uint32_t warp_inclusive_sum(uint32_t x, int lane, uint32_t &total) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, off);
+        if (lane >= off) x += y;
+    }
+    total = __shfl_sync(0xFFFFFFFFu, x, 31);
+    return x;
 }
 
 // Routing weights of the 16 picks (lane i < 16 holds pick i) and the
@@ -147,68 +205,46 @@ __device__ __forceinline__ void weights16_store(uint32_t mine_key, uint32_t mine
     weights16_store_terms(s_hi, s_lo, mine_id, lane, ids_out, w_out);
 }
 
-// The calling warp selects the row whose 896 keys it holds (lane l: the keys
-// of ids 32 j + l) and writes 16 ids and weights.  All 32 lanes must call
-// it; `cand` is this warp's shared buffer of kCandMax entries.
-__device__ __forceinline__ void topk16_warp_keys(uint32_t (&key)[kPerLane], int32_t *ids_out,
+// The calling warp selects the row whose 896 logits it holds (lane l: the
+// logits of ids 32 j + l) and writes 16 ids and weights.  All 32 lanes must
+// call it; `cand` is this warp's shared buffer of kCandMax entries.  The
+// threshold T is the 16th largest of the 32 lane maxima, as keys; when T is
+// a number, a logit's key is >= T exactly when the logit is >= the number
+// (NaN compares false, -0 equals +0), so only the candidates are turned
+// into keys.
+__device__ __forceinline__ void topk16_warp_vals(const float (&v)[kPerLane], int32_t *ids_out,
                                                  float *w_out, int lane, uint2 *cand) {
-    uint32_t lane_max = 0u;
+    float m = v[0];
 #pragma unroll
-    for (int j = 0; j < kPerLane; ++j) lane_max = max(lane_max, key[j]);
-    const uint32_t T = warp_16th_largest(lane_max, lane);
-
-    uint32_t cnt = 0u;
-#pragma unroll
-    for (int j = 0; j < kPerLane; ++j) cnt += (key[j] >= T) ? 1u : 0u;
-    uint32_t incl = cnt;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-        if (lane >= off) incl += y;
-    }
-    const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    for (int j = 1; j < kPerLane; ++j) m = fmaxf(m, v[j]);  // NaN only if all are NaN
+    const uint32_t T = warp_16th_largest(rank_key(m), lane);
 
     uint32_t mine_key = 0u;  // lane i keeps the i-th pick (i < 16)
     uint32_t mine_id = 0u;
-    if (total <= (uint32_t)kCandMax) {
-        uint32_t pos = incl - cnt;
+    bool done = false;
+    if (T > 1u) {  // a number: not NaN
+        const float t = key_to_float(T);
+        uint32_t cnt = 0u;
 #pragma unroll
-        for (int j = 0; j < kPerLane; ++j)
-            if (key[j] >= T) cand[pos++] = make_uint2(key[j], (uint32_t)(32 * j + lane));
-        __syncwarp();
-        pick16_from_candidates(cand, total, lane, mine_key, mine_id);
-    } else {
-        uint32_t best = 0u;
-        int best_j = 0;
+        for (int j = 0; j < kPerLane; ++j) cnt += (v[j] >= t) ? 1u : 0u;
+        uint32_t total;
+        const uint32_t incl = warp_inclusive_sum(cnt, lane, total);
+        if (total <= (uint32_t)kCandMax) {
+            unsigned long long *c64 = reinterpret_cast<unsigned long long *>(cand);
+            uint32_t pos = incl - cnt;
 #pragma unroll
-        for (int j = 0; j < kPerLane; ++j)
-            if (key[j] > best) {
-                best = key[j];
-                best_j = j;
-            }
-#pragma unroll 1
-        for (int i = 0; i < 16; ++i) {
-            const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, best);
-            const uint32_t c = (best == top) ? (uint32_t)(32 * best_j + lane) : 0xFFFFFFFFu;
-            const uint32_t pick = __reduce_min_sync(0xFFFFFFFFu, c);
-            if (lane == i) {
-                mine_key = top;
-                mine_id = pick;
-            }
-            if ((int)(pick & 31u) == lane) {  // the owner removes the pick and rescans
-                const int js = (int)(pick >> 5);
-                best = 0u;
-                best_j = 0;
-#pragma unroll
-                for (int j = 0; j < kPerLane; ++j) {
-                    if (j == js) key[j] = 0u;
-                    if (key[j] > best) {
-                        best = key[j];
-                        best_j = j;
-                    }
-                }
-            }
+            for (int j = 0; j < kPerLane; ++j)
+                if (v[j] >= t) c64[pos++] = pack_cand(rank_key(v[j]), (uint32_t)(32 * j + lane));
+            __syncwarp();
+            pick16_from_candidates(cand, total, lane, mine_key, mine_id);
+            done = true;
         }
+    }
+    if (!done) {
+        uint32_t key[kPerLane];
+#pragma unroll
+        for (int j = 0; j < kPerLane; ++j) key[j] = rank_key(v[j]);
+        pick16_by_rounds(key, lane, mine_key, mine_id);
     }
     weights16_store(mine_key, mine_id, lane, ids_out, w_out);
 }
@@ -218,10 +254,10 @@ __device__ __forceinline__ void topk16_warp_keys(uint32_t (&key)[kPerLane], int3
 // call it; `cand` is this warp's shared buffer of kCandMax entries.
 __device__ __forceinline__ void topk16_warp(const float *row, int32_t *ids_out, float *w_out,
                                             int lane, uint2 *cand) {
-    uint32_t key[kPerLane];
+    float v[kPerLane];
 #pragma unroll
-    for (int j = 0; j < kPerLane; ++j) key[j] = rank_key(row[32 * j + lane]);
-    topk16_warp_keys(key, ids_out, w_out, lane, cand);
+    for (int j = 0; j < kPerLane; ++j) v[j] = row[32 * j + lane];
+    topk16_warp_vals(v, ids_out, w_out, lane, cand);
 }
 
 // The 16 picks (lane i < 16 keeps the i-th, as a key and an id) of the n
@@ -241,55 +277,21 @@ __device__ __forceinline__ void topk16_warp_picks(const float *row, int n, int l
     uint32_t cnt = 0u;
 #pragma unroll
     for (int j = 0; j < kPerLane; ++j) cnt += (key[j] >= T) ? 1u : 0u;
-    uint32_t incl = cnt;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-        if (lane >= off) incl += y;
-    }
-    const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    uint32_t total;
+    const uint32_t incl = warp_inclusive_sum(cnt, lane, total);
     mine_key = 0u;
     mine_id = 0u;
     if (total <= (uint32_t)kCandMax) {
+        unsigned long long *c64 = reinterpret_cast<unsigned long long *>(cand);
         uint32_t pos = incl - cnt;
 #pragma unroll
         for (int j = 0; j < kPerLane; ++j)
-            if (key[j] >= T) cand[pos++] = make_uint2(key[j], (uint32_t)(32 * j + lane));
+            if (key[j] >= T) c64[pos++] = pack_cand(key[j], (uint32_t)(32 * j + lane));
         __syncwarp();
         pick16_from_candidates(cand, total, lane, mine_key, mine_id);
         return;
     }
-    uint32_t best = 0u;
-    int best_j = 0;
-#pragma unroll
-    for (int j = 0; j < kPerLane; ++j)
-        if (key[j] > best) {
-            best = key[j];
-            best_j = j;
-        }
-#pragma unroll 1
-    for (int i = 0; i < 16; ++i) {
-        const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, best);
-        const uint32_t c = (best == top) ? (uint32_t)(32 * best_j + lane) : 0xFFFFFFFFu;
-        const uint32_t pick = __reduce_min_sync(0xFFFFFFFFu, c);
-        if (lane == i) {
-            mine_key = top;
-            mine_id = pick;
-        }
-        if ((int)(pick & 31u) == lane) {
-            const int js = (int)(pick >> 5);
-            best = 0u;
-            best_j = 0;
-#pragma unroll
-            for (int j = 0; j < kPerLane; ++j) {
-                if (j == js) key[j] = 0u;
-                if (key[j] > best) {
-                    best = key[j];
-                    best_j = j;
-                }
-            }
-        }
-    }
+    pick16_by_rounds(key, lane, mine_key, mine_id);
 }
 
 // Shared memory of topk16_block.

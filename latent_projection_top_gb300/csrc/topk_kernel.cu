@@ -80,7 +80,9 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock)
 
 // A column shard's local top-16, one warp per row: global ids and the
 // picks' logits (the candidates route_merge_candidates ranks).
-__global__ void __launch_bounds__(32 * kRowsPerBlock)
+// (80 registers at most: under __launch_bounds__ alone it compiled to 64 with
+// a spilled word)
+__global__ void __maxnreg__(80)
     shard_topk16_kernel(const float *__restrict__ logits, int rows, int n, int id_base,
                         int32_t *__restrict__ cand_ids, float *__restrict__ cand_logits) {
     __shared__ uint2 cand[kRowsPerBlock][kCandMax];
