@@ -921,8 +921,56 @@ def sweep(rb, dist, peaks, args):
                 algo = WEIGHT_BYTES + rows * (ROW_BYTES + (4 if var.get("sumsq") else 0))
                 e.update({"bound": "hbm", "frac": round(algo / t / 1e9 / peaks["hbm_gbs"], 4)})
             res.append(e)
+    res += eager_sweep(rb, dist)
     res += shard_sweep(rb, dist)
     return res
+
+
+def eager_sweep(rb, dist, n: int = 4096):
+    """Decode layers launched eagerly (no graph), 8 weight banks cycled,
+    overlap on: through route_step (tensors checked on every call) and
+    through Step objects (checked once).  Per-layer time = CUDA events around
+    the n launches; the host's enqueue time per layer beside it."""
+    torch, route = rb.torch, rb.route
+    out = []
+    rows, wk = 8, "decode_r8"
+    for how in ("route_step", "Step"):
+        with guarded(f"eager {how}"):
+            plan = route.Plan(route.DECODE, rows, rb.device)
+            route.route_set_overlap(plan, True)
+            banks = rb.weight_banks("decode", 8)
+            hs = rb.hidden(wk, rows, 8)
+            outs = [rb.outputs(rows) for _ in range(8)]
+            s = torch.cuda.Stream(device=rb.dev)
+            s.wait_stream(torch.cuda.current_stream(rb.dev))
+            if how == "Step":
+                calls = [route.Step(plan, h, wl, wr, *o, stream=s)
+                         for (wl, wr), h, o in zip(banks, hs, outs)]
+            else:
+                calls = [(lambda h=h, wl=wl, wr=wr, o=o:
+                          route.route_step(plan, h, wl, wr, *o, stream=s))
+                         for (wl, wr), h, o in zip(banks, hs, outs)]
+            for i in range(64):
+                calls[i % 8]()
+            torch.cuda.synchronize(rb.dev)
+            dist.barrier()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(s):
+                e0.record(s)
+                t0 = time.perf_counter()
+                for i in range(n):
+                    calls[i % 8]()
+                t1 = time.perf_counter()
+                e1.record(s)
+            e1.synchronize()
+            us = dist.max(e0.elapsed_time(e1)) * 1e3 / n
+            route.route_device_status(plan)
+            plan.close()
+        out.append({"workload": wk, "rows": rows, "overlap": True, "launch": f"eager, {how}",
+                    "us_per_layer": round(us, 3), "host_us_per_layer": round((t1 - t0) / n * 1e6, 3),
+                    "layers": n})
+    return out
 
 
 def shard_sweep(rb, dist):

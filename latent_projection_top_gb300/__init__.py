@@ -13,6 +13,9 @@ The route step of one MoE layer (see ``include/route.h``):
 * ``topk16_select`` -- standalone top-16 with sigmoid-renormalised weights;
 * ``route_step`` -- both (for decode plans, a weight-stream kernel and a kernel
   that finishes the split-K sums and runs the top-16);
+* ``Step`` -- ``route_step`` on fixed device tensors, checked once (each call
+  is one C call: for eager loops whose host time would otherwise exceed a
+  decode step's device time);
 * ``route_step_sumsq`` -- ``route_step`` plus each latent row's sum of squares;
 * ``route_step_host`` -- ``route_step`` with host tensors (transfers included);
   ``HostStep`` -- the same on fixed buffers, checked once and (decode,
@@ -403,6 +406,31 @@ def route_step_host(plan: Plan, hidden_host, W_latent, W_router, latent_host, lo
     args = _host_step_args(plan, hidden_host, W_latent, W_router, latent_host, logits_host,
                            ids_host, weights_host)
     _check(lib().route_step_host(plan.handle, *args, _stream(stream, plan.device)))
+
+
+class Step:
+    """``route_step`` on fixed device tensors, checked once.
+
+    For an eager loop that runs the step on the same buffers every time (new
+    values written into ``hidden``, results read from the outputs): the
+    tensors are validated and their pointers marshalled here, so each call
+    is one C call (the library reuses its tensor maps for unchanged
+    addresses).  The object keeps references to the tensors and the plan;
+    the caller must not resize them.  Once the plan is closed a call raises.
+    """
+
+    def __init__(self, plan: Plan, hidden, W_latent, W_router, latent, logits, ids, weights,
+                 stream=None):
+        p = _proj_ptrs(plan, hidden, W_latent, W_router, latent, logits)
+        i, w = _topk_ptrs(plan, ids, weights)
+        self._keep = (plan, hidden, W_latent, W_router, latent, logits, ids, weights, stream)
+        self._args = (plan.handle,) + tuple(p) + (i, w, _stream(stream, plan.device))
+        self._fn = lib().route_step
+
+    def __call__(self) -> None:
+        st = self._fn(*self._args)
+        if st != ROUTE_OK:
+            _check(st)
 
 
 class HostStep:

@@ -476,6 +476,32 @@ def test_host_step_reuses_buffers(rows):
         step()
 
 
+@pytest.mark.parametrize("mode,workload,rows", [(route.DECODE, "decode_r8", 8),
+                                               (route.PREFILL, "prefill_r1024", 300)])
+def test_step_object_equals_route_step(mode, workload, rows):
+    """Step: the tensors checked once, each call one C call on the same
+    buffers; new hidden values written in place give that call's results."""
+    _, wl, wr = bank(workload, 0)
+    dwl, dwr = to_dev_bf16(wl), to_dev_bf16(wr)
+    hs = [to_dev_bf16(np.ascontiguousarray(np.resize(bank(workload, b)[0], (rows, route.K_HIDDEN))))
+          for b in (0, 1)]
+    with route.Plan(mode, rows) as plan:
+        want = [run_step(plan, h, dwl, dwr) for h in hs]
+        h = torch.empty_like(hs[0])
+        lat, lg, ids, w = outputs(rows)
+        step = route.Step(plan, h, dwl, dwr, lat, lg, ids, w)
+        for b in (0, 1, 0):
+            h.copy_(hs[b])
+            step()
+            torch.cuda.synchronize()
+            got = (bits_of(lat), lg.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy())
+            for x, y in zip(got, want[b]):
+                assert np.array_equal(np.asarray(x).view(np.uint8), np.asarray(y).view(np.uint8))
+        route.route_device_status(plan)
+    with pytest.raises(route.RouteError):
+        step()  # the plan is closed
+
+
 def test_host_step_results_visible_on_return_many_steps():
     """route_host_step_run returns on the step's completion word, not on the
     stream: 400 steps alternating two inputs, each step's results checked in
