@@ -24,7 +24,9 @@ The route step of one MoE layer (see ``include/route.h``):
 * ``ShardPlan``, ``route_shard_step``, ``route_merge_candidates`` -- one column
   shard of the step (its latent columns, its experts and its local top-16)
   and the merge of the shards' candidates into the final top-16;
-  ``gather_candidates`` is the exchange between them (torch.distributed).
+  ``gather_candidates`` is the exchange between them (torch.distributed), and
+  ``gather_latent_logits`` the paired gather of the shards' latent and logit
+  columns into the whole layer's.
 """
 
 from __future__ import annotations
@@ -385,6 +387,31 @@ def gather_candidates(cand_ids, cand_logits, group=None):
         dist.all_gather(list(g.unbind(0)), t, group=group)
         out.append(g)
     return out[0], out[1]
+
+
+def gather_latent_logits(latent_shard, logits_shard, group=None):
+    """The paired gather of a column-sharded step, one shard per rank: every
+    rank's [rows, 3584/W] BF16 latent columns and [rows, 896/W] FP32 logit
+    columns travel together in one all-gather (one message per rank, the two
+    blocks side by side as bytes) and come back as the whole layer's
+    [rows, 3584] latent and [rows, 896] logits, shard s at columns s * n ..
+    (s + 1) * n.  Layout plumbing around the collective; needs an initialised
+    torch.distributed group (NCCL for device tensors)."""
+    torch = _torch()
+    import torch.distributed as dist
+    W = dist.get_world_size(group)
+    lat, lg = latent_shard.contiguous(), logits_shard.contiguous()
+    R, NL = lat.shape
+    NE = lg.shape[1]
+    if lg.shape[0] != R or lat.dtype != torch.bfloat16 or lg.dtype != torch.float32:
+        raise ValueError("latent_shard [rows, n] BF16 and logits_shard [rows, m] FP32 expected")
+    mine = torch.cat([lat.view(torch.uint8), lg.view(torch.uint8)], dim=1)  # [R, 2 NL + 4 NE]
+    g = torch.empty((W,) + tuple(mine.shape), dtype=torch.uint8, device=mine.device)
+    dist.all_gather(list(g.unbind(0)), mine, group=group)
+    latent = g[:, :, :2 * NL].contiguous().view(torch.bfloat16)        # [W, R, NL]
+    logits = g[:, :, 2 * NL:].contiguous().view(torch.float32)        # [W, R, NE]
+    return (latent.permute(1, 0, 2).reshape(R, W * NL),
+            logits.permute(1, 0, 2).reshape(R, W * NE))
 
 
 def _host_step_args(plan, hidden_host, W_latent, W_router, latent_host, logits_host, ids_host,

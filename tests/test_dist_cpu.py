@@ -143,3 +143,46 @@ def test_candidate_exchange_and_merge_across_ranks(world):
     assert sorted(r["rank"] for r in res) == list(range(world))
     for r in res:
         assert r["layout"] and r["ids"] and r["weights"], r
+
+
+PAIRED_CHILD = """
+import json, sys
+sys.path.insert(0, {root!r})
+import numpy as np, torch, torch.distributed as dist
+import latent_projection_top_gb300 as route
+dist.init_process_group("gloo")
+r, W = dist.get_rank(), dist.get_world_size()
+rows = 20
+NL, NE = route.N_LATENT // W, route.N_EXPERTS // W
+g = torch.Generator().manual_seed(7)                 # the same whole layer on every rank
+lat = torch.randn(rows, route.N_LATENT, generator=g).to(torch.bfloat16)
+lg = torch.randn(rows, route.N_EXPERTS, generator=g)
+lg[0, 3] = float("nan"); lg[1, 5] = -0.0            # bits travel unchanged
+mine_lat = lat[:, r * NL:(r + 1) * NL].clone()
+mine_lg = lg[:, r * NE:(r + 1) * NE].clone()
+got_lat, got_lg = route.gather_latent_logits(mine_lat, mine_lg)
+ok_lat = bool(torch.equal(got_lat.view(torch.int16), lat.view(torch.int16)))
+ok_lg = bool(torch.equal(got_lg.view(torch.int32), lg.view(torch.int32)))
+shape = list(got_lat.shape) == [rows, route.N_LATENT] and list(got_lg.shape) == [rows, route.N_EXPERTS]
+print(json.dumps({{"rank": r, "latent": ok_lat, "logits": ok_lg, "shape": shape}}))
+dist.destroy_process_group()
+"""
+
+
+@pytest.mark.parametrize("world", [2, 4])
+def test_paired_gather_of_latent_and_logit_columns(world):
+    """The paired gather (gather_latent_logits): each rank's latent and logit
+    columns in one all-gather, stitched back into the whole layer's tensors
+    bit for bit (NaN and -0 included) on every rank."""
+    port = _free_port()
+    procs = [subprocess.Popen([sys.executable, "-c", PAIRED_CHILD.format(root=ROOT)],
+                              env=_env(r, world, port), stdout=subprocess.PIPE,
+                              stderr=subprocess.PIPE, text=True)
+             for r in range(world)]
+    outs = [p.communicate(timeout=300) for p in procs]
+    for p, (_, err) in zip(procs, outs):
+        assert p.returncode == 0, err[-2000:]
+    res = [json.loads(out.strip().splitlines()[-1]) for out, _ in outs]
+    assert sorted(r["rank"] for r in res) == list(range(world))
+    for r in res:
+        assert r["latent"] and r["logits"] and r["shape"], r
