@@ -730,31 +730,91 @@ __global__ void __maxnreg__(112) decode_finish_ss_kernel(const __grid_constant__
     }
 }
 
-// The finish of a column shard at decode sizes: CTA r < rows sums row r's
-// n_exp router logits (one column pair a thread), stores them, and its first
-// warp picks the shard's top-16 of them as candidates (the same selection
-// as the standalone shard top-16); CTA rows + i sums latent item i = (row,
-// latent tile), one column pair a thread, and stores the columns below
-// n_lat.  Slots are summed in segment order as two-floats, as for the whole
-// layer.
+// The finish of a column shard at decode sizes.  A shard's few column tiles
+// are streamed by many CTAs, so a value may have up to 64 partials: each
+// column pair is summed by S = 1, 2 or 4 neighbouring threads (`split`),
+// thread j of the S taking the j-th run of at most 16 consecutive slots (one
+// memory round trip), and the S two-floats are joined by a fixed shuffle
+// tree (j = 0 with 1 and 2 with 3, then the two), so that every value's bits
+// depend on the plan only.  CTA r < rows sums row r's n_exp router logits,
+// stores them, and its first warp picks the shard's top-16 of them as
+// candidates (the same selection as the standalone shard top-16); the other
+// CTAs take (row, latent tile, quarter of the tile's column pairs per
+// `split`) items and store the latent columns below n_lat.
+struct PairSum {
+    float2 hi, lo;  // the pair's two columns
+};
+
+__device__ __forceinline__ PairSum sum_slot_range(const float4 *p, int n) {
+    PairSum r{make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    float4 v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+        if (j < n) v[j] = __ldcg(p + j * kSlotF4);
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+        if (j < n) {
+            two_sum_acc(r.hi.x, r.lo.x, v[j].x);
+            r.lo.x += v[j].y;
+            two_sum_acc(r.hi.y, r.lo.y, v[j].z);
+            r.lo.y += v[j].w;
+        }
+    return r;
+}
+
+// Joins the two-floats of the `split` threads of a pair (lanes aligned to
+// `split`); the pair's first thread ends with the total.
+__device__ __forceinline__ void join_split(PairSum &s, int split) {
+    for (int off = 1; off < split; off <<= 1) {
+        const float hx = __shfl_down_sync(0xFFFFFFFFu, s.hi.x, off);
+        const float hy = __shfl_down_sync(0xFFFFFFFFu, s.hi.y, off);
+        const float lx = __shfl_down_sync(0xFFFFFFFFu, s.lo.x, off);
+        const float ly = __shfl_down_sync(0xFFFFFFFFu, s.lo.y, off);
+        two_sum_acc(s.hi.x, s.lo.x, hx);
+        s.lo.x += lx;
+        two_sum_acc(s.hi.y, s.lo.y, hy);
+        s.lo.y += ly;
+    }
+}
+
+// Thread j of the `split` threads of column pair cc of tile t, row r: its
+// run of the tile's slots.
+__device__ __forceinline__ SlotRun split_run(const DecodeArgs &a, int r, int t, int cc, int split,
+                                             int j) {
+    SlotRun run = slot_run(a, r, t, cc);
+    const int per = (run.n + split - 1) / split;
+    const int s0 = j * per < run.n ? j * per : run.n;
+    const int s1 = s0 + per < run.n ? s0 + per : run.n;
+    run.p += (size_t)s0 * kSlotF4;
+    run.n = s1 - s0;
+    return run;
+}
+
 __global__ void __maxnreg__(112)
     decode_shard_finish_kernel(const __grid_constant__ DecodeArgs a, int n_lat, int n_exp,
                                int id_base, int32_t *__restrict__ cand_ids,
-                               float *__restrict__ cand_logits) {
+                               float *__restrict__ cand_logits, int split) {
     __shared__ uint2 s_cand[kCandMax];
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x;
     const int b = blockIdx.x;
     const int rows = a.rows;
+    const int j = tid % split;
     if (b < rows) {
         const int r = b;
         float *lrow = a.logits + (size_t)r * n_exp;
         asm volatile("griddepcontrol.wait;" ::: "memory");  // the stream kernel's partials are complete
-        for (int c = 2 * tid; c < n_exp; c += 2 * kFinishThreads) {  // one pass below 513 experts
-            SlotRun run[1] = {slot_run(a, r, a.lat_tiles + c / kDTileCols, c % kDTileCols)};
-            float2 y[1];
-            sum_slot_pairs<1, 16>(run, y);
-            if (ROUTE_IN_BOUNDS(c + 1 < n_exp, a.words)) *reinterpret_cast<float2 *>(lrow + c) = y[0];
+        const int pairs = n_exp / 2;
+        for (int i0 = 0; i0 < pairs * split; i0 += kFinishThreads) {  // whole warps in every pass
+            const int i = i0 + tid, c = 2 * (i / split);
+            const bool mine = c < n_exp;
+            SlotRun run = mine ? split_run(a, r, a.lat_tiles + c / kDTileCols, c % kDTileCols, split, j)
+                               : SlotRun{nullptr, 0};
+            PairSum ps = sum_slot_range(run.p, run.n);
+            join_split(ps, split);
+            if (mine && j == 0 && ROUTE_IN_BOUNDS(c + 1 < n_exp, a.words))
+                *reinterpret_cast<float2 *>(lrow + c) = make_float2(
+                    two_float_value(ps.hi.x, ps.lo.x), two_float_value(ps.hi.y, ps.lo.y));
         }
         __syncthreads();  // the row's logits are stored
         if (tid < 32) {
@@ -766,17 +826,21 @@ __global__ void __maxnreg__(112)
             }
         }
     } else {
-        const int i = b - rows, r = i / a.lat_tiles, t = i % a.lat_tiles;
-        const int cc = 2 * tid, col = t * kDTileCols + cc;
+        // item (row, tile, part): part q covers column pairs q * 256 / split ..
+        const int parts = split > 2 ? split / 2 : 1;
+        const int i = b - rows, q = i % parts, t = (i / parts) % a.lat_tiles,
+                  r = i / (parts * a.lat_tiles);
+        const int cc = 2 * (q * (kFinishThreads / split) + tid / split), col = t * kDTileCols + cc;
         const bool mine = cc < kDTileCols && col < n_lat;
-        SlotRun run[1] = {mine ? slot_run(a, r, t, cc) : SlotRun{nullptr, 0}};
-        pin(run[0]);
+        SlotRun run = mine ? split_run(a, r, t, cc, split, j) : SlotRun{nullptr, 0};
+        pin(run);
         asm volatile("griddepcontrol.wait;" ::: "memory");  // the stream kernel's partials are complete
-        float2 y[1];
-        sum_slot_pairs<1, 16>(run, y);
-        if (mine && ROUTE_IN_BOUNDS(r < rows && col + 1 < n_lat, a.words))
+        PairSum ps = sum_slot_range(run.p, run.n);
+        join_split(ps, split);
+        if (mine && j == 0 && ROUTE_IN_BOUNDS(r < rows && col + 1 < n_lat, a.words))
             *reinterpret_cast<uint32_t *>(a.latent + (size_t)r * n_lat + col) =
-                (uint32_t)bf16_bits(y[0].x) | ((uint32_t)bf16_bits(y[0].y) << 16);
+                (uint32_t)bf16_bits(two_float_value(ps.hi.x, ps.lo.x)) |
+                ((uint32_t)bf16_bits(two_float_value(ps.hi.y, ps.lo.y)) << 16);
     }
 }
 
@@ -826,15 +890,20 @@ cudaError_t decode_shard_launch(int bn, const CUtensorMap &map_h, const CUtensor
                                 int n_exp, int id_base, int32_t *cand_ids, float *cand_logits,
                                 cudaStream_t stream) {
     if (n_exp < kTopK || n_exp > kExpertsTopk || args.lat_tiles < 1) return cudaErrorInvalidValue;
+    int most = 0;  // partials of a value: the CTAs covering a tile
+    for (int t = 0; t < args.tiles; ++t) most = args.seg_count[t] > most ? args.seg_count[t] : most;
+    const int split = most <= 16 ? 1 : most <= 32 ? 2 : most <= 64 ? 4 : 0;
+    if (split == 0) return cudaErrorInvalidValue;
     cudaError_t e = bn == 16   ? launch_bn<16>(map_h, map_wl, map_wr, args, stream)
                     : bn == 32 ? launch_bn<32>(map_h, map_wl, map_wr, args, stream)
                                : cudaErrorInvalidValue;
     if (e != cudaSuccess) return e;
+    const int parts = split > 2 ? split / 2 : 1;  // CTAs per (row, latent tile)
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t c = pdl_config(dim3(args.rows * (1 + args.lat_tiles)), dim3(kFinishThreads),
-                                      0, stream, attr);
+    cudaLaunchConfig_t c = pdl_config(dim3(args.rows * (1 + args.lat_tiles * parts)),
+                                      dim3(kFinishThreads), 0, stream, attr);
     return cudaLaunchKernelEx(&c, decode_shard_finish_kernel, args, n_lat, n_exp, id_base, cand_ids,
-                              cand_logits);
+                              cand_logits, split);
 }
 
 cudaError_t decode_launch(int bn, const CUtensorMap &map_h, const CUtensorMap &map_wl,

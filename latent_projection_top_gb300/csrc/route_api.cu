@@ -376,14 +376,14 @@ bool build_schedule(int rows, bool ksplit, int max_pairs, int lat_tiles, int rou
 // runs: every CTA streams the same number of bytes, and its k-blocks pair up
 // on one accumulator without a pair crossing a tile (tiles start at even
 // units).  The whole layer's 18 tiles: 144 CTAs of 14 units on 152 SMs.
-// At most 16 CTAs a tile, so that the finish adds at most 16 partials per
-// value in one memory round trip (this binds only a column shard's few
-// tiles).  Never below the tile count, which route_prepare requires of the
-// device.
+// At most 64 CTAs a tile: a column shard's finish sums a value's partials
+// with up to four threads of at most 16 each, one memory round trip (this
+// binds only a column shard's few tiles).  Never below the tile count, which
+// route_prepare requires of the device.
 int decode_grid(int sms, int cap, int tiles = kDTiles) {
     const int U = tiles * kKBlocks;
     int hi = sms < cap ? sms : cap;
-    hi = hi < 16 * tiles ? hi : 16 * tiles;
+    hi = hi < 64 * tiles ? hi : 64 * tiles;
     for (int g = hi; g > tiles; --g)
         if ((U / 2) % g == 0) return g;
     return tiles;
