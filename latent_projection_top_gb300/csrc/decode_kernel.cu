@@ -19,8 +19,9 @@
 //   a fresh TMEM accumulator per pair of k-blocks (runs are even and tiles
 //   start at even units, so a pair never crosses a tile); eight epilogue
 //   warps add each pair's FP32 result into a two-float (TwoSum) running sum
-//   kept in TMEM next to the accumulators, so the only rounding left is the
-//   tensor core's inside one 128-long block.  Pairing halves the epilogue's
+//   kept in TMEM next to the accumulators (two rows at a time in packed FP32
+//   pairs), so the only rounding left is the tensor core's inside one
+//   128-long block.  Pairing halves the epilogue's
 //   TMEM traffic, two-float work and barrier hand-offs per streamed byte,
 //   which set the pace at 17..20 rows (measured 12.6 -> 11.3 us a layer at
 //   20 rows, 10.7 -> 10.4 at 8).  A CTA's run covers at most two tiles; the
@@ -36,6 +37,9 @@
 //   row's bits do not depend on the row count (the partition depends only on
 //   the grid).  With each latent row's sum of squares asked for, the same
 //   work runs as decode_finish_ss_kernel, one thread-block cluster per row.
+//   A column shard's plan streams only its own tiles (up to 64 CTAs a tile)
+//   and finishes with decode_shard_finish_kernel, which sums each value's
+//   partials with up to four threads and picks the shard's candidates.
 //
 // Programmatic dependent launch: both kernels let their successor launch at
 // once.  The stream kernel prefetches its first weight boxes (model
