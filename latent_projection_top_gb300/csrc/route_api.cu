@@ -944,11 +944,16 @@ route_status route_host_step_run(route_host_step *step) {
     // Wait for this step's number in the completion word (the results are
     // in host memory before it); after kHostWaitNs without it, wait for the
     // stream instead and report what it reports.
+    // (A number at or past `want`, in wrap-around order, also counts, so that
+    // a step that completed after an earlier call gave up cannot stall the
+    // next.)
     const unsigned want = step->done + 1u;
+    auto reached = [&](unsigned v) { return (int)(v - want) >= 0; };
     const auto t0 = std::chrono::steady_clock::now();
     for (uint32_t it = 1;; ++it) {
-        if (__atomic_load_n(step->flag_host, __ATOMIC_ACQUIRE) == want) {
-            step->done = want;
+        const unsigned v = __atomic_load_n(step->flag_host, __ATOMIC_ACQUIRE);
+        if (reached(v)) {
+            step->done = v;
             return ROUTE_OK;
         }
         if ((it & 1023u) == 0u &&
@@ -957,9 +962,10 @@ route_status route_host_step_run(route_host_step *step) {
     }
     if ((e = cudaStreamSynchronize(step->stream)) != cudaSuccess)
         return cuda_fail(e, "cudaStreamSynchronize");
-    if (__atomic_load_n(step->flag_host, __ATOMIC_ACQUIRE) != want)
+    const unsigned v = __atomic_load_n(step->flag_host, __ATOMIC_ACQUIRE);
+    if (!reached(v))
         return fail(ROUTE_ERR_DEVICE, "the host step finished without its completion word");
-    step->done = want;
+    step->done = v;
     return ROUTE_OK;
 }
 
