@@ -944,9 +944,10 @@ route_status route_host_step_run(route_host_step *step) {
     // Wait for this step's number in the completion word (the results are
     // in host memory before it); after kHostWaitNs without it, wait for the
     // stream instead and report what it reports.
-    // (A number at or past `want`, in wrap-around order, also counts, so that
-    // a step that completed after an earlier call gave up cannot stall the
-    // next.)
+    // Every return below leaves no launch of this step unfinished (the wait
+    // ends on this step's number, or after the stream has drained), and
+    // `done` takes the word's value then, so the next call waits for exactly
+    // its own number.
     const unsigned want = step->done + 1u;
     auto reached = [&](unsigned v) { return (int)(v - want) >= 0; };
     const auto t0 = std::chrono::steady_clock::now();
@@ -963,9 +964,9 @@ route_status route_host_step_run(route_host_step *step) {
     if ((e = cudaStreamSynchronize(step->stream)) != cudaSuccess)
         return cuda_fail(e, "cudaStreamSynchronize");
     const unsigned v = __atomic_load_n(step->flag_host, __ATOMIC_ACQUIRE);
+    step->done = v;
     if (!reached(v))
         return fail(ROUTE_ERR_DEVICE, "the host step finished without its completion word");
-    step->done = v;
     return ROUTE_OK;
 }
 
