@@ -99,6 +99,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Prefetch of one 2-D box at (x, y) into L2 (no shared memory, no barrier):
+// a later tma_load_2d of the same box finds it there.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // 2-D tiled store of one box from shared memory to global memory at (x, y);
 // elements outside the tensor map's bounds are not written.  Tracked as a
 // bulk async-group of the issuing thread.
