@@ -389,10 +389,11 @@ int decode_grid(int sms, int cap, int tiles = kDTiles) {
     return tiles;
 }
 
-// Units past the first ring whose weights a decode CTA sends to L2 before
-// its grid dependency resolves (without overlap).  Measured, interleaved in
-// one process: 2 takes 0.06-0.42 us off a step that waits for the previous
-// one and 0.25 us off a step after a producer kernel; 8 is slower there.
+// Units past the first ring whose weights a decode CTA sends to L2 at its
+// start.  Measured, interleaved in one process: 2 takes 0.24-0.45 us off a
+// layer at 1-16 rows and 0.10-0.18 us at 20 rows with overlap, 0.06-0.42 us
+// without, 0.25 us after a producer kernel; 3 and more are slower at 16-20
+// rows.
 constexpr int kDecodePreL2 = 2;
 
 // Decode split-K partition: CTA g owns a contiguous run of (tile, k-block)
