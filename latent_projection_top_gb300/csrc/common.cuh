@@ -107,7 +107,7 @@ struct DecodeArgs {
     int ksplit;          // latent with the general path's K-split arithmetic
     int lat_tiles;       // latent column tiles (14; a column shard's: ceil(its columns / 256))
     int tiles;           // latent + router column tiles (18, or a column shard's)
-    int pre_l2;          // units past the first ring's whose weights go to L2 before the wait
+    int pre_l2;          // units after the first ring whose weights go to L2 at the CTA's start
     unsigned long long timeout_ns;
     int cta_unit[kMaxGrid + 1];  // CTA g owns units [cta_unit[g], cta_unit[g+1]); unit u =
                                  // (tile u / 112, k-block u % 112)
