@@ -71,7 +71,7 @@ template <int BN>
 struct DecCfg {
     static constexpr uint32_t kBStageBytes = BN * 128;  // BN rows x 64 k, BF16
     static constexpr uint32_t kStageBytes = kDAStageBytes + kBStageBytes;
-    static constexpr int kStages = 4;  // measured: 4 (and 3) beat 5 and 6 under back-to-back steps
+    static constexpr int kStages = 4;  // measured, with and without the L2 start prefetch: 4 beats 3, 5 and 6
     static constexpr uint32_t kAccCols = 2 * BN;       // two 128-column blocks per accumulator
     // TMEM columns: kNumAcc accumulators (k-block pairs in flight), then the
     // running sums, per column block BN hi columns and BN lo columns.
