@@ -42,11 +42,12 @@
 //   partials with up to four threads and picks the shard's candidates.
 //
 // Programmatic dependent launch: both kernels let their successor launch at
-// once.  The stream kernel prefetches its first weight boxes (model
-// parameters, which no predecessor writes) before `griddepcontrol.wait`.  By
-// default it reads the hidden rows only after the wait; with `overlap` set it
-// reads them at once and waits only before it writes scratch (at the end of
-// its stream), so one step's weight stream runs under the previous step's
+// once.  The stream kernel requests its first weight boxes (model
+// parameters, which no predecessor writes) before `griddepcontrol.wait`, and
+// the weights of its next two units into L2, a deeper start than its ring.
+// By default it reads the hidden rows only after the wait; with `overlap` set
+// it reads them at once and waits only before it writes scratch (at the end
+// of its stream), so one step's weight stream runs under the previous step's
 // finish kernel.
 #include <cuda_bf16.h>
 
