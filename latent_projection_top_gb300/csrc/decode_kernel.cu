@@ -382,7 +382,8 @@ __global__ void __maxnreg__(BN == 16 ? 80 : 88)
             // Scratch may still be read by the predecessor's finish kernel.
             if (last) asm volatile("griddepcontrol.wait;" ::: "memory");
             const int slot = args.seg_base[t] + (g - args.cta_first[t]);
-            const int nslots = args.seg_base[args.tiles - 1] + args.seg_count[args.tiles - 1];
+            [[maybe_unused]] const int nslots =  // read by the checked library's index check
+                args.seg_base[args.tiles - 1] + args.seg_count[args.tiles - 1];
             const bool slot_ok = ROUTE_IN_BOUNDS(
                 t < args.tiles && slot >= 0 && slot < nslots && col < kDTileCols, args.words);
             float2 *const out =
