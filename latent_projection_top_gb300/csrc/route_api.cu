@@ -117,7 +117,7 @@ route_status get_encode(EncodeTiledFn *out) {
 route_status encode_2d(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer,
                        uint32_t box_inner, uint32_t box_outer, const char *what,
                        bool fp32 = false, bool swizzle = true) {
-    EncodeTiledFn enc;
+    EncodeTiledFn enc = nullptr;
     route_status st = get_encode(&enc);
     if (st != ROUTE_OK) return st;
     const uint64_t esize = fp32 ? 4 : 2;
@@ -473,7 +473,7 @@ route_status noalloc_setup(int device, NoAllocDevice **out) {
                         decode_smem_bytes(bn));
         if ((e = decode_configure(bn)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
     }
-    EncodeTiledFn enc;
+    EncodeTiledFn enc = nullptr;
     route_status st = get_encode(&enc);
     if (st != ROUTE_OK) return st;
     void *ptr = nullptr;
@@ -520,7 +520,7 @@ route_status prepare_plan(int mode, int rows, int device, int shard, int num_sha
     if (prop.major != 10 || prop.minor != 3)
         return fail(ROUTE_ERR_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a only",
                     device, prop.major, prop.minor);
-    EncodeTiledFn enc;
+    EncodeTiledFn enc = nullptr;
     route_status st = get_encode(&enc);
     if (st != ROUTE_OK) return st;
 
