@@ -23,12 +23,14 @@ def test_plain_c_program_on_the_abi(tmp_path):
     ora = oracle.build()
     cuda = os.path.dirname(os.path.dirname(builder.NVCC))
     exe = str(tmp_path / "route_abi_check")
+    # the library the binding loads (the checked one under ROUTE_DEBUG_LIB=1),
+    # linked by its path
     lib_dirs = [os.path.dirname(lib), os.path.dirname(ora), os.path.join(cuda, "lib64")]
     cmd = ["gcc", "-std=c11", "-O2", "-Wall", "-o", exe, os.path.join(HERE, "c", "route_abi_check.c"),
-           "-I", os.path.join(ROOT, "include"), "-I", os.path.join(cuda, "include")]
+           "-I", os.path.join(ROOT, "include"), "-I", os.path.join(cuda, "include"), lib, ora]
     for d in lib_dirs:
         cmd += ["-L", d, f"-Wl,-rpath,{d}"]
-    cmd += ["-lroute", "-loracle", "-lcudart", "-lm"]
+    cmd += ["-lcudart", "-lm"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     assert res.returncode == 0, res.stderr[-3000:]
     run = subprocess.run([exe], capture_output=True, text=True, timeout=600)
