@@ -87,7 +87,7 @@ def _whole(h_dev, wl, wr, rows, ksplit=False):
         return run_step(plan, h_dev, to_dev_bf16(wl), to_dev_bf16(wr))
 
 
-@pytest.mark.parametrize("W", [2, 4, 8, 16, 1])
+@pytest.mark.parametrize("W", [2, 4, 7, 8, 14, 16, 1])
 def test_shards_then_merge_equal_the_whole_layer_and_the_oracle(W):
     rows = 300  # two 256-row blocks, the second ragged
     hid, wl, wr = bank("prefill_r3072", 0)
@@ -118,7 +118,8 @@ def _whole_decode(h_dev, wl, wr, rows):
 
 @pytest.mark.parametrize("workload,rows,W", [("decode_r8", 8, 8), ("decode_r8", 8, 2),
                                              ("decode_r8", 8, 16), ("decode_r1", 1, 4),
-                                             ("decode_sweep", 20, 7), ("decode_r8", 8, 1)])
+                                             ("decode_sweep", 20, 7), ("decode_r8", 8, 1),
+                                             ("decode_sweep", 12, 14), ("decode_sweep", 20, 16)])
 def test_decode_size_shards(workload, rows, W):
     """Up to 20 rows a shard streams its weights with the decode path's split
     K (TP8: 448 latent columns and 112 experts a shard; TP16: 224 and 56).
