@@ -14,7 +14,8 @@ The other row counts (1, 9, 12, 16, 20 decode; 1024 and 3072 prefill, the
 latter per 92-layer chunk) are measured the same way and reported under
 "sweep".  `e2e` repeats the headline through the host-buffer call (hidden
 rows read from pinned host memory and all results written back to it, every
-step): `HostStep`, the checked-once form of route_step_host, with the plain
+step): two `HostStep`s (the checked-once form of route_step_host) of one
+plan with two batches in flight, with one in flight and the plain
 route_step_host call timed beside it.
 `cpu_baseline` times the oracle on the host cores on a bounded sample.
 
@@ -602,20 +603,28 @@ class RouteBench:
         mode = route.DECODE if workload.startswith("decode") else route.PREFILL
         wl, wr = self.weight_banks("decode" if mode == route.DECODE else "prefill", 8)[0]
         wk = self.synth.WORKLOADS[workload]
-        hid = torch.from_numpy(wk.hidden(0, rows).view(np.int16)).view(torch.bfloat16).pin_memory()
-        lat = torch.empty((rows, route.N_LATENT), dtype=torch.bfloat16).pin_memory()
-        lg = torch.empty((rows, route.N_EXPERTS), dtype=torch.float32).pin_memory()
-        ids = torch.empty((rows, route.TOPK), dtype=torch.int32).pin_memory()
-        w = torch.empty((rows, route.TOPK), dtype=torch.float32).pin_memory()
+        def host_bufs(b):
+            return (torch.from_numpy(wk.hidden(b, rows).view(np.int16)).view(torch.bfloat16)
+                    .pin_memory(),
+                    torch.empty((rows, route.N_LATENT), dtype=torch.bfloat16).pin_memory(),
+                    torch.empty((rows, route.N_EXPERTS), dtype=torch.float32).pin_memory(),
+                    torch.empty((rows, route.TOPK), dtype=torch.int32).pin_memory(),
+                    torch.empty((rows, route.TOPK), dtype=torch.float32).pin_memory())
+
+        (hid, lat, lg, ids, w), other = host_bufs(0), host_bufs(1)
         s = torch.cuda.Stream(device=self.dev)
         with route.Plan(mode, rows, self.device) as plan:
             # route_step_host checks its tensors on every call; HostStep (the
             # serving-loop form of the same call) checks them once and launches
-            # a captured graph
+            # a captured graph; two HostSteps on their own buffers keep two
+            # batches in flight
             step = route.HostStep(plan, hid, wl, wr, lat, lg, ids, w, stream=s)
+            step_b = route.HostStep(plan, other[0], wl, wr, *other[1:], stream=s)
+            pair = (step, step_b)
             for _ in range(5):
                 route.route_step_host(plan, hid, wl, wr, lat, lg, ids, w, stream=s)
                 step()
+                step_b()
             dist.barrier()
             torch.cuda.synchronize(self.dev)
             t0 = time.perf_counter()
@@ -629,17 +638,30 @@ class RouteBench:
             for _ in range(k):
                 step()
             torch.cuda.synchronize(self.dev)
+            t_sync = time.perf_counter() - t0
+            dist.barrier()
+            torch.cuda.synchronize(self.dev)
+            t0 = time.perf_counter()
+            pair[0].launch()
+            for i in range(k):
+                if i + 1 < k:
+                    pair[(i + 1) % 2].launch()
+                pair[i % 2].wait()
+            torch.cuda.synchronize(self.dev)
             t = time.perf_counter() - t0
             dist.barrier()
-        t, t_checked = dist.max(t), dist.max(t_checked)
+        t, t_sync, t_checked = dist.max(t), dist.max(t_sync), dist.max(t_checked)
         h2d = hid.numel() * 2
         d2h = lat.numel() * 2 + lg.numel() * 4 + ids.numel() * 4 + w.numel() * 4
         return {"value": round(dist.world * k * rows / t, 1), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "us_per_step": round(t / k * 1e6, 3), "steps": k,
-                "path": "HostStep: route_step_host's copy-free path on pinned host buffers, "
-                        "prepared once as a CUDA graph (route_host_step_run); every call "
-                        "returns once its step's results are in the host buffers",
+                "path": "two HostSteps of one plan on one stream, each on its own pinned host "
+                        "buffers (route_step_host's copy-free path, prepared once as a CUDA "
+                        "graph): launch B, wait A, launch A, wait B, ...; every step reads its "
+                        "hidden rows from host memory and its wait returns once that step's "
+                        "results are in its host buffers",
+                "us_per_step_one_in_flight": round(t_sync / k * 1e6, 3),
                 "us_per_step_route_step_host": round(t_checked / k * 1e6, 3)}
 
 

@@ -182,14 +182,27 @@ route_status route_step_host(const route_plan *plan, const void *hidden_host,
  * into a CUDA graph (on a stream of the step's own), with a last one-thread
  * kernel that, once they have finished, stores the step's number into a
  * page-locked completion word after a system-scope fence.
- * route_host_step_run is one graph launch on `stream` and a wait for that
- * number in the completion word (not for the stream: the last kernel may
- * still be leaving when it returns); it returns after the results are in the
- * host buffers.  Without the number after 4 s it synchronises `stream` and
- * reports its error (or ROUTE_ERR_DEVICE).  The
- * graph keeps the plan's settings (route_set_latent_ksplit) as they were at
- * creation.  The step belongs to the plan: route_destroy releases its
- * graph, after which route_host_step_run returns ROUTE_ERR_NULL.
+ * route_host_step_run is one graph launch on `stream` and a wait (below).
+ * route_host_step_launch enqueues the same kernels with the same arguments
+ * one by one on `stream` and returns at once: unlike a graph launch, which
+ * starts once everything before it on the stream has finished, the staging
+ * kernel is chained to its predecessor by programmatic dependent launch, so
+ * that a step launched behind another one reads its hidden rows and starts
+ * streaming weights under the other's tail (it writes the plan's scratch
+ * only once the other has finished).
+ * route_host_step_wait waits for the number of the step's latest launch in
+ * the completion word (not for the stream: the last kernel may still be
+ * leaving when it returns) and returns after that launch's results are in
+ * the host buffers (at once when no launch is in flight).  Without the
+ * number after 4 s it synchronises `stream` and reports its error (or
+ * ROUTE_ERR_DEVICE).  Between a step's launch and its wait the caller
+ * neither writes its `hidden_host` nor reads its results.  Several steps of
+ * one plan may be in flight together (a serving loop with two batches:
+ * launch B, wait A, refill A, launch A, wait B, ...) when they were created
+ * with the same stream: they share the plan's device scratch, and the
+ * stream's order keeps them apart.  Both launch forms keep the plan's
+ * settings (route_set_latent_ksplit) as they were at creation.  The step belongs to the plan: route_destroy releases its
+ * graph, after which launch, wait and run return ROUTE_ERR_NULL.
  * route_host_step_destroy frees the step (NULL: no-op).  Steps and their
  * plan are not thread-safe.
  */
@@ -199,6 +212,8 @@ route_status route_host_step_create(route_plan *plan, const void *hidden_host,
                                     const void *W_latent, const void *W_router,
                                     void *latent_host, float *logits_host, int32_t *ids_host,
                                     float *weights_host, void *stream, route_host_step **out);
+route_status route_host_step_launch(route_host_step *step);
+route_status route_host_step_wait(route_host_step *step);
 route_status route_host_step_run(route_host_step *step);
 route_status route_host_step_destroy(route_host_step *step);
 

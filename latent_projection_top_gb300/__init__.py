@@ -66,7 +66,7 @@ EXPORTS = (
     "route_plan_grid", "route_plan_segments", "route_last_error", "route_test_stall",
     "route_set_overlap", "route_step_decode_noalloc", "route_step_sumsq",
     "route_set_latent_ksplit", "route_host_step_create", "route_host_step_run",
-    "route_host_step_destroy", "route_test_poison_scratch", "route_noalloc_status",
+    "route_host_step_launch", "route_host_step_wait", "route_host_step_destroy", "route_test_poison_scratch", "route_noalloc_status",
     "route_noalloc_grid", "route_prepare_shard", "route_shard_step", "route_merge_candidates",
     "route_plan_latent_cols", "route_plan_experts", "route_test_noalloc_stall",
 )
@@ -116,6 +116,8 @@ def lib() -> ctypes.CDLL:
         L.route_test_stall.restype = i32
         L.route_host_step_create.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(vp)]
         L.route_host_step_run.argtypes = [vp]
+        L.route_host_step_launch.argtypes = [vp]
+        L.route_host_step_wait.argtypes = [vp]
         L.route_host_step_destroy.argtypes = [vp]
         L.route_test_poison_scratch.argtypes = [vp, vp]
         L.route_noalloc_status.argtypes = [i32]
@@ -130,8 +132,8 @@ def lib() -> ctypes.CDLL:
         L.route_merge_candidates.restype = i32
         L.route_test_noalloc_stall.argtypes = [i32, i32, ctypes.c_uint64]
         L.route_test_noalloc_stall.restype = i32
-        for f in ("route_host_step_create", "route_host_step_run", "route_host_step_destroy",
-                  "route_test_poison_scratch"):
+        for f in ("route_host_step_create", "route_host_step_run", "route_host_step_launch",
+                  "route_host_step_wait", "route_host_step_destroy", "route_test_poison_scratch"):
             getattr(L, f).restype = i32
         for f in ("route_plan_rows", "route_plan_mode", "route_plan_grid", "route_plan_segments",
                   "route_plan_latent_cols", "route_plan_experts"):
@@ -472,6 +474,16 @@ class HostStep:
     ``route_step_host``.  The object keeps references to the tensors and the
     plan; the caller must not resize them.  ``close()`` (or the plan's)
     releases the graph.
+
+    ``launch()`` and ``wait()`` split a call in two
+    (``route_host_step_launch`` / ``route_host_step_wait``) so that two
+    steps of one plan, created on the same stream, can be in flight together:
+    launch B, wait A, refill A, launch A, wait B, ...  ``launch()`` enqueues
+    the graph's kernels directly, chained to the step before it on the
+    stream, so that the next step's weights stream in under that step's
+    tail.  Between a step's launch and its wait its hidden buffer is not
+    written and its results are not read.  Without a graph, ``launch()``
+    runs the whole step and ``wait()`` returns at once.
     """
 
     def __init__(self, plan: Plan, hidden_host, W_latent, W_router, latent_host, logits_host,
@@ -502,6 +514,23 @@ class HostStep:
         if self._fn is None:
             raise RouteError(STATUS_CODES["ROUTE_ERR_NULL"], "host step is closed")
         st = self._fn(*self._call_args)
+        if st != ROUTE_OK:
+            _check(st)
+
+    def launch(self) -> None:
+        if self._step is None:
+            self()
+            return
+        st = lib().route_host_step_launch(self._step)
+        if st != ROUTE_OK:
+            _check(st)
+
+    def wait(self) -> None:
+        if self._step is None:
+            if self._fn is None:
+                raise RouteError(STATUS_CODES["ROUTE_ERR_NULL"], "host step is closed")
+            return
+        st = lib().route_host_step_wait(self._step)
         if st != ROUTE_OK:
             _check(st)
 

@@ -66,7 +66,13 @@ struct route_host_step {
     unsigned *flag_host;
     unsigned *flag_dev;
     unsigned *counter;
-    unsigned done;            // the number of the last step that completed
+    unsigned launched;        // the number of the last step launched
+    unsigned done;            // the number of the last step seen complete
+    // For direct launches (route_host_step_launch): the mapped hidden rows,
+    // the weights, and the plan's decode arguments as they were at creation
+    // with this step's outputs filled in -- what the graph holds.
+    const void *hidden_mapped, *W_latent, *W_router;
+    route::DecodeArgs dec;
 };
 
 namespace {
@@ -934,6 +940,16 @@ route_status route_host_step_create(route_plan *plan, const void *hidden_host,
         delete step;
         return st != ROUTE_OK ? st : cuda_fail(e, "capture the host step");
     }
+    step->hidden_mapped = h;
+    step->W_latent = W_latent;
+    step->W_router = W_router;
+    step->dec = plan->dec;
+    step->dec.latent = static_cast<uint16_t *>(lat);
+    step->dec.logits = static_cast<float *>(lg);
+    step->dec.ids = static_cast<int32_t *>(ids);
+    step->dec.weights = static_cast<float *>(w);
+    step->dec.sumsq = nullptr;
+    step->dec.overlap = 0;  // after the staging kernel
     step->plan = plan;
     step->next = plan->steps;
     plan->steps = step;
@@ -941,23 +957,50 @@ route_status route_host_step_create(route_plan *plan, const void *hidden_host,
     return ROUTE_OK;
 }
 
-route_status route_host_step_run(route_host_step *step) {
+// The graph's kernels launched one by one on the step's stream, each chained
+// to its predecessor by programmatic dependent launch (the staging kernel to
+// whatever precedes it there, typically another step's completion kernel).
+static route_status enqueue_host_step(route_host_step *step) {
+    const route_plan *p = step->plan;
+    const Staging d = staging_of(p);
+    cudaError_t e = stage_in_launch(step->hidden_mapped, d.hidden, (size_t)p->rows * kHidden * 2,
+                                    step->stream);
+    if (e != cudaSuccess) return cuda_fail(e, "stage hidden rows");
+    CUtensorMap mh, ml, mr;
+    route_status st = encode_all(p, d.hidden, step->W_latent, step->W_router, &mh, &ml, &mr);
+    if (st != ROUTE_OK) return st;
+    if ((e = decode_launch(p->bn, mh, ml, mr, step->dec, 1, step->stream)) != cudaSuccess)
+        return cuda_fail(e, "decode kernel launch");
+    if ((e = host_done_launch(step->counter, step->flag_dev, step->stream)) != cudaSuccess)
+        return cuda_fail(e, "completion kernel launch");
+    return ROUTE_OK;
+}
+
+route_status route_host_step_launch(route_host_step *step) {
     g_err[0] = '\0';
     if (!step || !step->plan || !step->exec)
         return fail(ROUTE_ERR_NULL, "host step is NULL or its plan has been destroyed");
     DeviceGuard guard(step->plan->device);
     if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
-    cudaError_t e = cudaGraphLaunch(step->exec, step->stream);
-    if (e != cudaSuccess) return cuda_fail(e, "launch the host step");
-    // Wait for this step's number in the completion word (the results are
-    // in host memory before it); after kHostWaitNs without it, wait for the
-    // stream instead and report what it reports.
-    // Every return below leaves no launch of this step unfinished (the wait
-    // ends on this step's number, or after the stream has drained), and
-    // `done` takes the word's value then, so the next call waits for exactly
-    // its own number.
-    const unsigned want = step->done + 1u;
+    const route_status st = enqueue_host_step(step);
+    if (st != ROUTE_OK) return st;
+    ++step->launched;
+    return ROUTE_OK;
+}
+
+route_status route_host_step_wait(route_host_step *step) {
+    g_err[0] = '\0';
+    if (!step || !step->plan || !step->exec)
+        return fail(ROUTE_ERR_NULL, "host step is NULL or its plan has been destroyed");
+    // Wait for the latest launch's number in the completion word (the
+    // results are in host memory before it); after kHostWaitNs without it,
+    // wait for the stream instead and report what it reports.  Every return
+    // leaves no launch of this step unfinished (the wait ends on the latest
+    // number, or after the stream has drained), and `done` takes the word's
+    // value then.
+    const unsigned want = step->launched;
     auto reached = [&](unsigned v) { return (int)(v - want) >= 0; };
+    if (reached(step->done)) return ROUTE_OK;  // nothing in flight
     const auto t0 = std::chrono::steady_clock::now();
     for (uint32_t it = 1;; ++it) {
         const unsigned v = __atomic_load_n(step->flag_host, __ATOMIC_ACQUIRE);
@@ -969,13 +1012,29 @@ route_status route_host_step_run(route_host_step *step) {
             std::chrono::steady_clock::now() - t0 > std::chrono::nanoseconds(kHostWaitNs))
             break;
     }
-    if ((e = cudaStreamSynchronize(step->stream)) != cudaSuccess)
-        return cuda_fail(e, "cudaStreamSynchronize");
+    DeviceGuard guard(step->plan->device);
+    if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+    cudaError_t e = cudaStreamSynchronize(step->stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     const unsigned v = __atomic_load_n(step->flag_host, __ATOMIC_ACQUIRE);
-    step->done = v;
+    step->done = step->launched = v;  // nothing of this step is in flight now
     if (!reached(v))
         return fail(ROUTE_ERR_DEVICE, "the host step finished without its completion word");
     return ROUTE_OK;
+}
+
+route_status route_host_step_run(route_host_step *step) {
+    g_err[0] = '\0';
+    if (!step || !step->plan || !step->exec)
+        return fail(ROUTE_ERR_NULL, "host step is NULL or its plan has been destroyed");
+    {
+        DeviceGuard guard(step->plan->device);
+        if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+        const cudaError_t e = cudaGraphLaunch(step->exec, step->stream);
+        if (e != cudaSuccess) return cuda_fail(e, "launch the host step");
+        ++step->launched;
+    }
+    return route_host_step_wait(step);
 }
 
 route_status route_host_step_destroy(route_host_step *step) {

@@ -4,27 +4,40 @@
 // launch like the route kernels: it lets the next kernel launch at once (the
 // decode stream kernel then prefetches its weights while this copy runs) and
 // writes the staging buffer only after its own predecessor has completed.
+// The host rows are written by the caller before the launch, so they are
+// read before that wait: the host link's latency passes under it.
 #include "common.cuh"
 
 namespace route {
 namespace {
 
 constexpr int kStageThreads = 256;
+constexpr int kStageAhead = 4;  // 16-byte words a thread reads before the wait
 
 __global__ void __launch_bounds__(kStageThreads)
     stage_in_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst, int n16) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int stride = gridDim.x * kStageThreads;
+    const int i0 = blockIdx.x * kStageThreads + threadIdx.x;
+    uint4 v[kStageAhead];
+#pragma unroll
+    for (int j = 0; j < kStageAhead; ++j)
+        if (i0 + j * stride < n16) v[j] = src[i0 + j * stride];
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the staging buffer's last reader is done
-    for (int i = blockIdx.x * kStageThreads + threadIdx.x; i < n16; i += gridDim.x * kStageThreads)
-        dst[i] = src[i];
+#pragma unroll
+    for (int j = 0; j < kStageAhead; ++j)
+        if (i0 + j * stride < n16) dst[i0 + j * stride] = v[j];
+    for (int i = i0 + kStageAhead * stride; i < n16; i += stride) dst[i] = src[i];
 }
 
 // The last kernel of a prepared host step: once the step's kernels have
 // finished (the grid dependency) it advances the step's device counter and
 // stores the new value into a page-locked word that the calling thread
 // watches, with a system-scope fence before the store, so that the results
-// the finish kernel wrote into host memory are visible first.
+// the finish kernel wrote into host memory are visible first.  It lets the
+// next kernel on the stream (another step's staging kernel) launch at once.
 __global__ void host_done_kernel(unsigned *counter, unsigned *flag_mapped) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");  // every kernel of the step has finished
     if (threadIdx.x == 0) {
         const unsigned v = *counter + 1u;

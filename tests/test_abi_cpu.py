@@ -104,6 +104,8 @@ def test_calls_with_null_plan(lib):
     out = ctypes.c_void_p(0x1000)
     assert lib.route_host_step_create(null, x, x, x, x, x, x, x, None, ctypes.byref(out)) == 3
     assert lib.route_host_step_run(null) == 3
+    assert lib.route_host_step_launch(null) == 3
+    assert lib.route_host_step_wait(null) == 3
     assert lib.route_host_step_destroy(null) == 0
     assert lib.route_test_poison_scratch(null, None) == 3
     assert lib.route_destroy(null) == 0

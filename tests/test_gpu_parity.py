@@ -536,6 +536,86 @@ def test_host_step_results_visible_on_return_many_steps():
         step.close()
 
 
+def test_two_host_steps_in_flight_on_one_plan():
+    """Two HostSteps of one plan on one stream, pipelined: step A is launched,
+    then B is filled and launched before A is waited for, and so on for 300
+    steps over four inputs; each wait is followed by a check of that step's
+    host buffers against route_step's bits for its input.  Also: a wait with
+    nothing in flight returns at once; after two launches and one wait the
+    next launch and wait give that launch's results; a graph call of B behind
+    a direct launch of A gives both steps' results."""
+    rows = 8
+    _, wl, wr = bank("decode_r8", 0)
+    dwl, dwr = to_dev_bf16(wl), to_dev_bf16(wr)
+    hs = [np.ascontiguousarray(np.resize(bank("decode_r8", b)[0], (rows, route.K_HIDDEN)))
+          for b in range(4)]
+    s = torch.cuda.Stream()
+
+    def host_bufs():
+        return (torch.empty((rows, route.K_HIDDEN), dtype=torch.bfloat16).pin_memory(),
+                torch.empty((rows, route.N_LATENT), dtype=torch.bfloat16).pin_memory(),
+                torch.empty((rows, route.N_EXPERTS), dtype=torch.float32).pin_memory(),
+                torch.empty((rows, route.TOPK), dtype=torch.int32).pin_memory(),
+                torch.empty((rows, route.TOPK), dtype=torch.float32).pin_memory())
+
+    def check(b, got, i):
+        h, lat, lg, ids, w = got
+        assert np.array_equal(ids.numpy(), want[b][2]), f"step {i}"
+        assert np.array_equal(w.numpy().view(np.uint32), want[b][3].view(np.uint32)), f"step {i}"
+        assert np.array_equal(lg.numpy().view(np.uint32), want[b][1].view(np.uint32)), f"step {i}"
+        assert np.array_equal(lat.view(torch.int16).numpy().view(np.uint16), want[b][0]), \
+            f"step {i}"
+
+    with route.Plan(route.DECODE, rows) as plan:
+        want = [run_step(plan, to_dev_bf16(h), dwl, dwr) for h in hs]
+        src = [torch.from_numpy(h.view(np.int16).copy()).view(torch.bfloat16) for h in hs]
+        bufs = [host_bufs(), host_bufs()]
+        steps = [route.HostStep(plan, b[0], dwl, dwr, *b[1:], stream=s) for b in bufs]
+        assert all(st.graph for st in steps)
+        steps[0].wait()  # nothing in flight
+
+        def fill_and_launch(j, i):
+            h, lat, lg, ids, w = bufs[j]
+            h.copy_(src[i % 4])
+            lat.view(torch.int16).fill_(-1)
+            lg.fill_(float("nan"))
+            ids.fill_(-1)
+            w.fill_(float("nan"))
+            steps[j].launch()
+
+        n = 300
+        fill_and_launch(0, 0)
+        for i in range(n):
+            if i + 1 < n:
+                fill_and_launch((i + 1) % 2, i + 1)
+            steps[i % 2].wait()
+            check(i % 4, bufs[i % 2], i)
+        # two launches, one wait: the second launch's input
+        bufs[0][0].copy_(src[1])
+        steps[0].launch()
+        steps[0].wait()
+        bufs[0][0].copy_(src[2])
+        bufs[0][3].fill_(-1)
+        steps[0].launch()
+        steps[0].launch()
+        steps[0].wait()
+        check(2, bufs[0], n)
+        fill_and_launch(0, 3)  # the counts stay in step: the next wait is this launch's
+        steps[0].wait()
+        check(3, bufs[0], n + 1)
+        # a direct launch of A, then B as one graph call, then A's wait
+        fill_and_launch(0, 1)
+        bufs[1][0].copy_(src[2])
+        bufs[1][3].fill_(-1)
+        steps[1]()
+        check(2, bufs[1], n + 2)
+        steps[0].wait()
+        check(1, bufs[0], n + 3)
+        route.route_device_status(plan)
+        for st in steps:
+            st.close()
+
+
 @pytest.mark.parametrize("mode,rows,pinned", [(route.DECODE, 8, False), (route.PREFILL, 40, True)])
 def test_host_step_without_graph_runs_route_step_host(mode, rows, pinned):
     """Pageable buffers, or a prefill plan: HostStep calls route_step_host."""
