@@ -8,6 +8,9 @@
  *     within 5 FP32 ULP of the oracle's;
  *   - latent relative RMS error against the float64 sums <= 2e-3;
  *   - |logit - float64 sum| <= 2^-19 * sum_k |h * w| for every logit.
+ * Then two decode host steps of one plan on page-locked buffers, in flight
+ * together (route_host_step_launch / route_host_step_wait) on two inputs,
+ * each result equal bit for bit to route_step's on device buffers.
  * Inputs: a fixed 64-bit LCG, hidden ~ uniform(-1.7, 1.7) (about unit
  * variance), weights ~ uniform scaled to variance 1/7168, rounded to BF16.
  * Exit status 0 when every check passes. */
@@ -155,6 +158,109 @@ static int run_case(int mode, int R, const uint16_t *wl, const uint16_t *wr,
     return bad;
 }
 
+/* route_step on device buffers: the results copied back into `out`
+ * (latent, logits, ids, weights, packed in that order). */
+static int device_step(route_plan *plan, const uint16_t *h, int R, void *d_wl, void *d_wr,
+                       uint8_t *out) {
+    const size_t nh = sizeof(uint16_t) * (size_t)R * K, nl = sizeof(uint16_t) * (size_t)R * NL,
+                 ng = sizeof(float) * (size_t)R * NE, nk = sizeof(int32_t) * (size_t)R * TOPK;
+    void *d_h, *d_out;
+    CUDA_OK(cudaMalloc(&d_h, nh));
+    CUDA_OK(cudaMalloc(&d_out, nl + ng + 2 * nk));
+    CUDA_OK(cudaMemcpy(d_h, h, nh, cudaMemcpyHostToDevice));
+    uint8_t *o = d_out;
+    route_status st = route_step(plan, d_h, d_wl, d_wr, o, (float *)(o + nl), (int32_t *)(o + nl + ng),
+                                 (float *)(o + nl + ng + nk), NULL);
+    if (st == ROUTE_OK) CUDA_OK(cudaDeviceSynchronize());
+    if (st == ROUTE_OK) st = route_device_status(plan);
+    if (st != ROUTE_OK) {
+        fprintf(stderr, "route_step: status %d: %s\n", (int)st, route_last_error());
+        return 1;
+    }
+    CUDA_OK(cudaMemcpy(out, d_out, nl + ng + 2 * nk, cudaMemcpyDeviceToHost));
+    cudaFree(d_h);
+    cudaFree(d_out);
+    return 0;
+}
+
+/* Two host steps of one decode plan in flight together: launch A, launch B,
+ * wait A, check A, refill A, launch A, wait B, check B, wait A, check A. */
+static int run_host_steps(void *d_wl, void *d_wr) {
+    enum { R = 8 };
+    const size_t nh = sizeof(uint16_t) * (size_t)R * K, nl = sizeof(uint16_t) * (size_t)R * NL,
+                 ng = sizeof(float) * (size_t)R * NE, nk = sizeof(int32_t) * (size_t)R * TOPK,
+                 nout = nl + ng + 2 * nk;
+    uint16_t *h[2];
+    uint8_t *want[2];
+    route_plan *plan = NULL;
+    route_status st = route_prepare(ROUTE_DECODE, R, 0, &plan);
+    if (st != ROUTE_OK) {
+        fprintf(stderr, "host steps: prepare: %s\n", route_last_error());
+        return 1;
+    }
+    for (int i = 0; i < 2; ++i) {
+        h[i] = malloc(nh);
+        want[i] = malloc(nout);
+        fill(h[i], (size_t)R * K, 1.7320508);
+        if (device_step(plan, h[i], R, d_wl, d_wr, want[i])) return 1;
+    }
+    cudaStream_t s;
+    CUDA_OK(cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking));
+    uint16_t *hh[2];
+    uint8_t *out[2];
+    route_host_step *step[2];
+    for (int j = 0; j < 2; ++j) {
+        CUDA_OK(cudaHostAlloc((void **)&hh[j], nh, cudaHostAllocDefault));
+        CUDA_OK(cudaHostAlloc((void **)&out[j], nout, cudaHostAllocDefault));
+        uint8_t *o = out[j];
+        st = route_host_step_create(plan, hh[j], d_wl, d_wr, o, (float *)(o + nl),
+                                    (int32_t *)(o + nl + ng), (float *)(o + nl + ng + nk), s,
+                                    &step[j]);
+        if (st != ROUTE_OK) {
+            fprintf(stderr, "host steps: create: %s\n", route_last_error());
+            return 1;
+        }
+    }
+    /* launch A(0), launch B(1); wait A, check, A(1); wait B, check, B(0);
+     * wait A, check; wait B, check */
+    int in[2] = {0, 1}, bad = 0;
+    memcpy(hh[0], h[0], nh);
+    memcpy(hh[1], h[1], nh);
+    st = route_host_step_launch(step[0]);
+    if (st == ROUTE_OK) st = route_host_step_launch(step[1]);
+    for (int k = 0; k < 4 && st == ROUTE_OK; ++k) {
+        const int j = k % 2;
+        if ((st = route_host_step_wait(step[j])) != ROUTE_OK) break;
+        if (memcmp(out[j], want[in[j]], nout) != 0) {
+            fprintf(stderr, "host steps: wait %d (step %d, input %d) differs from route_step\n", k,
+                    j, in[j]);
+            bad = 1;
+            break;
+        }
+        if (k < 2) { /* the other input, launched behind the step still in flight */
+            in[j] = 1 - in[j];
+            memcpy(hh[j], h[in[j]], nh);
+            memset(out[j], 0xFF, nout);
+            st = route_host_step_launch(step[j]);
+        }
+    }
+    if (st != ROUTE_OK) {
+        fprintf(stderr, "host steps: status %d: %s\n", (int)st, route_last_error());
+        bad = 1;
+    }
+    for (int j = 0; j < 2; ++j) {
+        route_host_step_destroy(step[j]);
+        cudaFreeHost(hh[j]);
+        cudaFreeHost(out[j]);
+        free(h[j]);
+        free(want[j]);
+    }
+    route_destroy(plan);
+    cudaStreamDestroy(s);
+    if (!bad) printf("host steps, two in flight: ok\n");
+    return bad;
+}
+
 int main(void) {
     uint16_t *wl = malloc(sizeof(uint16_t) * (size_t)K * NL);
     uint16_t *wr = malloc(sizeof(uint16_t) * (size_t)K * NE);
@@ -170,6 +276,7 @@ int main(void) {
     CUDA_OK(cudaMemcpy(d_wr, wr, sizeof(uint16_t) * (size_t)K * NE, cudaMemcpyHostToDevice));
     int bad = run_case(ROUTE_DECODE, 8, wl, wr, d_wl, d_wr);
     bad |= run_case(ROUTE_PREFILL, 264, wl, wr, d_wl, d_wr);  /* two row blocks, ragged */
+    bad |= run_host_steps(d_wl, d_wr);
     cudaFree(d_wl);
     cudaFree(d_wr);
     free(wl);

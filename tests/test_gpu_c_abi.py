@@ -1,7 +1,8 @@
 """The C ABI from a plain C program (tests/c/route_abi_check.c): no Python
 binding and no PyTorch on the path, device memory from the CUDA runtime; one
 decode and one prefill step checked against the oracle, which the program
-links (test code only)."""
+links (test code only), and two host steps in flight together checked
+against route_step."""
 
 import os
 import subprocess
@@ -35,4 +36,5 @@ def test_plain_c_program_on_the_abi(tmp_path):
     assert res.returncode == 0, res.stderr[-3000:]
     run = subprocess.run([exe], capture_output=True, text=True, timeout=600)
     assert run.returncode == 0, run.stdout[-2000:] + run.stderr[-2000:]
-    assert "decode 8 rows: ok" in run.stdout and "prefill 264 rows: ok" in run.stdout, run.stdout
+    for line in ("decode 8 rows: ok", "prefill 264 rows: ok", "host steps, two in flight: ok"):
+        assert line in run.stdout, run.stdout
