@@ -200,7 +200,9 @@ route_status route_step_host(const route_plan *plan, const void *hidden_host,
  * one plan may be in flight together (a serving loop with two batches:
  * launch B, wait A, refill A, launch A, wait B, ...) when they were created
  * with the same stream: they share the plan's device scratch, and the
- * stream's order keeps them apart.  Both launch forms keep the plan's
+ * stream's order keeps them apart.  A launch or run while another step of
+ * the plan, created with another stream, has a launch in flight returns
+ * ROUTE_ERR_PLAN and launches nothing.  Both launch forms keep the plan's
  * settings (route_set_latent_ksplit) as they were at creation.  The step belongs to the plan: route_destroy releases its
  * graph, after which launch, wait and run return ROUTE_ERR_NULL.
  * route_host_step_destroy frees the step (NULL: no-op).  Steps and their

@@ -976,10 +976,23 @@ static route_status enqueue_host_step(route_host_step *step) {
     return ROUTE_OK;
 }
 
+// True when another step of the plan has a launch in flight on a stream
+// other than this step's: the two would share the plan's scratch unordered.
+static bool in_flight_elsewhere(const route_host_step *step) {
+    for (const route_host_step *o = step->plan->steps; o; o = o->next) {
+        if (o == step || o->stream == step->stream || !o->flag_host) continue;
+        const unsigned v = __atomic_load_n(o->flag_host, __ATOMIC_ACQUIRE);
+        if ((int)(v - o->launched) < 0) return true;
+    }
+    return false;
+}
+
 route_status route_host_step_launch(route_host_step *step) {
     g_err[0] = '\0';
     if (!step || !step->plan || !step->exec)
         return fail(ROUTE_ERR_NULL, "host step is NULL or its plan has been destroyed");
+    if (in_flight_elsewhere(step))
+        return fail(ROUTE_ERR_PLAN, "another step of this plan is in flight on another stream");
     DeviceGuard guard(step->plan->device);
     if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
     const route_status st = enqueue_host_step(step);
@@ -1027,6 +1040,8 @@ route_status route_host_step_run(route_host_step *step) {
     g_err[0] = '\0';
     if (!step || !step->plan || !step->exec)
         return fail(ROUTE_ERR_NULL, "host step is NULL or its plan has been destroyed");
+    if (in_flight_elsewhere(step))
+        return fail(ROUTE_ERR_PLAN, "another step of this plan is in flight on another stream");
     {
         DeviceGuard guard(step->plan->device);
         if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");

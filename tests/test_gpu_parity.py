@@ -616,6 +616,49 @@ def test_two_host_steps_in_flight_on_one_plan():
             st.close()
 
 
+def test_host_steps_on_two_streams_are_not_in_flight_together():
+    """Two HostSteps of one plan created with different streams would share the
+    plan's scratch unordered: while one has a launch in flight the other's
+    launch and call are refused (nothing launched), and once it is waited for
+    the other runs and gives route_step's bits."""
+    rows = 8
+    _, wl, wr = bank("decode_r8", 0)
+    dwl, dwr = to_dev_bf16(wl), to_dev_bf16(wr)
+    h = np.ascontiguousarray(np.resize(bank("decode_r8", 3)[0], (rows, route.K_HIDDEN)))
+    with route.Plan(route.DECODE, rows) as plan:
+        want = run_step(plan, to_dev_bf16(h), dwl, dwr)
+
+        def make(stream):
+            bufs = (torch.from_numpy(h.view(np.int16).copy()).view(torch.bfloat16).pin_memory(),
+                    torch.empty((rows, route.N_LATENT), dtype=torch.bfloat16).pin_memory(),
+                    torch.empty((rows, route.N_EXPERTS), dtype=torch.float32).pin_memory(),
+                    torch.empty((rows, route.TOPK), dtype=torch.int32).pin_memory(),
+                    torch.empty((rows, route.TOPK), dtype=torch.float32).pin_memory())
+            return bufs, route.HostStep(plan, bufs[0], dwl, dwr, *bufs[1:], stream=stream)
+
+        sa = torch.cuda.Stream()
+        (ba, a), (bb, b) = make(sa), make(torch.cuda.Stream())
+        assert a.graph and b.graph
+        with torch.cuda.stream(sa):
+            torch.cuda._sleep(20_000_000)  # A's launch stays in flight behind ~10 ms of spin
+        a.launch()
+        with pytest.raises(route.RouteError) as e1:
+            b.launch()
+        with pytest.raises(route.RouteError) as e2:
+            b()
+        assert e1.value.status == e2.value.status == 7  # ROUTE_ERR_PLAN
+        a.wait()
+        b.launch()
+        b.wait()
+        for bufs in (ba, bb):
+            assert np.array_equal(bufs[1].view(torch.int16).numpy().view(np.uint16), want[0])
+            assert np.array_equal(bufs[3].numpy(), want[2])
+            assert np.array_equal(bufs[4].numpy().view(np.uint32), want[3].view(np.uint32))
+        route.route_device_status(plan)
+        a.close()
+        b.close()
+
+
 @pytest.mark.parametrize("mode,rows,pinned", [(route.DECODE, 8, False), (route.PREFILL, 40, True)])
 def test_host_step_without_graph_runs_route_step_host(mode, rows, pinned):
     """Pageable buffers, or a prefill plan: HostStep calls route_step_host."""
