@@ -121,6 +121,11 @@ struct DecodeArgs {
     int32_t *ids;
     float *weights;
     float *sumsq;                // optional [rows]: sum of squares of each latent row
+    // With overlap set, hidden rows published by a concurrent staging kernel:
+    // the stream kernel reads them once *hidden_count >= hidden_target
+    // (acquire; null: no wait).
+    const unsigned *hidden_count = nullptr;
+    unsigned hidden_target = 0;
 };
 
 // Internal launchers (defined next to their kernels).  Every launch uses
@@ -145,6 +150,14 @@ cudaError_t decode_launch(int bn, const CUtensorMap &map_h, const CUtensorMap &m
 // kernels.
 cudaError_t stage_in_launch(const void *src_mapped, void *dst, size_t bytes, cudaStream_t stream);
 cudaError_t host_done_launch(unsigned *counter, unsigned *flag_mapped, cudaStream_t stream);
+// The same copy for a step whose stream kernel does not wait for it to
+// complete: it writes `dst` once *done_counter >= need (the buffer's last
+// reader has finished), then adds one per CTA to *published (release) and,
+// last, waits for its own predecessor.  *ctas receives the CTAs launched.
+cudaError_t stage_publish_launch(const void *src_mapped, void *dst, size_t bytes,
+                                 const unsigned *done_counter, unsigned need, unsigned *published,
+                                 unsigned *status, unsigned long long timeout_ns, int *ctas,
+                                 cudaStream_t stream);
 
 // The top-16 of each row; with `sumsq` non-null also the row's latent sum
 // of squares (the sum of its kSsParts parts in `ss_part`, which the same

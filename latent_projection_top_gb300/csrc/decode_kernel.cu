@@ -48,7 +48,9 @@
 // By default it reads the hidden rows only after the wait; with `overlap` set
 // it reads them at once and waits only before it writes scratch (at the end
 // of its stream), so one step's weight stream runs under the previous step's
-// finish kernel.
+// finish kernel.  Rows that a concurrent staging kernel publishes (a host
+// step launched behind another step) are read once a device counter says
+// they are all there.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -193,6 +195,21 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, const 
     }
 }
 
+// Rows published by a concurrent staging kernel (a host step launched behind
+// another step): wait until its CTAs have all published them (bounded: after
+// the timeout the status word records it and the stream goes on, its
+// outputs invalid), then order the acquire before this thread's TMA reads.
+__device__ __noinline__ void wait_published(const DecodeArgs &a) {
+    const uint64_t t0 = ptx::global_timer_ns();
+    while ((int)(ptx::ld_acquire_gpu(a.hidden_count) - a.hidden_target) < 0) {
+        if (ptx::global_timer_ns() - t0 > a.timeout_ns) {
+            atomicOr(&a.words[kWordStatus], kStatusTimeout);
+            break;
+        }
+    }
+    ptx::fence_proxy_async_global();
+}
+
 // Register caps (the most each variant compiles to without spilling) leave
 // room on every SM sub-partition for two warps of a finish CTA.
 template <int BN>
@@ -294,6 +311,8 @@ __global__ void __maxnreg__(BN == 16 ? 80 : 88)
             if (!args.overlap) {
                 prefetch_l2();
                 asm volatile("griddepcontrol.wait;" ::: "memory");
+            } else if (args.hidden_count != nullptr) {
+                wait_published(args);
             }
             for (int i = 0; i < n_pre; ++i) {
                 if (args.test_stall && i == n_units - 1) continue;  // test hook

@@ -73,6 +73,18 @@ struct route_host_step {
     // with this step's outputs filled in -- what the graph holds.
     const void *hidden_mapped, *W_latent, *W_router;
     route::DecodeArgs dec;
+    // Direct launches stage the hidden rows into two buffers of the step's
+    // own, alternately (hbuf, hbuf + hbuf_stride; hmap: their tensor maps),
+    // and publish them through the device word `published` (one addition
+    // per staging CTA; published_total: the sum after the last launch).
+    // buf_launch[j]: the number of the launch that last read buffer j.
+    uint8_t *hbuf;
+    size_t hbuf_stride;
+    CUtensorMap hmap[2];
+    unsigned *published;
+    unsigned published_total;
+    unsigned staged;
+    unsigned buf_launch[2];
 };
 
 namespace {
@@ -162,10 +174,13 @@ void release_step_graph(route_host_step *h) {
     if (h->graph) cudaGraphDestroy(h->graph);
     if (h->counter) cudaFree(h->counter);
     if (h->flag_host) cudaFreeHost(h->flag_host);
+    if (h->hbuf) cudaFree(h->hbuf);
     h->exec = nullptr;
     h->graph = nullptr;
     h->counter = nullptr;
     h->flag_host = h->flag_dev = nullptr;
+    h->hbuf = nullptr;
+    h->published = nullptr;
 }
 
 void free_plan(route_plan *p) {
@@ -917,6 +932,13 @@ route_status route_host_step_create(route_plan *plan, const void *hidden_host,
         *step->flag_host = 0u;
         e = cudaHostGetDevicePointer(reinterpret_cast<void **>(&step->flag_dev), step->flag_host, 0);
     }
+    // the direct launches' two staging buffers, then the `published` word
+    step->hbuf_stride = align256((size_t)plan->rows * kHidden * 2);
+    if (e == cudaSuccess) e = cudaMalloc(&step->hbuf, 2 * step->hbuf_stride + 256);
+    if (e == cudaSuccess) {
+        step->published = reinterpret_cast<unsigned *>(step->hbuf + 2 * step->hbuf_stride);
+        e = cudaMemset(step->published, 0, sizeof(unsigned));
+    }
     if (e == cudaSuccess) e = cudaDeviceSynchronize();  // the counter's zero is in place
     // Capture on a stream of our own: the caller's may be the legacy
     // default stream, which cannot be captured.
@@ -940,6 +962,14 @@ route_status route_host_step_create(route_plan *plan, const void *hidden_host,
         delete step;
         return st != ROUTE_OK ? st : cuda_fail(e, "capture the host step");
     }
+    for (int j = 0; j < 2 && st == ROUTE_OK; ++j)
+        st = encode_2d(&step->hmap[j], step->hbuf + j * step->hbuf_stride, kHidden,
+                       (uint64_t)plan->rows, kKBlock, (uint32_t)plan->bn, "hidden");
+    if (st != ROUTE_OK) {
+        release_step_graph(step);
+        delete step;
+        return st;
+    }
     step->hidden_mapped = h;
     step->W_latent = W_latent;
     step->W_router = W_router;
@@ -957,19 +987,41 @@ route_status route_host_step_create(route_plan *plan, const void *hidden_host,
     return ROUTE_OK;
 }
 
-// The graph's kernels launched one by one on the step's stream, each chained
-// to its predecessor by programmatic dependent launch (the staging kernel to
-// whatever precedes it there, typically another step's completion kernel).
+// The step's kernels launched one by one on its stream, each chained to its
+// predecessor by programmatic dependent launch: a staging kernel that copies
+// the hidden rows into the step's next buffer (once the launch that last read
+// that buffer has finished) and publishes them, the stream kernel in overlap
+// mode, which reads them as soon as they are published -- under the tail of
+// whatever precedes it on the stream, typically another step -- and writes
+// scratch only after that has finished, the finish kernel and the completion
+// kernel.
 static route_status enqueue_host_step(route_host_step *step) {
     const route_plan *p = step->plan;
-    const Staging d = staging_of(p);
-    cudaError_t e = stage_in_launch(step->hidden_mapped, d.hidden, (size_t)p->rows * kHidden * 2,
-                                    step->stream);
+    const unsigned launch = step->launched + 1u;
+    const int j = (int)(step->staged & 1u);
+    int ctas = 0;
+    cudaError_t e = stage_publish_launch(
+        step->hidden_mapped, step->hbuf + j * step->hbuf_stride, (size_t)p->rows * kHidden * 2,
+        step->counter, step->buf_launch[j], step->published, p->words, step->dec.timeout_ns, &ctas,
+        step->stream);
     if (e != cudaSuccess) return cuda_fail(e, "stage hidden rows");
-    CUtensorMap mh, ml, mr;
-    route_status st = encode_all(p, d.hidden, step->W_latent, step->W_router, &mh, &ml, &mr);
-    if (st != ROUTE_OK) return st;
-    if ((e = decode_launch(p->bn, mh, ml, mr, step->dec, 1, step->stream)) != cudaSuccess)
+    // the rows are on their way into buffer j: count them even if a launch
+    // below fails (the device adds them all the same)
+    step->published_total += (unsigned)ctas;
+    step->staged += 1u;
+    step->buf_launch[j] = launch;
+    CUtensorMap ml, mr;
+    route_status st;
+    if ((st = cached_map(p->map_wl, step->W_latent, (uint64_t)p->n_lat, kHidden, 64, kKBlock,
+                         "W_latent", &ml)) != ROUTE_OK ||
+        (st = cached_map(p->map_wr, step->W_router, (uint64_t)p->n_exp, kHidden, 64, kKBlock,
+                         "W_router", &mr)) != ROUTE_OK)
+        return st;
+    DecodeArgs a = step->dec;
+    a.overlap = 1;
+    a.hidden_count = step->published;
+    a.hidden_target = step->published_total;
+    if ((e = decode_launch(p->bn, step->hmap[j], ml, mr, a, 1, step->stream)) != cudaSuccess)
         return cuda_fail(e, "decode kernel launch");
     if ((e = host_done_launch(step->counter, step->flag_dev, step->stream)) != cudaSuccess)
         return cuda_fail(e, "completion kernel launch");
