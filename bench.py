@@ -14,8 +14,8 @@ The other row counts (1, 9, 12, 16, 20 decode; 1024 and 3072 prefill, the
 latter per 92-layer chunk) are measured the same way and reported under
 "sweep".  `e2e` repeats the headline through the host-buffer call (hidden
 rows read from pinned host memory and all results written back to it, every
-step): two `HostStep`s (the checked-once form of route_step_host) of one
-plan with two batches in flight, with one in flight and the plain
+step): three `HostStep`s (the checked-once form of route_step_host) of one
+plan with three batches in flight, with one and two in flight and the plain
 route_step_host call timed beside it.
 `cpu_baseline` times the oracle on the host cores on a bounded sample.
 
@@ -611,20 +611,21 @@ class RouteBench:
                     torch.empty((rows, route.TOPK), dtype=torch.int32).pin_memory(),
                     torch.empty((rows, route.TOPK), dtype=torch.float32).pin_memory())
 
-        (hid, lat, lg, ids, w), other = host_bufs(0), host_bufs(1)
+        (hid, lat, lg, ids, w), others = host_bufs(0), [host_bufs(b) for b in (1, 2)]
         s = torch.cuda.Stream(device=self.dev)
         with route.Plan(mode, rows, self.device) as plan:
             # route_step_host checks its tensors on every call; HostStep (the
             # serving-loop form of the same call) checks them once and launches
-            # a captured graph; two HostSteps on their own buffers keep two
-            # batches in flight
+            # a captured graph; HostSteps on buffers of their own keep several
+            # batches in flight through launch / wait
             step = route.HostStep(plan, hid, wl, wr, lat, lg, ids, w, stream=s)
-            step_b = route.HostStep(plan, other[0], wl, wr, *other[1:], stream=s)
-            pair = (step, step_b)
+            ring = [step] + [route.HostStep(plan, o[0], wl, wr, *o[1:], stream=s) for o in others]
             for _ in range(5):
                 route.route_step_host(plan, hid, wl, wr, lat, lg, ids, w, stream=s)
-                step()
-                step_b()
+                for st in ring:
+                    st()
+                    st.launch()
+                    st.wait()
             dist.barrier()
             torch.cuda.synchronize(self.dev)
             t0 = time.perf_counter()
@@ -639,29 +640,37 @@ class RouteBench:
                 step()
             torch.cuda.synchronize(self.dev)
             t_sync = time.perf_counter() - t0
+            by_depth = {}
+            for depth in (2, 3):
+                dist.barrier()
+                torch.cuda.synchronize(self.dev)
+                t0 = time.perf_counter()
+                for i in range(depth - 1):
+                    ring[i].launch()
+                for i in range(k):
+                    if i + depth - 1 < k:
+                        ring[(i + depth - 1) % depth].launch()
+                    ring[i % depth].wait()
+                torch.cuda.synchronize(self.dev)
+                by_depth[depth] = dist.max(time.perf_counter() - t0)
             dist.barrier()
-            torch.cuda.synchronize(self.dev)
-            t0 = time.perf_counter()
-            pair[0].launch()
-            for i in range(k):
-                if i + 1 < k:
-                    pair[(i + 1) % 2].launch()
-                pair[i % 2].wait()
-            torch.cuda.synchronize(self.dev)
-            t = time.perf_counter() - t0
-            dist.barrier()
-        t, t_sync, t_checked = dist.max(t), dist.max(t_sync), dist.max(t_checked)
+        t_sync, t_checked = dist.max(t_sync), dist.max(t_checked)
+        depth = E2E_DEPTH
+        t = by_depth[depth]
         h2d = hid.numel() * 2
         d2h = lat.numel() * 2 + lg.numel() * 4 + ids.numel() * 4 + w.numel() * 4
         return {"value": round(dist.world * k * rows / t, 1), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "us_per_step": round(t / k * 1e6, 3), "steps": k,
-                "path": "two HostSteps of one plan on one stream, each on its own pinned host "
-                        "buffers (route_step_host's copy-free path, prepared once as a CUDA "
-                        "graph): launch B, wait A, launch A, wait B, ...; every step reads its "
+                "us_per_step": round(t / k * 1e6, 3), "steps": k, "in_flight": depth,
+                "path": f"{depth} HostSteps of one plan on one stream, each on its own pinned "
+                        f"host buffers, launched and waited for in turn with {depth} batches in "
+                        "flight (launch C, wait A, launch A, wait B, ...); every step reads its "
                         "hidden rows from host memory and its wait returns once that step's "
                         "results are in its host buffers",
-                "us_per_step_one_in_flight": round(t_sync / k * 1e6, 3),
+                "us_per_step_by_in_flight": {"1 (HostStep call, CUDA graph)":
+                                             round(t_sync / k * 1e6, 3),
+                                             **{str(d): round(v / k * 1e6, 3)
+                                                for d, v in by_depth.items()}},
                 "us_per_step_route_step_host": round(t_checked / k * 1e6, 3)}
 
 
@@ -828,6 +837,9 @@ def summarise(us):
             "max": round(srt[-1], 3), "runs": len(srt)}
 
 
+# batches in flight in the e2e figure: with three the host's launches set the
+# pace (two leave the device idle between steps)
+E2E_DEPTH = 3
 DECODE_SPREAD = dict(runs=5, replays=200, graph_len=GRAPH_LEN)
 PREFILL_SPREAD = dict(runs=5, replays=10, graph_len=92)
 SPREAD_METHOD = ("per-layer us: median (min, max) over 5 runs; decode: 200 replays of a "

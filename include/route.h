@@ -183,13 +183,15 @@ route_status route_step_host(const route_plan *plan, const void *hidden_host,
  * kernel that, once they have finished, stores the step's number into a
  * page-locked completion word after a system-scope fence.
  * route_host_step_run is one graph launch on `stream` and a wait (below).
- * route_host_step_launch enqueues the same kernels with the same arguments
- * one by one on `stream` and returns at once: unlike a graph launch, which
- * starts once everything before it on the stream has finished, the staging
- * kernel is chained to its predecessor by programmatic dependent launch, so
- * that a step launched behind another one reads its hidden rows and starts
- * streaming weights under the other's tail (it writes the plan's scratch
- * only once the other has finished).
+ * route_host_step_launch enqueues the step's kernels one by one on `stream`
+ * and returns at once: unlike a graph launch, which starts once everything
+ * before it on the stream has finished, they are chained to their
+ * predecessor by programmatic dependent launch.  Its staging kernel copies
+ * the hidden rows into one of two device buffers of the step's own
+ * (alternate launches) and publishes them through a device counter, so that
+ * a step launched behind another one streams its weights and reads its rows
+ * under the other's tail (it writes the plan's scratch only once the other
+ * has finished).
  * route_host_step_wait waits for the number of the step's latest launch in
  * the completion word (not for the stream: the last kernel may still be
  * leaving when it returns) and returns after that launch's results are in

@@ -479,9 +479,9 @@ class HostStep:
     (``route_host_step_launch`` / ``route_host_step_wait``) so that two
     steps of one plan, created on the same stream, can be in flight together:
     launch B, wait A, refill A, launch A, wait B, ...  ``launch()`` enqueues
-    the graph's kernels directly, chained to the step before it on the
-    stream, so that the next step's weights stream in under that step's
-    tail.  Between a step's launch and its wait its hidden buffer is not
+    the step's kernels directly, chained to the step before it on the
+    stream, so that its weights stream in, and its published rows are read,
+    under that step's tail.  Between a step's launch and its wait its hidden buffer is not
     written and its results are not read.  Without a graph, ``launch()``
     runs the whole step and ``wait()`` returns at once.
     """

@@ -536,10 +536,12 @@ def test_host_step_results_visible_on_return_many_steps():
         step.close()
 
 
-def test_two_host_steps_in_flight_on_one_plan():
-    """Two HostSteps of one plan on one stream, pipelined: step A is launched,
-    then B is filled and launched before A is waited for, and so on for 300
-    steps over four inputs; each wait is followed by a check of that step's
+@pytest.mark.parametrize("depth", [2, 3])
+def test_host_steps_in_flight_on_one_plan(depth):
+    """`depth` HostSteps of one plan on one stream, pipelined: step A is
+    launched, then B (and C) are filled and launched before A is waited for,
+    and so on for 300 steps over five inputs (so that a step's next input
+    differs from its last); each wait is followed by a check of that step's
     host buffers against route_step's bits for its input.  Also: a wait with
     nothing in flight returns at once; after two launches and one wait the
     next launch and wait give that launch's results; a graph call of B behind
@@ -548,7 +550,7 @@ def test_two_host_steps_in_flight_on_one_plan():
     _, wl, wr = bank("decode_r8", 0)
     dwl, dwr = to_dev_bf16(wl), to_dev_bf16(wr)
     hs = [np.ascontiguousarray(np.resize(bank("decode_r8", b)[0], (rows, route.K_HIDDEN)))
-          for b in range(4)]
+          for b in range(5)]
     s = torch.cuda.Stream()
 
     def host_bufs():
@@ -569,14 +571,14 @@ def test_two_host_steps_in_flight_on_one_plan():
     with route.Plan(route.DECODE, rows) as plan:
         want = [run_step(plan, to_dev_bf16(h), dwl, dwr) for h in hs]
         src = [torch.from_numpy(h.view(np.int16).copy()).view(torch.bfloat16) for h in hs]
-        bufs = [host_bufs(), host_bufs()]
+        bufs = [host_bufs() for _ in range(depth)]
         steps = [route.HostStep(plan, b[0], dwl, dwr, *b[1:], stream=s) for b in bufs]
         assert all(st.graph for st in steps)
         steps[0].wait()  # nothing in flight
 
         def fill_and_launch(j, i):
             h, lat, lg, ids, w = bufs[j]
-            h.copy_(src[i % 4])
+            h.copy_(src[i % 5])
             lat.view(torch.int16).fill_(-1)
             lg.fill_(float("nan"))
             ids.fill_(-1)
@@ -584,12 +586,13 @@ def test_two_host_steps_in_flight_on_one_plan():
             steps[j].launch()
 
         n = 300
-        fill_and_launch(0, 0)
+        for i in range(depth - 1):
+            fill_and_launch(i, i)
         for i in range(n):
-            if i + 1 < n:
-                fill_and_launch((i + 1) % 2, i + 1)
-            steps[i % 2].wait()
-            check(i % 4, bufs[i % 2], i)
+            if i + depth - 1 < n:
+                fill_and_launch((i + depth - 1) % depth, i + depth - 1)
+            steps[i % depth].wait()
+            check(i % 5, bufs[i % depth], i)
         # two launches, one wait: the second launch's input
         bufs[0][0].copy_(src[1])
         steps[0].launch()
