@@ -536,8 +536,8 @@ def test_host_step_results_visible_on_return_many_steps():
         step.close()
 
 
-@pytest.mark.parametrize("depth", [2, 3])
-def test_host_steps_in_flight_on_one_plan(depth):
+@pytest.mark.parametrize("depth,rows", [(2, 8), (3, 8), (3, 20), (2, 1)])
+def test_host_steps_in_flight_on_one_plan(depth, rows):
     """`depth` HostSteps of one plan on one stream, pipelined: step A is
     launched, then B (and C) are filled and launched before A is waited for,
     and so on for 300 steps over five inputs (so that a step's next input
@@ -545,8 +545,8 @@ def test_host_steps_in_flight_on_one_plan(depth):
     host buffers against route_step's bits for its input.  Also: a wait with
     nothing in flight returns at once; after two launches and one wait the
     next launch and wait give that launch's results; a graph call of B behind
-    a direct launch of A gives both steps' results."""
-    rows = 8
+    a direct launch of A gives both steps' results.  At 20 rows the staging
+    kernel publishes from seven CTAs and the stream kernel takes 32-row MMAs."""
     _, wl, wr = bank("decode_r8", 0)
     dwl, dwr = to_dev_bf16(wl), to_dev_bf16(wr)
     hs = [np.ascontiguousarray(np.resize(bank("decode_r8", b)[0], (rows, route.K_HIDDEN)))
