@@ -837,8 +837,8 @@ def summarise(us):
             "max": round(srt[-1], 3), "runs": len(srt)}
 
 
-# batches in flight in the e2e figure: with three the host's launches set the
-# pace (two leave the device idle between steps)
+# batches in flight in the e2e figure: three keep the device busy (two leave
+# it idle between steps, a step's own latency being about 25 us)
 E2E_DEPTH = 3
 DECODE_SPREAD = dict(runs=5, replays=200, graph_len=GRAPH_LEN)
 PREFILL_SPREAD = dict(runs=5, replays=10, graph_len=92)
