@@ -178,7 +178,9 @@ route_status route_step_host(const route_plan *plan, const void *hidden_host,
  * route_host_step_create takes the arguments of route_step_host.  Decode
  * plans with every host buffer page-locked and 16-byte aligned only (the
  * path that copies nothing); otherwise ROUTE_ERR_PLAN, and the caller uses
- * route_step_host.  The staging, stream and finish kernels are captured once
+ * route_step_host.  A step holds, besides its graph, two device buffers of
+ * the hidden rows (2 x rows x 14,336 bytes) and a few device and page-locked
+ * words, until route_host_step_destroy or the plan's route_destroy.  The staging, stream and finish kernels are captured once
  * into a CUDA graph (on a stream of the step's own), with a last one-thread
  * kernel that, once they have finished, stores the step's number into a
  * page-locked completion word after a system-scope fence.
