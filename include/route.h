@@ -180,10 +180,11 @@ route_status route_step_host(const route_plan *plan, const void *hidden_host,
  * path that copies nothing); otherwise ROUTE_ERR_PLAN, and the caller uses
  * route_step_host.  A step holds, besides its graph, two device buffers of
  * the hidden rows (2 x rows x 14,336 bytes) and a few device and page-locked
- * words, until route_host_step_destroy or the plan's route_destroy.  The staging, stream and finish kernels are captured once
- * into a CUDA graph (on a stream of the step's own), with a last one-thread
- * kernel that, once they have finished, stores the step's number into a
- * page-locked completion word after a system-scope fence.
+ * words, until route_host_step_destroy or the plan's route_destroy.  The
+ * staging, stream and finish kernels are captured once into a CUDA graph (on
+ * a stream of the step's own), with a last one-thread kernel that, once they
+ * have finished, stores the step's number into a page-locked completion word
+ * after a system-scope fence.
  * route_host_step_run is one graph launch on `stream` and a wait (below).
  * route_host_step_launch enqueues the step's kernels one by one on `stream`
  * and returns at once: unlike a graph launch, which starts once everything
@@ -207,8 +208,9 @@ route_status route_step_host(const route_plan *plan, const void *hidden_host,
  * stream's order keeps them apart.  A launch or run while another step of
  * the plan, created with another stream, has a launch in flight returns
  * ROUTE_ERR_PLAN and launches nothing.  Both launch forms keep the plan's
- * settings (route_set_latent_ksplit) as they were at creation.  The step belongs to the plan: route_destroy releases its
- * graph, after which launch, wait and run return ROUTE_ERR_NULL.
+ * settings (route_set_latent_ksplit) as they were at creation.  The step
+ * belongs to the plan: route_destroy releases its graph and buffers, after
+ * which launch, wait and run return ROUTE_ERR_NULL.
  * route_host_step_destroy frees the step (NULL: no-op).  Steps and their
  * plan are not thread-safe.
  */
