@@ -619,6 +619,56 @@ def test_host_steps_in_flight_on_one_plan(depth, rows):
             st.close()
 
 
+def test_host_step_keeps_the_ksplit_setting_of_its_creation():
+    """A HostStep created while the plan computes the K-split latent keeps
+    that arithmetic after the plan is switched back, in both launch forms
+    (the graph call and the direct launch), and a step created afterwards
+    gives the full-K bits: each equal to route_step's under the same setting."""
+    rows = 8
+    _, wl, wr = bank("decode_r8", 0)
+    dwl, dwr = to_dev_bf16(wl), to_dev_bf16(wr)
+    h = np.ascontiguousarray(np.resize(bank("decode_r8", 2)[0], (rows, route.K_HIDDEN)))
+    dh = to_dev_bf16(h)
+
+    def host_bufs():
+        return (torch.from_numpy(h.view(np.int16).copy()).view(torch.bfloat16).pin_memory(),
+                torch.empty((rows, route.N_LATENT), dtype=torch.bfloat16).pin_memory(),
+                torch.empty((rows, route.N_EXPERTS), dtype=torch.float32).pin_memory(),
+                torch.empty((rows, route.TOPK), dtype=torch.int32).pin_memory(),
+                torch.empty((rows, route.TOPK), dtype=torch.float32).pin_memory())
+
+    def same(bufs, want):
+        return (np.array_equal(bufs[1].view(torch.int16).numpy().view(np.uint16), want[0]) and
+                np.array_equal(bufs[2].numpy().view(np.uint32), want[1].view(np.uint32)) and
+                np.array_equal(bufs[3].numpy(), want[2]) and
+                np.array_equal(bufs[4].numpy().view(np.uint32), want[3].view(np.uint32)))
+
+    with route.Plan(route.DECODE, rows) as plan:
+        full = run_step(plan, dh, dwl, dwr)
+        route.route_set_latent_ksplit(plan, True)
+        ks = run_step(plan, dh, dwl, dwr)
+        assert not np.array_equal(full[0], ks[0])  # the two arithmetics differ here
+        ba = host_bufs()
+        a = route.HostStep(plan, ba[0], dwl, dwr, *ba[1:])
+        route.route_set_latent_ksplit(plan, False)
+        bb = host_bufs()
+        b = route.HostStep(plan, bb[0], dwl, dwr, *bb[1:])
+        a()
+        assert same(ba, ks)
+        ba[1].view(torch.int16).fill_(-1)
+        a.launch()
+        a.wait()
+        assert same(ba, ks)
+        b.launch()
+        b.wait()
+        assert same(bb, full)
+        b()
+        assert same(bb, full)
+        route.route_device_status(plan)
+        a.close()
+        b.close()
+
+
 def test_host_steps_on_two_streams_are_not_in_flight_together():
     """Two HostSteps of one plan created with different streams would share the
     plan's scratch unordered: while one has a launch in flight the other's
