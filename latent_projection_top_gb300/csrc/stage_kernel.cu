@@ -1,6 +1,7 @@
 // Copy of one step's hidden rows from page-locked host memory (read by the
 // GPU over its host link through the mapped address) into the plan's device
-// staging buffer, for route_step_host.  Launched with programmatic dependent
+// staging buffer, for route_step_host and a host step's graph, and the
+// completion kernel of a host step.  Launched with programmatic dependent
 // launch like the route kernels: it lets the next kernel launch at once (the
 // decode stream kernel then prefetches its weights while this copy runs) and
 // writes the staging buffer only after its own predecessor has completed.
